@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 W4A4 small-M decode projection on GB300.
+
+Metric: small-M NVFP4 GEMV us/call and achieved HBM GB/s (% of peak), M=1..8,
+Qwen3 shapes.  One step = for M in 1..8, for each Qwen3-32B projection (qkv,
+o, gate_up, down): quantize a fresh BF16 activation [M, K] to NVFP4 on the GPU
+and run the small-M GEMV against resident NVFP4 weights -- 32 quantize+GEMV
+calls streaming 2.3 GB of weights.  Between two uses of one weight matrix the
+step streams >= 245 MB of other weights, more than the 129 MB L2, so every
+call reads its weights from HBM (no flush kernel needed).
+
+value = algorithmic HBM bytes of the step (weight codes + scales, activation
+in/out, outputs) / device time of the step, in GB/s.  The step is captured
+once into a CUDA graph and replayed; events around every call give per-call
+GEMV times for the roofline.  `e2e` repeats the step through the eager C-ABI
+calls with the activations copied from pinned host memory and the outputs
+copied back inside the timed region.
+
+Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+(for N > 1 under torch.distributed.run: N independent replicas, weak scaling).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_w4a4_decode_gemv_gb300 import synth  # noqa: E402
+
+METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Qwen3 shapes"
+WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8])}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3-32b", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if not self.uuid.startswith("GPU-"):
+                self.uuid = "GPU-" + self.uuid
+        except Exception:
+            pass
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.uuid:
+                cmd.insert(1, f"--id={self.uuid}")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[1].isdigit():
+                    rows.append(p)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace('.', '').isdigit())}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+def build_problem(shapes, Ms, rank):
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    dev = torch.device("cuda")
+    weights = {}
+    for i, (name, K, N) in enumerate(shapes):
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 + i)
+        wb = (torch.randn((N, K), generator=g, device=dev, dtype=torch.float32) * synth.W_STD).to(torch.bfloat16)
+        weights[name] = api.nvfp4_quantize_act(wb)
+        del wb
+    calls = []
+    for M in Ms:
+        for i, (name, K, N) in enumerate(shapes):
+            x = synth.activations(M, K, seed=100 * M + i).to(dev)
+            calls.append(dict(M=M, name=name, K=K, N=N, x=x, xq=api.NVFP4Tensor.empty(M, K, dev),
+                              y=torch.empty((M, N), dtype=torch.float32, device=dev),
+                              gemv_bytes=synth.gemv_bytes(M, N, K), q_bytes=synth.quantize_bytes(M, K)))
+    ws_bytes = max(api.nvfp4_gemv_workspace_bytes(c["M"], c["N"], c["K"]) for c in calls)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    return weights, calls, ws
+
+
+def run_ours(args, world, rank):
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    shapes, Ms = WORKLOADS[args.workload]
+    weights, calls, ws = build_problem(shapes, Ms, rank)
+
+    def one_step(evs=None):
+        for j, c in enumerate(calls):
+            if evs is not None:
+                evs[j][0].record()
+            api.nvfp4_quantize_act(c["x"], out=c["xq"])
+            if evs is not None:
+                evs[j][1].record()
+            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            if evs is not None:
+                evs[j][2].record()
+
+    one_step()                       # initialises kernel attributes outside capture
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in calls] for _ in range(args.steps)]
+    g_warm, g_main = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_warm, stream=stream):
+            for _ in range(args.warmup):
+                one_step()
+        with torch.cuda.graph(g_main, stream=stream):
+            for k in range(args.steps):
+                one_step(evs[k])
+    torch.cuda.synchronize()
+    g_warm.replay()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0.record()
+        g_main.replay()
+        t1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(world, t0.elapsed_time(t1))
+    clocks = clk.summary()
+
+    step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
+    value_gbs = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    per_call = {}
+    gemv_ms_total = 0.0
+    gemv_bytes_total = 0
+    for j, c in enumerate(calls):
+        g_ms = [evs[k][j][1].elapsed_time(evs[k][j][2]) for k in range(args.steps)]
+        q_ms = [evs[k][j][0].elapsed_time(evs[k][j][1]) for k in range(args.steps)]
+        gm = float(np.mean(g_ms))
+        gemv_ms_total += gm
+        gemv_bytes_total += c["gemv_bytes"]
+        per_call[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(gm * 1e3, 2), "quant_us": round(float(np.mean(q_ms)) * 1e3, 2),
+                                              "gemv_gbs": round(c["gemv_bytes"] / (gm * 1e-3) / 1e9, 1)}
+    peak, peak_kind = measured_peaks()
+    achieved = gemv_bytes_total / (gemv_ms_total * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3/16 x fp32) w4a4, fp32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights; N(0,1) activations with 1% x20 outlier channels)",
+        "config": {"workload": f"{args.workload} decode projections qkv/o/gate_up/down, M={Ms[0]}..{Ms[-1]}, "
+                               f"quantize+GEMV per call",
+                   "calls_per_step": len(calls), "weights_resident_gb": round(sum(
+                       w.codes.numel() + w.scales.numel() for w in weights.values()) / 1e9, 3),
+                   "l2": "inputs larger than L2: >=245 MB of other weights between two uses of one matrix",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "nvfp4_gemv_smallm (prep + gemv), algorithmic bytes / per-call event time",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "clocks": clocks,
+        "gpu_launches": len(calls) * 3 * args.steps,
+        "per_call": per_call,
+    }
+    return result, calls, weights, ws
+
+
+def run_e2e(args, calls, weights, ws):
+    """Same step through the eager API, activations from pinned host memory and outputs back."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    host_x = [c["x"].cpu().pin_memory() for c in calls]
+    host_y = [torch.empty(c["y"].shape, dtype=torch.float32).pin_memory() for c in calls]
+    dev_x = [torch.empty_like(c["x"]) for c in calls]
+
+    def step():
+        for j, c in enumerate(calls):
+            dev_x[j].copy_(host_x[j], non_blocking=True)
+            api.nvfp4_quantize_act(dev_x[j], out=c["xq"])
+            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            host_y[j].copy_(c["y"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
+    return {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms / args.steps, 4),
+            "h2d_bytes_per_step": int(sum(c["x"].numel() * 2 for c in calls)),
+            "d2h_bytes_per_step": int(sum(c["y"].numel() * 4 for c in calls))}
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_sample(args, seconds):
+    """The oracle as it stands, on the host: per call, quantize the activation
+    and multiply against a sample of pre-quantized weight rows (FP64 dequant +
+    matmul), cycling through the workload's (M, projection) calls until about
+    `seconds` of CPU time.  Returns (GB/s of algorithmic bytes, sample text, threads)."""
+    from oracle import nvfp4 as Q
+    shapes, Ms = WORKLOADS[args.workload]
+    rows = 128
+    prepared = {}
+    for i, (name, K, N) in enumerate(shapes):
+        w = synth.weights(rows, K, seed=1000 + i)
+        prepared[name] = Q.quantize_bf16(synth.bf16_bits(w))
+    xs = {(M, name): synth.bf16_bits(synth.activations(M, K, seed=100 * M + i))
+          for M in Ms for i, (name, K, N) in enumerate(shapes)}
+    done_bytes, calls = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for M in Ms:
+            for name, K, N in shapes:
+                xq, xsc, xg = Q.quantize_bf16(xs[(M, name)])
+                wq, wsc, wg = prepared[name]
+                Q.gemv(xq, xsc, xg, wq, wsc, wg)
+                done_bytes += synth.gemv_bytes(M, rows, K) + synth.quantize_bytes(M, K)
+                calls += 1
+    dt = time.perf_counter() - t0
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        threads = max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        pass
+    sample = (f"{calls} calls of the {args.workload} sweep (M={Ms[0]}..{Ms[-1]} x 4 projections), each: oracle "
+              f"quantize of the BF16 activation + FP64 GEMV against {rows} pre-quantized weight rows; {dt:.1f} s")
+    return done_bytes / dt / 1e9, sample, threads, dt
+
+
+def main():
+    args = parse()
+    world, rank = dist_setup(args)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, sample, threads, dt = cpu_oracle_sample(args, seconds=max(5.0, min(60.0, args.cpu_seconds)))
+        _, Ms = WORKLOADS[args.workload]
+        line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64 (oracle: FP32 quantize recipe, FP64 dequant and dot)",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": f"{args.workload} decode projections qkv/o/gate_up/down, M={Ms[0]}..{Ms[-1]}, "
+                                       f"quantize+GEMV per call"},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    result, calls, weights, ws = run_ours(args, world, rank)
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, calls, weights, ws)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            gbs, sample, threads, _ = cpu_oracle_sample(args, seconds=args.cpu_seconds)
+            result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                      "sample": sample}
+        print(json.dumps(result))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

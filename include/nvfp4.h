@@ -1,0 +1,219 @@
+/*
+ * nvfp4.h -- C ABI of the NVFP4 W4A4 small-M decode library for GB300 (sm_103a).
+ *
+ * What it computes (the ReSET pages):
+ *   - NVFP4 = E2M1 4-bit elements, one E4M3 scale per 16 consecutive elements
+ *     along K, one FP32 global scale per tensor (ReSET reading note, §2.1;
+ *     §6.1 setup: "E2M1 elements, E4M3 block scales, group size 16").
+ *   - The small-M decode projection Y = dequant(Xq) . dequant(Wq)^T for
+ *     M = 1..8 active tokens, computed without a 128-row tensor-core tile
+ *     (ReSET project page, "Why a CUDA-core NVFP4 kernel?" and "Core
+ *     contribution -- the nvfp4r CUDA-core kernel", design choices C1-C3).
+ *   - The ReSET step-aware temperature sampler: token entropy, online step
+ *     entropy estimate (HSE), step-aware threshold (SAT), two-temperature
+ *     sample (project page, "Step-aware temperature scaling"; reading note
+ *     §3.1, §4.1-§4.3).
+ *
+ * Conventions for every entry point:
+ *   - Data pointers are DEVICE pointers owned by the caller; the library keeps
+ *     no reference after the call returns and allocates nothing.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *     may be captured into a CUDA graph, except where a function says otherwise.
+ *   - Argument errors are reported synchronously, before anything is launched:
+ *     NVFP4_ERR_NULL, NVFP4_ERR_SHAPE, NVFP4_ERR_ALIGN, NVFP4_ERR_RANGE.
+ *     A failed launch returns NVFP4_ERR_CUDA; nvfp4_last_cuda_error() names it.
+ *   - Tensors are row-major and dense.  NVFP4 tensor layout:
+ *       codes  uint8 [rows, K/2]  element 2j in the low nibble of byte j,
+ *                                 element 2j+1 in the high nibble;
+ *       scales uint8 [rows, K/16] E4M3 (OCP "fn") scale of elements 16b..16b+15,
+ *                                 not interleaved;
+ *       global float (one, on the device) -- dequant: x = e2m1(c) * e4m3(s) * global.
+ *   - Calls on distinct streams are independent, except where a function
+ *     says that concurrent calls share a buffer.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,   /* a required pointer is NULL */
+  NVFP4_ERR_SHAPE = 2,  /* a size is negative, too large or not a required multiple */
+  NVFP4_ERR_ALIGN = 3,  /* a pointer is not aligned as the function requires */
+  NVFP4_ERR_RANGE = 4,  /* a parameter value is out of range (M, temperatures, w, ...) */
+  NVFP4_ERR_CUDA = 5,   /* a CUDA runtime call or a kernel launch failed */
+  NVFP4_ERR_DEVICE = 6  /* the current device is not a Blackwell sm_100-family GPU */
+} nvfp4_status;
+
+/* Static string for a status code. */
+const char* nvfp4_status_str(nvfp4_status s);
+
+/* Text of the last CUDA error seen by this library in the calling thread (static storage). */
+const char* nvfp4_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int nvfp4_version(void);
+
+/*
+ * Reads and clears the device error word of the current device.  A kernel sets
+ * it (non-zero) when one of its bounded waits on an mbarrier gave up; the
+ * kernel then returned early and its outputs are incomplete.  Synchronous
+ * (it copies 4 bytes from the device); not for use inside stream capture.
+ */
+nvfp4_status nvfp4_device_status(unsigned int* code);
+
+/* ------------------------------------------------------------------------ */
+/* Quantizer: BF16 -> NVFP4                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * Quantizes x[rows, K] (BF16 bit patterns) by the NVFP4 two-level recipe, all
+ * in FP32 with IEEE rounding at each step:
+ *   amax = max|x| over the whole tensor; global = amax / 2688 (448 * 6);
+ *   per 16-element block: s = E4M3_rne_satfinite(max|x_block| / (6 * global));
+ *   per element: code = E2M1_rne_satfinite(x / (e4m3(s) * global)).
+ * The sign bit of each code is the sign bit of x (a negative value that rounds
+ * to zero gives 0x8).  When e4m3(s) * global is 0 (all-zero block, a scale that
+ * underflows, all-zero tensor) the code is the sign bit alone.
+ * Format: ReSET reading note §2.1 and §6.1; the pages' activation quantizer
+ * "Q" with a non-interleaved scale layout: reading note §5.3 (Table 3).
+ *
+ *   x_bf16   device, [rows, K] BF16, 16-byte aligned
+ *   rows     >= 0 (activations: the M tokens; weights: N output channels)
+ *   K        >= 0, multiple of 16
+ *   codes    device, [rows, K/2], 16-byte aligned            (written)
+ *   scales   device, [rows, K/16], 4-byte aligned            (written)
+ *   global   device, one float, 4-byte aligned               (written)
+ * Inputs with NaN or Inf are outside the contract (results unspecified).
+ * rows == 0 or K == 0 writes global = 0.
+ */
+nvfp4_status nvfp4_quantize_act(const uint16_t* x_bf16, int rows, int K, uint8_t* codes,
+                                uint8_t* scales, float* global_scale, cudaStream_t stream);
+
+/*
+ * Same recipe on FP32 input rows that are first rounded to BF16 (RNE): the
+ * values quantized are exactly those nvfp4_quantize_act would see after a
+ * FP32->BF16 cast.  Row r of the input starts at x + r * ld (ld >= K, in
+ * floats), so a column slice [0, K) of a wider matrix can be quantized in
+ * place (the decode step feeds the query columns of the qkv output to the o
+ * projection this way).  x 16-byte aligned, ld a multiple of 4.
+ */
+nvfp4_status nvfp4_quantize_f32(const float* x, int rows, int K, int ld, uint8_t* codes,
+                                uint8_t* scales, float* global_scale, cudaStream_t stream);
+
+/*
+ * SiLU(gate) * up on FP32 gate_up[rows, 2*I] (gate = columns [0, I), up =
+ * columns [I, 2I)), each product computed in FP32 and rounded to BF16, then
+ * quantized by the recipe above into codes[rows, I/2], scales[rows, I/16].
+ * I a multiple of 16; gate_up 16-byte aligned.  (The MLP of the decode step
+ * between the gate_up and down projections.)
+ */
+nvfp4_status nvfp4_silu_mul_quantize(const float* gate_up, int rows, int I, uint8_t* codes,
+                                     uint8_t* scales, float* global_scale, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Small-M NVFP4 GEMV                                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * y[m, n] = xg * wg * sum_k e2m1(xq[m,k]) e4m3(xs[m,k/16]) e2m1(wq[n,k]) e4m3(ws[n,k/16])
+ * for m < M, n < N: the decode projection Y = X W^T of the ReSET project page
+ * ("Core contribution": one CTA group reuses each streamed weight tile for all
+ * M tokens, several accumulator chains per thread, register-only dequant).
+ * Accumulation is FP32 across blocks; the result is within
+ * 1e-3 * sum_k |x_k w_k| + 1e-6 of the exact product.
+ *
+ *   xq, xs, xg   activations in NVFP4 layout, [M, K/2], [M, K/16], one float
+ *   M            1..8
+ *   wq, ws, wg   weights in NVFP4 layout, [N, K/2], [N, K/16], one float
+ *   N            1 .. 2^20
+ *   K            >= 256, multiple of 256
+ *   y            device, [M, N] FP32 (written)
+ *   workspace    device scratch of at least nvfp4_gemv_workspace_bytes(M, N, K)
+ *                bytes, 256-byte aligned, ZEROED ONCE before its first use
+ *                (cudaMemset); every call leaves it ready for the next one,
+ *                whatever the shape of the next call.
+ *                Calls that overlap in time on the GPU must use different
+ *                workspaces.
+ * Alignment: xq, wq, xs, ws 16-byte aligned; y 16-byte aligned.
+ */
+size_t nvfp4_gemv_workspace_bytes(int M, int N, int K);
+
+nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                               const uint8_t* wq, const uint8_t* ws, const float* wg, int N, int K,
+                               float* y, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* BF16 GEMV (the decode step's lm_head)                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * y[m, n] = sum_k x[m, k] * w[n, k], BF16 inputs, FP32 accumulation and output.
+ * M 1..8, K a multiple of 8, all pointers 16-byte aligned.
+ */
+nvfp4_status nvfp4_bf16_gemv(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
+                             cudaStream_t stream);
+
+/* FP32 -> BF16 (RNE) elementwise cast of n values; x, y 16-byte aligned, n a multiple of 8. */
+nvfp4_status nvfp4_f32_to_bf16(const float* x, size_t n, uint16_t* y, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* ReSET sampler                                                              */
+/* ------------------------------------------------------------------------ */
+typedef struct reset_params {
+  float tau0;    /* global entropy threshold (nats), used in confident steps        */
+  float t_low;   /* temperature below the threshold, > 0                            */
+  float t_high;  /* temperature at or above the threshold, > 0                      */
+  int w;         /* HSE window: positions 0..w-1 of a step use the last-w mean, 1..256 */
+} reset_params;
+
+/* Bytes of the per-row sampler state for M rows and window w. */
+size_t reset_state_bytes(int M, int w);
+
+/* Puts every row of `state` at sequence position 0 (asynchronous). */
+nvfp4_status reset_state_init(void* state, int M, int w, cudaStream_t stream);
+
+/* Scratch needed by reset_sample for M rows of V logits. */
+size_t reset_workspace_bytes(int M, int V);
+
+/*
+ * One decode position of the ReSET sampler for M rows (ReSET reading note
+ * §4.1 SAT, §4.2 HSE, §4.3; project page "Step-aware temperature scaling"):
+ *   H      = entropy (nats, temperature 1) of softmax(logits[r, :]);
+ *   a new step starts at this position when step_start[r] != 0 (the previous
+ *   token was the step delimiter) and always at the row's first position;
+ *   H_step = mean of the last w entropies (including H) while the in-step
+ *            position j < w, else the mean of the step's entropies so far;
+ *   H_bar  = mean of all entropies of the row so far (including H);
+ *   tau    = tau0 if H_step <= H_bar else H_step;
+ *   T      = t_low if H < tau else t_high;
+ *   token  = min{ i : sum_{k<=i} exp((l_k - max l)/T) > u[r] * sum_k exp((l_k - max l)/T) }.
+ *
+ *   logits     device, [M, V] FP32, 16-byte aligned, finite
+ *   M          1..64;  V 1 .. 2^24
+ *   step_start device, [M] uint8 (may be NULL: no step boundaries)
+ *   u          device, [M] FP32 uniforms in [0, 1)
+ *   state      device, reset_state_bytes(M, p->w) bytes from reset_state_init (updated)
+ *   p          HOST pointer to the parameters (copied at the call)
+ *   token      device, [M] int32 (written)
+ *   H_out      device, [M] FP32 entropies (written; may be NULL)
+ *   T_out      device, [M] FP32 chosen temperatures (written; may be NULL)
+ *   workspace  device scratch of reset_workspace_bytes(M, V) bytes, 256-byte aligned,
+ *              ZEROED ONCE before its first use (every call leaves it ready for
+ *              the next); calls that overlap on the GPU must use different workspaces.
+ */
+nvfp4_status reset_sample(const float* logits, int M, int V, const uint8_t* step_start,
+                          const float* u, void* state, const reset_params* p, int32_t* token,
+                          float* H_out, float* T_out, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

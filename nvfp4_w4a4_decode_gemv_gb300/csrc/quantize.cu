@@ -1,0 +1,315 @@
+// BF16 -> NVFP4 quantizer (E2M1 codes, E4M3 block scales, FP32 global scale).
+//
+// Format: ReSET reading note §2.1 and §6.1 (E2M1 elements, E4M3 scale per
+// 16-element block, FP32 global scale); the activation quantizer "Q" feeding
+// the GEMV with a non-interleaved scale layout: reading note §5.3 (Table 3).
+//
+// The recipe is evaluated with one IEEE rounding per operation (__fdiv_rn,
+// __fmul_rn: no contraction, no approximate reciprocal), so codes and scales
+// are bit-identical to a plain FP32 evaluation of the recipe:
+//   g = amax / 2688;  s = E4M3(bm / (6 g));  code = E2M1(x / (dec(s) g)).
+//
+// Two launch shapes:
+//  * activations (<= 16384 blocks of 16): ONE launch of a thread-block cluster;
+//    every CTA keeps its blocks in registers, the tensor amax is reduced across
+//    the cluster through distributed shared memory, then codes are written
+//    without a second read of x.
+//  * larger tensors (offline weight quantization): amax kernel (atomicMax on
+//    the float bits, which order like the values for non-negative floats, into
+//    the global-scale slot), a grid-stride quantize kernel that reads that amax,
+//    and a one-thread kernel that turns amax into amax / 2688.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxCluster = 8;
+constexpr float kGlobalDivisor = 2688.0f;   // 448 * 6
+
+// ---- element sources: block b of a [rows, K] tensor -> 16 floats ----------
+// Each source returns values that are exactly representable in BF16.
+struct SrcBF16 {
+  const uint16_t* x;
+  int nbr;      // blocks per row = K / 16
+  int K;
+  __device__ void load(long b, float v[16]) const {
+    const long r = b / nbr, c = b % nbr;
+    const uint4* p = reinterpret_cast<const uint4*>(x + r * (long)K + c * 16);
+    const uint4 a = __ldg(p), d = __ldg(p + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(w[i]);
+      v[2 * i + 1] = bf16_hi(w[i]);
+    }
+  }
+};
+
+NVFP4_DEVINL float round_bf16(float f) {
+  return __bfloat162float(__float2bfloat16_rn(f));
+}
+
+struct SrcF32 {
+  const float* x;
+  int nbr;
+  long ld;
+  __device__ void load(long b, float v[16]) const {
+    const long r = b / nbr, c = b % nbr;
+    const float4* p = reinterpret_cast<const float4*>(x + r * ld + c * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 q = __ldg(p + i);
+      v[4 * i] = round_bf16(q.x);
+      v[4 * i + 1] = round_bf16(q.y);
+      v[4 * i + 2] = round_bf16(q.z);
+      v[4 * i + 3] = round_bf16(q.w);
+    }
+  }
+};
+
+// SiLU(gate) * up, FP32, rounded to BF16.  gate = columns [0, I), up = [I, 2I).
+struct SrcSiluMul {
+  const float* gu;
+  int nbr;   // I / 16
+  int I;
+  __device__ void load(long b, float v[16]) const {
+    const long r = b / nbr, c = b % nbr;
+    const float4* pg = reinterpret_cast<const float4*>(gu + r * 2L * I + c * 16);
+    const float4* pu = reinterpret_cast<const float4*>(gu + r * 2L * I + I + c * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 g = __ldg(pg + i), u = __ldg(pu + i);
+      const float gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float s = __fdiv_rn(gs[j], __fadd_rn(1.0f, expf(-gs[j])));
+        v[4 * i + j] = round_bf16(__fmul_rn(s, us[j]));
+      }
+    }
+  }
+};
+
+NVFP4_DEVINL float block_absmax(const float v[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// Quantize one block given the global scale g.  Returns the scale byte and
+// writes the 8 code bytes.
+NVFP4_DEVINL uint32_t quant_block(const float v[16], float bm, float g, uint2& codes) {
+  const float d = __fmul_rn(6.0f, g);
+  const float t = (d > 0.0f) ? __fdiv_rn(bm, d) : 0.0f;
+  const uint32_t s = f32x2_to_e4m3x2(0.0f, t) & 0xFFu;
+  const float S = __fmul_rn(e4m3_to_f32(s), g);
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = v[2 * i], hi = v[2 * i + 1];
+    const uint32_t sgn = ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
+    uint32_t byte = sgn;
+    if (S > 0.0f) {
+      const uint32_t q = f32x2_to_e2m1x2(__fdiv_rn(hi, S), __fdiv_rn(lo, S));
+      byte = (q & 0x77u) | sgn;       // magnitude from the conversion, sign from x
+    }
+    packed[i >> 2] |= byte << (8 * (i & 3));
+  }
+  codes = make_uint2(packed[0], packed[1]);
+  return s;
+}
+
+// ---- single-launch cluster path --------------------------------------------
+template <class Src, int NB>
+__global__ void __launch_bounds__(kThreads) quant_cluster_kernel(Src src, long nblocks, uint8_t* codes,
+                                                                 uint8_t* scales, float* global) {
+  __shared__ float s_warp[kThreads / 32];
+  __shared__ float s_cta_max;
+  __shared__ float s_amax;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t csize = gridDim.x;          // the whole grid is one cluster
+  const long T = (long)csize * kThreads;
+  const long gt = (long)rank * kThreads + threadIdx.x;
+
+  float v[NB][16];
+  float bm[NB];
+  float local = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const long b = gt + i * T;
+    if (b < nblocks) {
+      src.load(b, v[i]);
+      bm[i] = block_absmax(v[i]);
+      local = fmaxf(local, bm[i]);
+    } else {
+      bm[i] = 0.0f;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.0f;
+    for (int w = 0; w < kThreads / 32; ++w) m = fmaxf(m, s_warp[w]);
+    s_cta_max = m;
+  }
+  cluster_sync();                            // every CTA's s_cta_max is visible cluster-wide
+  if (threadIdx.x == 0) {
+    float m = 0.0f;
+    for (uint32_t r = 0; r < csize; ++r) m = fmaxf(m, ld_dsmem_f32(dsmem_addr(&s_cta_max, r)));
+    s_amax = m;
+  }
+  cluster_sync();                            // reads done before any CTA may exit; s_amax visible
+  const float g = __fdiv_rn(s_amax, kGlobalDivisor);
+  if (rank == 0 && threadIdx.x == 0) *global = g;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const long b = gt + i * T;
+    if (b < nblocks) {
+      uint2 c;
+      const uint32_t s = quant_block(v[i], bm[i], g, c);
+      reinterpret_cast<uint2*>(codes)[b] = c;
+      scales[b] = static_cast<uint8_t>(s);
+    }
+  }
+}
+
+// ---- multi-launch path for large tensors -----------------------------------
+template <class Src>
+__global__ void __launch_bounds__(kThreads) amax_kernel(Src src, long nblocks, unsigned int* amax_bits) {
+  __shared__ float s_warp[kThreads / 32];
+  float local = 0.0f;
+  for (long b = (long)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += (long)gridDim.x * kThreads) {
+    float v[16];
+    src.load(b, v);
+    local = fmaxf(local, block_absmax(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.0f;
+    for (int w = 0; w < kThreads / 32; ++w) m = fmaxf(m, s_warp[w]);
+    atomicMax(amax_bits, __float_as_uint(m));     // m >= 0: uint order == float order
+  }
+}
+
+template <class Src>
+__global__ void __launch_bounds__(kThreads) quant_grid_kernel(Src src, long nblocks, const float* amax,
+                                                              uint8_t* codes, uint8_t* scales) {
+  const float g = __fdiv_rn(*amax, kGlobalDivisor);
+  for (long b = (long)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += (long)gridDim.x * kThreads) {
+    float v[16];
+    src.load(b, v);
+    uint2 c;
+    const uint32_t s = quant_block(v, block_absmax(v), g, c);
+    reinterpret_cast<uint2*>(codes)[b] = c;
+    scales[b] = static_cast<uint8_t>(s);
+  }
+}
+
+__global__ void finalize_global_kernel(float* global) {
+  *global = __fdiv_rn(*global, kGlobalDivisor);
+}
+
+__global__ void zero_global_kernel(float* global) { *global = 0.0f; }
+
+template <class Src, int NB>
+cudaError_t launch_cluster(const Src& src, long nblocks, int csize, uint8_t* codes, uint8_t* scales,
+                           float* global, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_cluster_kernel<Src, NB>, src, nblocks, codes, scales, global);
+}
+
+int g_num_sms = 0;
+
+template <class Src>
+cudaError_t quantize_dispatch(const Src& src, long nblocks, uint8_t* codes, uint8_t* scales, float* global,
+                              cudaStream_t stream) {
+  if (nblocks == 0) {
+    zero_global_kernel<<<1, 1, 0, stream>>>(global);
+    return cudaGetLastError();
+  }
+  const long per_cta = kThreads;
+  if (nblocks <= (long)kMaxCluster * per_cta * 8) {
+    int csize = (int)((nblocks + per_cta - 1) / per_cta);
+    if (csize > kMaxCluster) csize = kMaxCluster;
+    const long T = (long)csize * per_cta;
+    const long nb = (nblocks + T - 1) / T;
+    if (nb <= 1) return launch_cluster<Src, 1>(src, nblocks, csize, codes, scales, global, stream);
+    if (nb <= 2) return launch_cluster<Src, 2>(src, nblocks, csize, codes, scales, global, stream);
+    if (nb <= 4) return launch_cluster<Src, 4>(src, nblocks, csize, codes, scales, global, stream);
+    return launch_cluster<Src, 8>(src, nblocks, csize, codes, scales, global, stream);
+  }
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  long grid = (nblocks + kThreads - 1) / kThreads;
+  if (grid > (long)g_num_sms * 8) grid = (long)g_num_sms * 8;
+  cudaError_t e = cudaMemsetAsync(global, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  amax_kernel<Src><<<(unsigned)grid, kThreads, 0, stream>>>(src, nblocks, reinterpret_cast<unsigned int*>(global));
+  quant_grid_kernel<Src><<<(unsigned)grid, kThreads, 0, stream>>>(src, nblocks, global, codes, scales);
+  finalize_global_kernel<<<1, 1, 0, stream>>>(global);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Defined in abi.cu.
+nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
+bool nvfp4_internal_aligned(const void* p, size_t a);
+
+extern "C" nvfp4_status nvfp4_quantize_act(const uint16_t* x_bf16, int rows, int K, uint8_t* codes,
+                                           uint8_t* scales, float* global_scale, cudaStream_t stream) {
+  if (rows < 0 || K < 0 || (K % 16) != 0) return NVFP4_ERR_SHAPE;
+  if (!global_scale) return NVFP4_ERR_NULL;
+  const long nblocks = (long)rows * (K / 16);
+  if (nblocks > 0 && (!x_bf16 || !codes || !scales)) return NVFP4_ERR_NULL;
+  if (!nvfp4_internal_aligned(x_bf16, 16) || !nvfp4_internal_aligned(codes, 16) ||
+      !nvfp4_internal_aligned(scales, 4) || !nvfp4_internal_aligned(global_scale, 4))
+    return NVFP4_ERR_ALIGN;
+  SrcBF16 src{x_bf16, K / 16, K};
+  return nvfp4_internal_cuda_status(quantize_dispatch(src, nblocks, codes, scales, global_scale, stream));
+}
+
+extern "C" nvfp4_status nvfp4_quantize_f32(const float* x, int rows, int K, int ld, uint8_t* codes,
+                                           uint8_t* scales, float* global_scale, cudaStream_t stream) {
+  if (rows < 0 || K < 0 || (K % 16) != 0 || ld < K || (ld % 4) != 0) return NVFP4_ERR_SHAPE;
+  if (!global_scale) return NVFP4_ERR_NULL;
+  const long nblocks = (long)rows * (K / 16);
+  if (nblocks > 0 && (!x || !codes || !scales)) return NVFP4_ERR_NULL;
+  if (!nvfp4_internal_aligned(x, 16) || !nvfp4_internal_aligned(codes, 16) ||
+      !nvfp4_internal_aligned(scales, 4) || !nvfp4_internal_aligned(global_scale, 4))
+    return NVFP4_ERR_ALIGN;
+  SrcF32 src{x, K / 16, (long)ld};
+  return nvfp4_internal_cuda_status(quantize_dispatch(src, nblocks, codes, scales, global_scale, stream));
+}
+
+extern "C" nvfp4_status nvfp4_silu_mul_quantize(const float* gate_up, int rows, int I, uint8_t* codes,
+                                                uint8_t* scales, float* global_scale, cudaStream_t stream) {
+  if (rows < 0 || I < 0 || (I % 16) != 0) return NVFP4_ERR_SHAPE;
+  if (!global_scale) return NVFP4_ERR_NULL;
+  const long nblocks = (long)rows * (I / 16);
+  if (nblocks > 0 && (!gate_up || !codes || !scales)) return NVFP4_ERR_NULL;
+  if (!nvfp4_internal_aligned(gate_up, 16) || !nvfp4_internal_aligned(codes, 16) ||
+      !nvfp4_internal_aligned(scales, 4) || !nvfp4_internal_aligned(global_scale, 4))
+    return NVFP4_ERR_ALIGN;
+  SrcSiluMul src{gate_up, I / 16, I};
+  return nvfp4_internal_cuda_status(quantize_dispatch(src, nblocks, codes, scales, global_scale, stream));
+}

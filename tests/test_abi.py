@@ -1,0 +1,88 @@
+"""The C ABI library loads and exports every function include/nvfp4.h declares;
+argument errors come back synchronously (no GPU needed for any of this)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_w4a4_decode_gemv_gb300 import build
+    from nvfp4_w4a4_decode_gemv_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("nvfp4_quantize_act", "nvfp4_gemv_smallm", "reset_sample", "reset_state_bytes",
+                     "reset_state_init", "nvfp4_gemv_workspace_bytes"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from nvfp4_w4a4_decode_gemv_gb300 import _lib
+    names = _declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in nvfp4.h but not exported"
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.nvfp4_version() >> 16 == 1
+    for s in range(7):
+        assert lib.nvfp4_status_str(s)
+
+
+FAKE = 1 << 20       # a 256-byte aligned non-NULL address; never dereferenced: validation fails first
+
+
+def test_quantize_argument_errors(lib):
+    assert lib.nvfp4_quantize_act(FAKE, 2, 24, FAKE, FAKE, FAKE, None) == 2       # K % 16
+    assert lib.nvfp4_quantize_act(FAKE, -1, 32, FAKE, FAKE, FAKE, None) == 2
+    assert lib.nvfp4_quantize_act(None, 2, 32, FAKE, FAKE, FAKE, None) == 1
+    assert lib.nvfp4_quantize_act(FAKE + 8, 2, 32, FAKE, FAKE, FAKE, None) == 3   # x not 16-B aligned
+    assert lib.nvfp4_quantize_f32(FAKE, 2, 32, 30, FAKE, FAKE, FAKE, None) == 2   # ld < K
+
+
+def test_gemv_argument_errors(lib):
+    args = lambda M, N, K, x=FAKE, ws=FAKE: (x, FAKE, FAKE, M, FAKE, FAKE, FAKE, N, K, FAKE, ws, 1 << 30, None)
+    assert lib.nvfp4_gemv_smallm(*args(9, 256, 256)) == 4            # M > 8
+    assert lib.nvfp4_gemv_smallm(*args(0, 256, 256)) == 4
+    assert lib.nvfp4_gemv_smallm(*args(1, 256, 272)) == 2            # K % 256
+    assert lib.nvfp4_gemv_smallm(*args(1, 0, 256)) == 2
+    assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, x=None)) == 1
+    assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, x=FAKE + 4)) == 3
+    assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, ws=FAKE + 16)) == 3
+    assert lib.nvfp4_gemv_workspace_bytes(9, 256, 256) == 0
+    assert lib.nvfp4_gemv_workspace_bytes(1, 256, 100) == 0
+
+
+def test_reset_argument_errors(lib):
+    from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams
+    p = ResetParams(0.6, 0.3, 1.0, 8)
+    call = lambda M, V, prm: lib.reset_sample(FAKE, M, V, None, FAKE, FAKE, ctypes.byref(prm), FAKE, None, None,
+                                              FAKE, 1 << 30, None)
+    assert call(0, 100, p) == 4
+    assert call(65, 100, p) == 4
+    assert call(8, 0, p) == 2
+    assert call(8, 100, ResetParams(0.6, 0.0, 1.0, 8)) == 4           # T_low must be > 0
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 0)) == 4           # w >= 1
+    assert lib.reset_state_bytes(8, 8) > 0 and lib.reset_state_bytes(8, 0) == 0
+    assert lib.reset_workspace_bytes(8, 151936) > 0
+    assert lib.nvfp4_bf16_gemv(FAKE, 9, FAKE, 10, 64, FAKE, None) == 4
+    assert lib.nvfp4_f32_to_bf16(FAKE, 12, FAKE, None) == 2
