@@ -10,11 +10,13 @@ step streams >= 245 MB of other weights, more than the 129 MB L2, so every
 call reads its weights from HBM (no flush kernel needed).
 
 value = algorithmic HBM bytes of the step (weight codes + scales, activation
-in/out, outputs) / device time of the step, in GB/s.  The step is captured
-once into a CUDA graph and replayed; events around every call give per-call
-GEMV times for the roofline.  `e2e` repeats the step through the eager C-ABI
-calls with the activations copied from pinned host memory and the outputs
-copied back inside the timed region.
+in/out, outputs) / device time of the step, in GB/s.  For each M the four
+quantizations and the four GEMVs are captured as two CUDA graphs; the timed
+region replays them back to back with events recorded between the graph
+launches, so the same region gives the GEMV time for the roofline.  A cold-L2
+breakdown per (projection, M) follows (512 MB flush before each call).  `e2e`
+repeats the step through the eager C-ABI calls with the activations copied
+from pinned host memory and the outputs copied back inside the timed region.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (for N > 1 under torch.distributed.run: N independent replicas, weak scaling).
@@ -50,6 +52,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
+    ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
     return ap.parse_args()
 
 
@@ -147,7 +150,7 @@ def max_over_ranks(world, v):
 
 
 # ---------------------------------------------------------------------------
-def build_problem(shapes, Ms, rank):
+def build_problem(shapes, Ms, rank, only=None):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     dev = torch.device("cuda")
     weights = {}
@@ -160,6 +163,8 @@ def build_problem(shapes, Ms, rank):
     calls = []
     for M in Ms:
         for i, (name, K, N) in enumerate(shapes):
+            if only and f"{name}:{M}" != only:
+                continue
             x = synth.activations(M, K, seed=100 * M + i).to(dev)
             calls.append(dict(M=M, name=name, K=K, N=N, x=x, xq=api.NVFP4Tensor.empty(M, K, dev),
                               y=torch.empty((M, N), dtype=torch.float32, device=dev),
@@ -173,57 +178,71 @@ def build_problem(shapes, Ms, rank):
 def run_ours(args, world, rank):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     shapes, Ms = WORKLOADS[args.workload]
-    weights, calls, ws = build_problem(shapes, Ms, rank)
+    weights, calls, ws = build_problem(shapes, Ms, rank, args.only)
+    groups = {}
+    for c in calls:
+        groups.setdefault(c["M"], []).append(c)
+    order = sorted(groups)
 
-    def one_step(evs=None):
-        for j, c in enumerate(calls):
-            if evs is not None:
-                evs[j][0].record()
+    def quantize_all(cs):
+        for c in cs:
             api.nvfp4_quantize_act(c["x"], out=c["xq"])
-            if evs is not None:
-                evs[j][1].record()
-            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
-            if evs is not None:
-                evs[j][2].record()
 
-    one_step()                       # initialises kernel attributes outside capture
+    def gemv_all(cs):
+        for c in cs:
+            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+
+    for M in order:                  # initialises kernel attributes outside capture
+        quantize_all(groups[M])
+        gemv_all(groups[M])
     torch.cuda.synchronize()
+    # Per M: one graph with that M's quantizations, one with its GEMVs.  Events
+    # recorded between the graph launches bracket the GEMVs on the GPU.
     stream = torch.cuda.Stream()
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in calls] for _ in range(args.steps)]
-    g_warm, g_main = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    graphs = {}
     with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_warm, stream=stream):
-            for _ in range(args.warmup):
-                one_step()
-        with torch.cuda.graph(g_main, stream=stream):
-            for k in range(args.steps):
-                one_step(evs[k])
+        for M in order:
+            gq, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gq, stream=stream):
+                quantize_all(groups[M])
+            with torch.cuda.graph(gg, stream=stream):
+                gemv_all(groups[M])
+            graphs[M] = (gq, gg)
     torch.cuda.synchronize()
-    g_warm.replay()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in order]
+           for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for M in order:
+                graphs[M][0].replay()
+                graphs[M][1].replay()
     barrier(world)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
-        t0.record()
-        g_main.replay()
-        t1.record()
+        with torch.cuda.stream(stream):
+            t0.record()
+            for k in range(args.steps):
+                for i, M in enumerate(order):
+                    graphs[M][0].replay()
+                    evs[k][i][0].record()
+                    graphs[M][1].replay()
+                    evs[k][i][1].record()
+            t1.record()
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(world, t0.elapsed_time(t1))
     clocks = clk.summary()
+    gemv_ms = {M: float(np.mean([evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)]))
+               for i, M in enumerate(order)}
+    per_call = cold_per_call(calls, weights, ws, reps=3)
 
     step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
     value_gbs = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
-    per_call = {}
-    gemv_ms_total = 0.0
-    gemv_bytes_total = 0
-    for j, c in enumerate(calls):
-        g_ms = [evs[k][j][1].elapsed_time(evs[k][j][2]) for k in range(args.steps)]
-        q_ms = [evs[k][j][0].elapsed_time(evs[k][j][1]) for k in range(args.steps)]
-        gm = float(np.mean(g_ms))
-        gemv_ms_total += gm
-        gemv_bytes_total += c["gemv_bytes"]
-        per_call[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(gm * 1e3, 2), "quant_us": round(float(np.mean(q_ms)) * 1e3, 2),
-                                              "gemv_gbs": round(c["gemv_bytes"] / (gm * 1e-3) / 1e9, 1)}
+    gemv_ms_total = sum(gemv_ms.values())
+    gemv_bytes_total = sum(c["gemv_bytes"] for c in calls)
+    per_m = {f"M{M}": {"gemv_us_per_call": round(gemv_ms[M] * 1e3 / len(groups[M]), 2),
+                       "gemv_gbs": round(sum(c["gemv_bytes"] for c in groups[M]) / (gemv_ms[M] * 1e-3) / 1e9, 1)}
+             for M in order}
     peak, peak_kind = measured_peaks()
     achieved = gemv_bytes_total / (gemv_ms_total * 1e-3) / 1e9
     result = {
@@ -239,13 +258,41 @@ def run_ours(args, world, rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "nvfp4_gemv_smallm (prep + gemv), algorithmic bytes / per-call event time",
+                     "kernel": "nvfp4_gemv_smallm (activation prep + GEMV kernels): algorithmic bytes of all GEMV "
+                               "calls / their event-timed duration in the timed region",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clocks,
-        "gpu_launches": len(calls) * 3 * args.steps,
-        "per_call": per_call,
+        "gpu_launches": len(calls) * 3 * args.steps,   # per call: quantize, activation prep, GEMV
+        "per_m": per_m,
+        "per_call_cold_l2": per_call,
     }
     return result, calls, weights, ws
+
+
+def cold_per_call(calls, weights, ws, reps=3):
+    """us per call of the quantizer and the GEMV with L2 flushed before every
+    call (a 512 MB memset, during which the host enqueues the timed call)."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    out = {}
+    for c in calls:
+        q_us, g_us = [], []
+        for _ in range(reps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            flush.zero_()
+            e[0].record()
+            api.nvfp4_quantize_act(c["x"], out=c["xq"])
+            e[1].record()
+            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            e[2].record()
+            torch.cuda.synchronize()
+            q_us.append(e[0].elapsed_time(e[1]) * 1e3)
+            g_us.append(e[1].elapsed_time(e[2]) * 1e3)
+        g = float(np.median(g_us))
+        out[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(g, 2), "quant_us": round(float(np.median(q_us)), 2),
+                                         "gemv_gbs": round(c["gemv_bytes"] / (g * 1e-6) / 1e9, 1)}
+    del flush
+    return out
 
 
 def run_e2e(args, calls, weights, ws):

@@ -49,7 +49,6 @@ constexpr int kChunk = 256;                 // K elements per stage
 constexpr int kMaxM = 8;
 constexpr int kRecBytes = 32;               // activation record per (token, 16-block)
 constexpr int kRecsPerChunk = kChunk / 16;  // 16
-constexpr int kTileRows = 128;              // rows per tile (R * 32 * WC for every variant)
 
 // Weight nibble -> 12 + 2 * e2m1(code), split over two 8-entry tables for prmt.
 // Positive codes index kPos*, negative codes (sign bit 3 flipped) index kNeg*.
@@ -65,8 +64,8 @@ struct GemvArgs {
   const float* xg;
   const float* wg;
   float* y;
-  float* partials;              // [G][2][kTileRows][M]
-  unsigned int* counters;       // [RT * (kTileRows / (32 * R))]
+  float* partials;              // [G][2][tile rows][M]
+  unsigned int* counters;       // one per 32-row group of weight rows
   int M, N, K, C, RT;
   long long U;
 };
@@ -119,18 +118,21 @@ __global__ void __launch_bounds__(256) xrec_kernel(const uint8_t* __restrict__ x
 }
 
 // ---- the GEMV kernel ----------------------------------------------------------
-template <int R, int WC>
+// Tile = TR weight rows x 256 K.  TR / (32 R) consumer warps, each lane owning R
+// rows; one producer warp; S pipeline stages.
+template <int M, int TR, int R>
 struct Layout {
-  static_assert(R * 32 * WC == kTileRows, "tile is 128 rows");
-  static constexpr int kCodeBytes = kTileRows * 128;          // one swizzled 128-byte row per weight row
-  static constexpr int kScaleBytes = kTileRows * 16;
-  static constexpr int kXBytes = kMaxM * kRecsPerChunk * kRecBytes;
+  static constexpr int kWC = TR / (32 * R);
+  static_assert(kWC * 32 * R == TR && kWC >= 1, "tile rows must be a multiple of 32 R");
+  static constexpr int kCodeBytes = TR * 128;          // one swizzled 128-byte row per weight row
+  static constexpr int kScaleBytes = TR * 16;
+  static constexpr int kXBytes = M * kRecsPerChunk * kRecBytes;
   static constexpr int kSlot = ((kCodeBytes + kScaleBytes + kXBytes + 1023) / 1024) * 1024;
 };
 
-template <int R, int WC, int S>
+template <int M, int TR, int R, int S>
 constexpr size_t gemv_smem_bytes() {
-  return (size_t)S * Layout<R, WC>::kSlot + 1024 /* alignment slack */ + 2 * S * sizeof(uint64_t);
+  return (size_t)S * Layout<M, TR, R>::kSlot + 1024 /* alignment slack */ + 2 * S * sizeof(uint64_t);
 }
 
 NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { return (q * U) / G; }
@@ -138,25 +140,29 @@ NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { retur
 // CTA whose unit range contains unit x: the largest q with unit_start(q) <= x.
 NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { return ((x + 1) * G - 1) / U; }
 
-template <int M, int R, int WC>
-NVFP4_DEVINL void compute_stage(const uint8_t* slot, int warp, int lane, float (&acc)[R][M]) {
-  using L = Layout<R, WC>;
+template <int R>
+NVFP4_DEVINL float acc_get(const float2* a, int r) { return (r & 1) ? a[r / 2].y : a[r / 2].x; }
+
+// One 256-K stage for this lane's R rows and all M tokens.  The block loop stays
+// rolled (small code); the token and row loops are unrolled.
+template <int M, int TR, int R>
+NVFP4_DEVINL void compute_stage(const uint8_t* slot, int warp, int lane, float2 (&acc2)[M][(R + 1) / 2]) {
+  using L = Layout<M, TR, R>;
   const uint8_t* codes = slot;
   const uint8_t* scl = slot + L::kCodeBytes;
   const uint4* xr = reinterpret_cast<const uint4*>(slot + L::kCodeBytes + L::kScaleBytes);
   int rr[R];
-  uint4 sc[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    rr[r] = warp * 32 * R + r * 32 + lane;
-    sc[r] = *reinterpret_cast<const uint4*>(scl + rr[r] * 16);
-  }
-#pragma unroll
+  for (int r = 0; r < R; ++r) rr[r] = warp * 32 * R + r * 32 + lane;
+#pragma unroll 1
   for (int j = 0; j < 8; ++j) {
     uint4 cw[R];
+    uint32_t sb[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r) {
       cw[r] = *reinterpret_cast<const uint4*>(codes + rr[r] * 128 + ((j ^ (rr[r] & 7)) << 4));
+      sb[r] = *reinterpret_cast<const unsigned short*>(scl + rr[r] * 16 + 2 * j);   // scales of blocks 2j, 2j+1
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int b = 2 * j + h;
@@ -166,56 +172,59 @@ NVFP4_DEVINL void compute_stage(const uint8_t* slot, int warp, int lane, float (
       for (int r = 0; r < R; ++r) {
         unpack_w8(h ? cw[r].z : cw[r].x, wv[r][0], wv[r][1]);
         unpack_w8(h ? cw[r].w : cw[r].y, wv[r][2], wv[r][3]);
-        const uint32_t sword = (b < 4) ? sc[r].x : (b < 8) ? sc[r].y : (b < 12) ? sc[r].z : sc[r].w;
-        swr[r] = __uint_as_float(((sword >> (8 * (b & 3))) & 0xFFu) << 20);   // e4m3 * 2^-120
+        swr[r] = __uint_as_float(((sb[r] >> (8 * h)) & 0xFFu) << 20);   // e4m3 * 2^-120
       }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         const uint4 xa = xr[2 * (m * kRecsPerChunk + b)];
         const uint4 xb = xr[2 * (m * kRecsPerChunk + b) + 1];
+        float t[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           int d = __dp4a((int)xa.x, (int)wv[r][0], (int)xb.x);
           d = __dp4a((int)xa.y, (int)wv[r][1], d);
           d = __dp4a((int)xa.z, (int)wv[r][2], d);
           d = __dp4a((int)xa.w, (int)wv[r][3], d);
-          const float t = fmaf(__int_as_float(d), __uint_as_float(xb.y), __uint_as_float(xb.z));
-          acc[r][m] = fmaf(t, swr[r], acc[r][m]);
+          t[r] = fmaf(__int_as_float(d), __uint_as_float(xb.y), __uint_as_float(xb.z));   // exact: sx * D * 2^60
         }
+#pragma unroll
+        for (int r = 0; r + 1 < R; r += 2)
+          acc2[m][r / 2] = __ffma2_rn(make_float2(t[r], t[r + 1]), make_float2(swr[r], swr[r + 1]), acc2[m][r / 2]);
+        if (R & 1) acc2[m][R / 2].x = fmaf(t[R - 1], swr[R - 1], acc2[m][R / 2].x);
       }
     }
   }
 }
 
-template <int M, int R, int WC>
+template <int M, int TR, int R>
 NVFP4_DEVINL void flush_tile(const GemvArgs& a, int tile, long long first_unit_of_cta, int warp, int lane,
-                             const float (&acc)[R][M]) {
+                             const float2 (&acc2)[M][(R + 1) / 2]) {
   const long long G = gridDim.x;
   const long long C = a.C;
   const long long first = cta_of_unit((long long)tile * C, a.U, G);
   const long long last = cta_of_unit((long long)tile * C + C - 1, a.U, G);
   const float yscale = __fmul_rn(__fmul_rn(__ldg(a.xg), __ldg(a.wg)), 1152921504606846976.0f /* 2^60 */);
-  const int row0 = tile * kTileRows + warp * 32 * R;
+  const int row0 = tile * TR + warp * 32 * R;
   if (first == last) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int n = row0 + r * 32 + lane;
       if (n < a.N) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = acc[r][m] * yscale;
+        for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = acc_get<R>(acc2[m], r) * yscale;
       }
     }
     return;
   }
   const int my_slot = (tile == (int)(first_unit_of_cta / C)) ? 0 : 1;
-  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * kTileRows + warp * 32 * R) * M;
+  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * TR + warp * 32 * R) * M;
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int m = 0; m < M; ++m) __stcg(part + (size_t)(r * 32 + lane) * M + m, acc[r][m]);
+    for (int m = 0; m < M; ++m) __stcg(part + (size_t)(r * 32 + lane) * M + m, acc_get<R>(acc2[m], r));
   __threadfence();
   __syncwarp();
-  unsigned int* cnt = a.counters + (size_t)tile * WC + warp;
+  unsigned int* cnt = a.counters + (size_t)(row0 / 32);
   int is_last = 0;
   if (lane == 0) is_last = (atomicAdd(cnt, 1u) == (unsigned int)(last - first));
   is_last = __shfl_sync(0xffffffffu, is_last, 0);
@@ -228,7 +237,7 @@ NVFP4_DEVINL void flush_tile(const GemvArgs& a, int tile, long long first_unit_o
     for (int m = 0; m < M; ++m) sum[m] = 0.0f;
     for (long long q = first; q <= last; ++q) {
       const int qslot = (tile == (int)(unit_start(q, a.U, G) / C)) ? 0 : 1;
-      const float* pq = a.partials + (((size_t)q * 2 + qslot) * kTileRows + warp * 32 * R + r * 32 + lane) * M;
+      const float* pq = a.partials + (((size_t)q * 2 + qslot) * TR + warp * 32 * R + r * 32 + lane) * M;
 #pragma unroll
       for (int m = 0; m < M; ++m) sum[m] += __ldcg(pq + m);
     }
@@ -241,13 +250,16 @@ NVFP4_DEVINL void flush_tile(const GemvArgs& a, int tile, long long first_unit_o
   if (lane == 0) *cnt = 0u;
 }
 
-template <int M, int R, int WC, int S>
-__global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                                                             const __grid_constant__ CUtensorMap tm_scales,
-                                                             const GemvArgs a) {
-  using L = Layout<R, WC>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+template <int M, int TR, int R, int S>
+__global__ void __launch_bounds__(32 * (TR / (32 * R) + 1)) gemv_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                                                                        const __grid_constant__ CUtensorMap tm_scales,
+                                                                        const GemvArgs a) {
+  using L = Layout<M, TR, R>;
+  constexpr int WC = L::kWC;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base for the 128-byte swizzle.  Offset arithmetic on the
+  // shared array keeps every access in the shared state space.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * L::kSlot);
   uint64_t* empty = full + S;
 
@@ -256,8 +268,8 @@ __global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_consta
   const long long u0 = unit_start(blockIdx.x, a.U, G);
   const long long u1 = unit_start(blockIdx.x + 1, a.U, G);
   const int nunits = (int)(u1 - u0);
-  const uint32_t xbytes = (uint32_t)a.M * kRecsPerChunk * kRecBytes;
-  const uint32_t stage_tx = L::kCodeBytes + L::kScaleBytes + xbytes;
+  constexpr uint32_t xbytes = (uint32_t)M * kRecsPerChunk * kRecBytes;
+  constexpr uint32_t stage_tx = L::kCodeBytes + L::kScaleBytes + xbytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -279,8 +291,8 @@ __global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_consta
         const int tile = (int)(u / a.C), c = (int)(u % a.C);
         uint8_t* slot = smem + k * L::kSlot;
         mbar_arrive_expect_tx(&full[k], stage_tx);
-        tma_load_2d(slot, &tm_codes, c * 128, tile * kTileRows, &full[k]);
-        tma_load_2d(slot + L::kCodeBytes, &tm_scales, c * 16, tile * kTileRows, &full[k]);
+        tma_load_2d(slot, &tm_codes, c * 128, tile * TR, &full[k]);
+        tma_load_2d(slot + L::kCodeBytes, &tm_scales, c * 16, tile * TR, &full[k]);
       }
       griddep_wait();   // activation records are written by the prep kernel
       for (int k = 0; k < pre; ++k) {
@@ -295,8 +307,8 @@ __global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_consta
         const int tile = (int)(u / a.C), c = (int)(u % a.C);
         uint8_t* slot = smem + s * L::kSlot;
         mbar_arrive_expect_tx(&full[s], stage_tx);
-        tma_load_2d(slot, &tm_codes, c * 128, tile * kTileRows, &full[s]);
-        tma_load_2d(slot + L::kCodeBytes, &tm_scales, c * 16, tile * kTileRows, &full[s]);
+        tma_load_2d(slot, &tm_codes, c * 128, tile * TR, &full[s]);
+        tma_load_2d(slot + L::kCodeBytes, &tm_scales, c * 16, tile * TR, &full[s]);
         bulk_g2s(slot + L::kCodeBytes + L::kScaleBytes, a.xrec + (size_t)c * xbytes, xbytes, &full[s]);
         issued = k + 1;
       }
@@ -309,11 +321,11 @@ __global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_consta
 
   // ---------------- consumer warps ----------------
   griddep_wait();
-  float acc[R][M];
+  float2 acc2[M][(R + 1) / 2];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+  for (int m = 0; m < M; ++m)
 #pragma unroll
-    for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+    for (int r = 0; r < (R + 1) / 2; ++r) acc2[m][r] = make_float2(0.0f, 0.0f);
   int cur_tile = -1;
   for (int k = 0; k < nunits; ++k) {
     const int s = k % S;
@@ -321,18 +333,18 @@ __global__ void __launch_bounds__(32 * (WC + 1)) gemv_kernel(const __grid_consta
     const long long u = u0 + k;
     const int tile = (int)(u / a.C);
     if (tile != cur_tile) {
-      if (cur_tile >= 0) flush_tile<M, R, WC>(a, cur_tile, u0, warp, lane, acc);
+      if (cur_tile >= 0) flush_tile<M, TR, R>(a, cur_tile, u0, warp, lane, acc2);
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+      for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+        for (int r = 0; r < (R + 1) / 2; ++r) acc2[m][r] = make_float2(0.0f, 0.0f);
       cur_tile = tile;
     }
-    compute_stage<M, R, WC>(smem + s * L::kSlot, warp, lane, acc);
+    compute_stage<M, TR, R>(smem + s * L::kSlot, warp, lane, acc2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (cur_tile >= 0) flush_tile<M, R, WC>(a, cur_tile, u0, warp, lane, acc);
+  if (cur_tile >= 0) flush_tile<M, TR, R>(a, cur_tile, u0, warp, lane, acc2);
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -369,36 +381,37 @@ int device_sms() {
   return n > 0 ? n : 148;
 }
 
-constexpr int kMaxCtasPerSm = 4;
+constexpr int kMaxCtasPerSm = 8;
+constexpr int kMaxTileRows = 128;
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
   size_t xrec, counters, partials, total;
 };
 
-// Counters sit first, in a fixed-size region, so that calls of any shape that
-// share a workspace find them at the same place (and zero).
+// Counters sit first, in a fixed-size region (one per 32-row group of weight
+// rows), so that calls of any shape that share a workspace find them at the
+// same place, and zero.
 constexpr int kMaxN = 1 << 20;
-constexpr size_t kCounterBytes = (size_t)(kMaxN / kTileRows) * 4 * sizeof(unsigned int);   // 128 KB
+constexpr size_t kCounterBytes = align256((size_t)(kMaxN / 32 + 64) * sizeof(unsigned int));
 
-WsLayout ws_layout(int M, int N, int K) {
-  (void)N;
+WsLayout ws_layout(int M, int K) {
   WsLayout l;
   l.counters = 0;
   l.xrec = kCounterBytes;
   l.partials = l.xrec + align256((size_t)M * (K / 16) * kRecBytes);
   const size_t gmax = (size_t)device_sms() * kMaxCtasPerSm;
-  l.total = l.partials + align256(gmax * 2 * kTileRows * (size_t)M * sizeof(float));
+  l.total = l.partials + align256(gmax * 2 * kMaxTileRows * (size_t)M * sizeof(float));
   return l;
 }
 
-template <int M, int R, int WC, int S>
-cudaError_t launch_variant(const CUtensorMap& tc, const CUtensorMap& ts, const GemvArgs& a, cudaStream_t stream,
-                           int grid_cap) {
+template <int M, int TR, int R, int S>
+cudaError_t launch_variant(const void* wq, const void* wsc, GemvArgs a, cudaStream_t stream, int grid_cap) {
   static int occ = -1;
-  constexpr size_t smem = gemv_smem_bytes<R, WC, S>();
-  auto kern = gemv_kernel<M, R, WC, S>;
+  constexpr int WC = TR / (32 * R);
+  constexpr size_t smem = gemv_smem_bytes<M, TR, R, S>();
+  auto kern = gemv_kernel<M, TR, R, S>;
   if (occ < 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -407,6 +420,12 @@ cudaError_t launch_variant(const CUtensorMap& tc, const CUtensorMap& ts, const G
     if (e != cudaSuccess) return e;
     occ = o < 1 ? 1 : (o > kMaxCtasPerSm ? kMaxCtasPerSm : o);
   }
+  CUtensorMap tc, ts;
+  if (!encode_2d(&tc, wq, (uint64_t)a.K / 2, (uint64_t)a.N, 128, TR, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&ts, wsc, (uint64_t)a.K / 16, (uint64_t)a.N, 16, TR, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  a.RT = (a.N + TR - 1) / TR;
+  a.U = (long long)a.RT * a.C;
   long long G = (long long)occ * device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
@@ -423,13 +442,17 @@ cudaError_t launch_variant(const CUtensorMap& tc, const CUtensorMap& ts, const G
   return cudaLaunchKernelEx(&cfg, kern, tc, ts, a);
 }
 
+// Kernel variants: tile rows x rows per lane x pipeline stages.
 template <int M>
-cudaError_t launch_m(int variant, const CUtensorMap& tc, const CUtensorMap& ts, const GemvArgs& a,
-                     cudaStream_t stream, int grid_cap) {
+cudaError_t launch_m(int variant, const void* wq, const void* wsc, const GemvArgs& a, cudaStream_t stream,
+                     int grid_cap) {
   switch (variant) {
-    case 1: return launch_variant<M, 1, 4, 3>(tc, ts, a, stream, grid_cap);
-    case 2: return launch_variant<M, 4, 1, 3>(tc, ts, a, stream, grid_cap);
-    default: return launch_variant<M, 2, 2, 3>(tc, ts, a, stream, grid_cap);
+    case 1: return launch_variant<M, 128, 2, 3>(wq, wsc, a, stream, grid_cap);
+    case 2: return launch_variant<M, 64, 1, 4>(wq, wsc, a, stream, grid_cap);
+    case 3: return launch_variant<M, 64, 2, 4>(wq, wsc, a, stream, grid_cap);
+    case 4: return launch_variant<M, 128, 1, 4>(wq, wsc, a, stream, grid_cap);
+    case 5: return launch_variant<M, 64, 1, 6>(wq, wsc, a, stream, grid_cap);
+    default: return launch_variant<M, 128, 1, 3>(wq, wsc, a, stream, grid_cap);
   }
 }
 
@@ -446,7 +469,7 @@ nvfp4_status nvfp4_internal_check_device();
 
 extern "C" size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
-  return ws_layout(M, N, K).total;
+  return ws_layout(M, K).total;
 }
 
 extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
@@ -459,15 +482,10 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
       !nvfp4_internal_aligned(ws, 16) || !nvfp4_internal_aligned(y, 16) || !nvfp4_internal_aligned(xg, 4) ||
       !nvfp4_internal_aligned(wg, 4) || !nvfp4_internal_aligned(workspace, 256))
     return NVFP4_ERR_ALIGN;
-  const WsLayout wl = ws_layout(M, N, K);
+  const WsLayout wl = ws_layout(M, K);
   if (workspace_bytes < wl.total) return NVFP4_ERR_SHAPE;
   nvfp4_status ds = nvfp4_internal_check_device();
   if (ds != NVFP4_OK) return ds;
-
-  CUtensorMap tc, ts;
-  if (!encode_2d(&tc, wq, (uint64_t)K / 2, (uint64_t)N, 128, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&ts, ws, (uint64_t)K / 16, (uint64_t)N, 16, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return NVFP4_ERR_CUDA;
 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   GemvArgs a;
@@ -481,25 +499,25 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   a.N = N;
   a.K = K;
   a.C = K / kChunk;
-  a.RT = (N + kTileRows - 1) / kTileRows;
-  a.U = (long long)a.RT * a.C;
+  a.RT = 0;   // set by the variant (depends on its tile height)
+  a.U = 0;
 
   const int nrec = M * (K / 16);
   xrec_kernel<<<(nrec + 255) / 256, 256, 0, stream>>>(xq, xs, M, K, reinterpret_cast<uint4*>(wsb + wl.xrec));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
 
-  static const int variant = env_int("NVFP4_GEMV_VARIANT", 0);
-  static const int grid_cap = env_int("NVFP4_GEMV_GRID", 0);
+  const int variant = env_int("NVFP4_GEMV_VARIANT", 0);
+  const int grid_cap = env_int("NVFP4_GEMV_GRID", 0);
   switch (M) {
-    case 1: e = launch_m<1>(variant, tc, ts, a, stream, grid_cap); break;
-    case 2: e = launch_m<2>(variant, tc, ts, a, stream, grid_cap); break;
-    case 3: e = launch_m<3>(variant, tc, ts, a, stream, grid_cap); break;
-    case 4: e = launch_m<4>(variant, tc, ts, a, stream, grid_cap); break;
-    case 5: e = launch_m<5>(variant, tc, ts, a, stream, grid_cap); break;
-    case 6: e = launch_m<6>(variant, tc, ts, a, stream, grid_cap); break;
-    case 7: e = launch_m<7>(variant, tc, ts, a, stream, grid_cap); break;
-    default: e = launch_m<8>(variant, tc, ts, a, stream, grid_cap); break;
+    case 1: e = launch_m<1>(variant, wq, ws, a, stream, grid_cap); break;
+    case 2: e = launch_m<2>(variant, wq, ws, a, stream, grid_cap); break;
+    case 3: e = launch_m<3>(variant, wq, ws, a, stream, grid_cap); break;
+    case 4: e = launch_m<4>(variant, wq, ws, a, stream, grid_cap); break;
+    case 5: e = launch_m<5>(variant, wq, ws, a, stream, grid_cap); break;
+    case 6: e = launch_m<6>(variant, wq, ws, a, stream, grid_cap); break;
+    case 7: e = launch_m<7>(variant, wq, ws, a, stream, grid_cap); break;
+    default: e = launch_m<8>(variant, wq, ws, a, stream, grid_cap); break;
   }
   return nvfp4_internal_cuda_status(e);
 }
