@@ -11,8 +11,10 @@
 //   token  = min{ i : sum_{k<=i} p_k > u * sum_k p_k },  p_k = exp((l_k - max l) / T)
 //
 // One launch: grid = M rows x NC chunks of kChunk logits.  Each CTA reduces its
-// chunk to (max, sum e^(l-m), sum e^(l-m)(l-m), sum e^((l-m)/T_low),
-// sum e^((l-m)/T_high)) in FP32 and publishes it; the last CTA of a row to
+// chunk to (max m, the number of logits equal to m, sum of e^(l-m) over the
+// others, sum e^(l-m)(l-m), sum e^((l-m)/T_low), sum e^((l-m)/T_high)) in FP32
+// and publishes it (keeping the terms equal to 1 out of the FP32 sum keeps the
+// small tail of a peaked distribution, and so its entropy, accurate); the last CTA of a row to
 // arrive (atomic counter, no spin-wait) merges the chunks in chunk order in
 // FP64 -- deterministic whichever CTA is last -- updates the row's state,
 // picks T, finds the chunk that holds u * Z_T and scans that one chunk with an
@@ -65,7 +67,7 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 // Per-chunk partials, padded to 8 floats.
 struct Part {
-  float mx, z1, a1, zl, zh, pad0, pad1, pad2;
+  float mx, z1, a1, zl, zh, n0, pad0, pad1;   // z1, a1 exclude the n0 logits equal to mx
 };
 
 __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __restrict__ logits, int M, int V, int NC,
@@ -108,19 +110,24 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
   __syncthreads();
   const float cm = s_rowmax;
   const float inv_tl = 1.0f / p.t_low, inv_th = 1.0f / p.t_high;   // same expressions as below
-  float z1 = 0.f, a1 = 0.f, zl = 0.f, zh = 0.f;
+  float n0 = 0.f, z1 = 0.f, a1 = 0.f, zl = 0.f, zh = 0.f;
 #pragma unroll
   for (int k = 0; k < kPerThread; ++k) {
     const int i = lo + threadIdx.x + k * kThreads;
     if (i < hi) {
       const float s = v[k] - cm;
-      const float e = expf(s);
-      z1 += e;
-      a1 += e * s;
+      if (s == 0.0f) {
+        n0 += 1.0f;                      // e^0 = 1, counted exactly
+      } else {
+        const float e = expf(s);
+        z1 += e;
+        a1 += e * s;
+      }
       zl += expf(s * inv_tl);
       zh += expf(s * inv_th);
     }
   }
+  n0 = warp_sum(n0);
   z1 = warp_sum(z1);
   a1 = warp_sum(a1);
   zl = warp_sum(zl);
@@ -131,21 +138,22 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
     s_red[1][warp] = a1;
     s_red[2][warp] = zl;
     s_red[3][warp] = zh;
+    s_red[4][warp] = n0;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     Part q;
     q.mx = cm;
-    q.z1 = q.a1 = q.zl = q.zh = 0.f;
+    q.z1 = q.a1 = q.zl = q.zh = q.n0 = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) {
       q.z1 += s_red[0][w];
       q.a1 += s_red[1][w];
       q.zl += s_red[2][w];
       q.zh += s_red[3][w];
+      q.n0 += s_red[4][w];
     }
-    q.pad0 = q.pad1 = q.pad2 = 0.f;
     __stcg(reinterpret_cast<float4*>(parts + (size_t)row * NC + c), make_float4(q.mx, q.z1, q.a1, q.zl));
-    __stcg(reinterpret_cast<float4*>(parts + (size_t)row * NC + c) + 1, make_float4(q.zh, 0.f, 0.f, 0.f));
+    __stcg(reinterpret_cast<float4*>(parts + (size_t)row * NC + c) + 1, make_float4(q.zh, q.n0, 0.f, 0.f));
     __threadfence();
     s_last = (atomicAdd(counters + row, 1u) == (unsigned int)(NC - 1));
   }
@@ -161,10 +169,11 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
     double Z = 0.0, A = 0.0;
     for (int q = lane; q < NC; q += 32) {
       const float4 p0 = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)row * NC + q));
+      const float4 p1 = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)row * NC + q) + 1);
       const float d = p0.x - gmax;                      // <= 0
       const double r1 = (double)expf(d);
-      Z += r1 * p0.y;
-      A += r1 * ((double)p0.z + (double)d * (double)p0.y);
+      Z += r1 * ((double)p1.y + (double)p0.y);
+      A += r1 * ((double)p0.z + (double)d * ((double)p0.y + (double)p1.y));
     }
     Z = warp_sum_d(Z);
     A = warp_sum_d(A);

@@ -1,0 +1,118 @@
+"""GPU ReSET sampler vs the oracle over whole sequences.
+
+Per row and position: H within 1e-4 relative; T equal unless the oracle's
+comparison is inside its 1e-4 guard band (then either T is accepted); the
+token equal to the oracle's inverse-CDF sample at the GPU's T, up to the
+tokens whose cumulative sum lies within 4e-6 * Z of u * Z (the GPU sums exp
+values of FP32 accuracy -- 2 ulp per exp, FP32 chunk sums of <= 2048 terms --
+so its partial sums carry a relative error below that bound).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import reset as R
+from nvfp4_w4a4_decode_gemv_gb300 import api, synth
+from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams
+
+pytestmark = pytest.mark.gpu
+
+TOKEN_REL = 4e-6
+
+
+def _f32(v):
+    return float(np.float32(v))
+
+
+def _run(M, V, steps, sigmas, starts, us, tau0=0.6, t_low=0.3, t_high=1.0, w=8, seed0=4, pass_starts=True):
+    p_gpu = dict(tau0=tau0, t_low=t_low, t_high=t_high, w=w)
+    sampler = api.ResetSampler(M, V, **p_gpu)
+    p = R.ResetParams(tau0=_f32(tau0), t_low=_f32(t_low), t_high=_f32(t_high), w=w)
+    states = [R.RowState(w=w) for _ in range(M)]
+    n_amb = 0
+    for t in range(steps):
+        logits = synth.reset_logits(t, M, V, float(sigmas[t]), base_seed=seed0)
+        st = torch.from_numpy(starts[t]).cuda() if pass_starts else None
+        u = torch.from_numpy(us[t]).cuda()
+        tok, H, T = sampler(logits.cuda(), st, u)
+        torch.cuda.synchronize()
+        tok, H, T = tok.cpu().numpy(), H.cpu().numpy(), T.cpu().numpy()
+        ln = logits.numpy().astype(np.float64)
+        for r in range(M):
+            Hr = R.token_entropy(ln[r])
+            res = R.reset_update(states[r], Hr, bool(starts[t, r]) and pass_starts, p)
+            assert abs(H[r] - Hr) <= 1e-4 * max(abs(Hr), 1e-6), (t, r, H[r], Hr)
+            if R.temperature_is_ambiguous(res, p):
+                n_amb += 1
+                assert T[r] in (np.float32(t_low), np.float32(t_high))
+            else:
+                assert T[r] == np.float32(res.T), (t, r, T[r], res)
+            lo, hi = R.acceptable_tokens(ln[r], float(T[r]), float(us[t, r]), TOKEN_REL)
+            assert lo <= tok[r] <= hi, (t, r, tok[r], lo, hi)
+    assert api.device_status() == 0
+    return n_amb
+
+
+def test_small_vocab_sequence():
+    M, V, steps = 8, 5000, 40
+    _run(M, V, steps, synth.reset_sigmas(steps), synth.reset_boundaries(steps, M, p=0.15),
+         synth.reset_uniforms(steps, M))
+
+
+def test_full_size_sequence_prefix():
+    """M = 8 rows x V = 151936 logits (the sampler workload), first 24 positions."""
+    M, V, steps = 8, synth.LM_HEAD_VOCAB, 24
+    _run(M, V, steps, synth.reset_sigmas(steps), synth.reset_boundaries(steps, M, p=1 / 4),
+         synth.reset_uniforms(steps, M))
+
+
+@pytest.mark.parametrize("V", [1, 2, 2047, 2048, 2049, 4096 + 5])
+def test_ragged_and_tiny_vocab(V):
+    M, steps = 3, 6
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=V), synth.reset_boundaries(steps, M, p=0.3, seed=V),
+         synth.reset_uniforms(steps, M, seed=V))
+
+
+def test_no_step_flags_and_other_params():
+    M, V, steps = 4, 3000, 20
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=1), synth.reset_boundaries(steps, M, p=0.2, seed=1),
+         synth.reset_uniforms(steps, M, seed=1), tau0=0.5, t_low=0.1, t_high=1.0, w=3, pass_starts=False)
+
+
+def test_u_zero_gives_first_token_with_mass():
+    M, V = 2, 100
+    sampler = api.ResetSampler(M, V)
+    logits = torch.zeros((M, V))
+    logits[0, :10] = -200.0          # exp underflows to 0 at T = 0.3 and T = 1 in FP32
+    tok, _, _ = sampler(logits.cuda(), None, torch.zeros(M).cuda())
+    torch.cuda.synchronize()
+    assert tok.tolist() == [10, 0]
+
+
+def test_repeatable_and_state_restart():
+    M, V, steps = 4, 7000, 8
+    sig, st, us = synth.reset_sigmas(steps), synth.reset_boundaries(steps, M, p=0.3), synth.reset_uniforms(steps, M)
+    outs = []
+    for _ in range(2):
+        sampler = api.ResetSampler(M, V)
+        toks = []
+        for t in range(steps):
+            tok, H, T = sampler(synth.reset_logits(t, M, V, float(sig[t])).cuda(), torch.from_numpy(st[t]).cuda(),
+                                torch.from_numpy(us[t]).cuda())
+            toks.append((tok.cpu().numpy().copy(), H.cpu().numpy().copy(), T.cpu().numpy().copy()))
+        outs.append(toks)
+    for a, b in zip(*outs):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+
+
+def test_window_mismatch_is_reported_without_fault():
+    """A call whose window differs from the state's records a device error; the
+    context stays usable."""
+    M, V = 2, 512
+    sampler = api.ResetSampler(M, V, w=8)
+    sampler.params = ResetParams(0.6, 0.3, 1.0, 4)
+    sampler(torch.zeros((M, V)).cuda(), None, torch.zeros(M).cuda())
+    torch.cuda.synchronize()
+    assert api.device_status() == 2
+    assert api.device_status() == 0
