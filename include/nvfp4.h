@@ -212,6 +212,30 @@ nvfp4_status reset_sample(const float* logits, int M, int V, const uint8_t* step
                           float* H_out, float* T_out, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
 
+/*
+ * reset_sample without a workspace argument: same inputs, outputs and rule as
+ * reset_sample.  The ReSET pages have no counterpart to this function; it is
+ * for callers that cannot allocate device memory -- for example a plugin
+ * inside a serving engine that owns every device allocation through its own
+ * pool and only hands out fixed input/output buffers, or a latency-critical
+ * decode loop that must not call cudaMalloc because it synchronizes the device.
+ *
+ * The scratch (per-row counters and per-chunk partial sums) lives in a
+ * 131,328-byte array that the library reserves statically on every GPU that
+ * loads it, until the process exits.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   Limit: M * ceil(V / 2048) <= 4096 (M = 8 allows V up to 1,048,576);
+ *          larger calls return NVFP4_ERR_SHAPE without launching anything.
+ *   The first call on a device looks up that device's copy of the array
+ *   (cudaGetSymbolAddress); make it before any stream capture on that device.
+ *   Every call on a device uses the same array and clears its counters (a
+ *   256-byte memset on `stream`); calls that overlap on the GPU (for example
+ *   on two unordered streams) race and give wrong results -- order them.
+ */
+nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, const uint8_t* step_start,
+                                  const float* u, void* state, const reset_params* p, int32_t* token,
+                                  float* H_out, float* T_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,8 @@ SIGNATURES = {
     "reset_workspace_bytes": (_c_sz, [_c_i, _c_i]),
     "reset_sample": (_c_i, [_c_p, _c_i, _c_i, _c_p, _c_p, _c_p, ctypes.POINTER(ResetParams), _c_p, _c_p, _c_p,
                             _c_p, _c_sz, _c_p]),
+    "reset_sample_noalloc": (_c_i, [_c_p, _c_i, _c_i, _c_p, _c_p, _c_p, ctypes.POINTER(ResetParams), _c_p, _c_p,
+                                    _c_p, _c_p]),
 }
 
 _lib = None

@@ -12,7 +12,7 @@ from ._lib import ResetParams, check, lib, ptr, stream_handle
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_workspace_bytes", "nvfp4_bf16_gemv", "nvfp4_f32_to_bf16", "reset_state_bytes",
-    "reset_state_init", "reset_workspace_bytes", "reset_sample", "device_status", "GemvWorkspace",
+    "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
     "NVFP4Tensor", "ResetSampler",
 ]
 
@@ -159,6 +159,16 @@ def reset_sample(logits, step_start, u, state, params: ResetParams, token, H_out
     check(lib().reset_sample(ptr(logits), M, V, ptr(step_start), ptr(u), ptr(state), ctypes.byref(params),
                              ptr(token), ptr(H_out), ptr(T_out), ptr(workspace), workspace.numel(),
                              stream_handle(stream)), "reset_sample")
+
+
+def reset_sample_noalloc(logits, step_start, u, state, params: ResetParams, token, H_out, T_out, stream=None):
+    """reset_sample with its scratch in the library's static device array (no
+    workspace): for callers that may not allocate device memory.  Limit
+    M * ceil(V / 2048) <= 4096; calls that overlap on the GPU race."""
+    M, V = logits.shape
+    check(lib().reset_sample_noalloc(ptr(logits), M, V, ptr(step_start), ptr(u), ptr(state), ctypes.byref(params),
+                                     ptr(token), ptr(H_out), ptr(T_out), stream_handle(stream)),
+          "reset_sample_noalloc")
 
 
 class ResetSampler:

@@ -21,6 +21,8 @@
 // FP64 prefix sum.  It resets the row counter for the next call.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 NVFP4_DEFINE_ERROR_READER(nvfp4_internal_read_error_reset)
@@ -366,5 +368,68 @@ extern "C" nvfp4_status reset_sample(const float* logits, int M, int V, const ui
   reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
                                                         (int)state_stride(p->w), prm, token, H_out, T_out, parts,
                                                         counters);
+  return nvfp4_internal_cuda_status(cudaGetLastError());
+}
+
+// ---- allocation-free variant ------------------------------------------------------
+// Same kernel, with its scratch (row counters, then per-chunk partials) in a
+// file-scope device array instead of a caller workspace, for callers that may
+// not allocate device memory.  The array is reserved on every GPU that loads
+// the library, until the process exits.
+namespace {
+constexpr int kNoAllocMaxChunks = 4096;   // limit on M * ceil(V / 2048)
+constexpr size_t kNoAllocScratchBytes = kCounterBytes + (size_t)kNoAllocMaxChunks * sizeof(Part);   // 131,328
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_scratch_dev[kNoAllocMaxDevices] = {};
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_reset_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of this device's copy of the array (host code may not use the
+// array's name as a device pointer).  Looked up once per device.
+static cudaError_t noalloc_scratch_address(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_scratch_dev[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_reset_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_scratch_dev[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_scratch_dev[dev];
+  return cudaSuccess;
+}
+
+extern "C" nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, const uint8_t* step_start,
+                                             const float* u, void* state, const reset_params* p, int32_t* token,
+                                             float* H_out, float* T_out, cudaStream_t stream) {
+  if (!logits || !u || !state || !p || !token) return NVFP4_ERR_NULL;
+  if (M < 1 || M > kMaxRows) return NVFP4_ERR_RANGE;
+  if (V < 1 || V > (1 << 24)) return NVFP4_ERR_SHAPE;
+  if (!(p->t_low > 0.0f) || !(p->t_high > 0.0f) || p->w < 1 || p->w > kMaxW || !(p->tau0 == p->tau0))
+    return NVFP4_ERR_RANGE;
+  if (p->t_low == p->t_high) return NVFP4_ERR_RANGE;
+  if (!nvfp4_internal_aligned(logits, 16) || !nvfp4_internal_aligned(state, 16) || !nvfp4_internal_aligned(u, 4) ||
+      !nvfp4_internal_aligned(token, 4))
+    return NVFP4_ERR_ALIGN;
+  const int NC = (V + kChunk - 1) / kChunk;
+  if (NC > 1024 || (long long)M * NC > kNoAllocMaxChunks) return NVFP4_ERR_SHAPE;   // beyond the static scratch
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  uint8_t* scratch = nullptr;
+  cudaError_t e = noalloc_scratch_address(&scratch);
+  if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
+  // The array keeps the previous call's contents: clear the row counters.
+  e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
+  if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
+  Params prm{p->tau0, p->t_low, p->t_high, p->w};
+  reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
+                                                        (int)state_stride(p->w), prm, token, H_out, T_out,
+                                                        reinterpret_cast<Part*>(scratch + kCounterBytes),
+                                                        reinterpret_cast<unsigned int*>(scratch));
   return nvfp4_internal_cuda_status(cudaGetLastError());
 }
