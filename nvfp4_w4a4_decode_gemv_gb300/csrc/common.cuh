@@ -107,6 +107,15 @@ NVFP4_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32
       : "memory");
 }
 
+// GPU-scope acquire-release fence (cheaper than the sequentially consistent
+// __threadfence).
+NVFP4_DEVINL void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Programmatic dependent launch: wait for the preceding grid's completion and
+// memory, and let the next grid start launching.
+NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 NVFP4_DEVINL void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

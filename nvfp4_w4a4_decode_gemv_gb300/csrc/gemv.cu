@@ -84,8 +84,6 @@ NVFP4_DEVINL void unpack_w8(uint32_t w, uint32_t& lo, uint32_t& hi) {
   hi = prmt(kPosLo, kPosHi, w >> 16) | prmt(kNegLo, kNegHi, wx >> 16);
 }
 
-NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---- prep: activation codes -> records --------------------------------------
 // Record of token m, block b: int8 x = 2*e2m1 (4 words, element i in byte i%4 of
@@ -94,6 +92,7 @@ NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.lau
 __global__ void __launch_bounds__(256) xrec_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs,
                                                    int M, int K, uint4* __restrict__ xrec) {
   griddep_launch_dependents();
+  griddep_wait();               // the activation codes come from the preceding quantizer
   const int nb = K / 16;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M * nb) return;
@@ -222,14 +221,17 @@ NVFP4_DEVINL void flush_tile(const GemvArgs& a, int tile, long long first_unit_o
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int m = 0; m < M; ++m) __stcg(part + (size_t)(r * 32 + lane) * M + m, acc_get<R>(acc2[m], r));
-  __threadfence();
-  __syncwarp();
+  __syncwarp();                 // the warp's partial stores are ordered before lane 0's release
   unsigned int* cnt = a.counters + (size_t)(row0 / 32);
   int is_last = 0;
-  if (lane == 0) is_last = (atomicAdd(cnt, 1u) == (unsigned int)(last - first));
+  if (lane == 0) {
+    fence_acq_rel_gpu();        // release: this warp's partials before the count
+    is_last = (atomicAdd(cnt, 1u) == (unsigned int)(last - first));
+    if (is_last) fence_acq_rel_gpu();   // acquire: every contributor's partials
+  }
   is_last = __shfl_sync(0xffffffffu, is_last, 0);
   if (!is_last) return;
-  __threadfence();
+  __syncwarp();                 // the lanes' partial loads are ordered after lane 0's acquire
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     float sum[M];
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(32 * (TR / (32 * R) + 1)) gemv_kernel(const __
     fence_mbar_init();
   }
   __syncthreads();
+  if (threadIdx.x == 0) griddep_launch_dependents();   // the next kernel in the stream may start launching
 
   if (warp == WC) {
     // ---------------- producer warp ----------------
@@ -396,6 +399,12 @@ struct WsLayout {
 constexpr int kMaxN = 1 << 20;
 constexpr size_t kCounterBytes = align256((size_t)(kMaxN / 32 + 64) * sizeof(unsigned int));
 
+}  // namespace
+
+
+namespace {
+
+// [counters][activation records of the CUDA-core path][partial sums]
 WsLayout ws_layout(int M, int K) {
   WsLayout l;
   l.counters = 0;
@@ -466,6 +475,27 @@ int env_int(const char* name, int dflt) {
 nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
 bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
+cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
+                                   const uint8_t* ws, const float* wg, int N, int K, float* y, float* partials,
+                                   unsigned int* counters, int grid_cap, int max_ctas_per_sm, cudaStream_t stream);
+
+bool nvfp4_internal_encode_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                              uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+  return encode_2d(map, base, inner_bytes, rows, box_inner, box_rows,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+int nvfp4_internal_device_sms() { return device_sms(); }
+
+namespace {
+// GEMV path: "tc" = tensor cores (gemv_tc.cu), "cc" = CUDA cores (this file).
+bool use_tensor_cores(int M) {
+  (void)M;
+  const char* v = getenv("NVFP4_GEMV_PATH");
+  if (v && v[0] == 'c') return false;
+  return true;
+}
+}  // namespace
 
 extern "C" size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
@@ -488,6 +518,11 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   if (ds != NVFP4_OK) return ds;
 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  if (use_tensor_cores(M)) {
+    return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
+        xq, xs, xg, M, wq, ws, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
+        reinterpret_cast<unsigned int*>(wsb + wl.counters), env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
+  }
   GemvArgs a;
   a.xrec = wsb + wl.xrec;
   a.xg = xg;
@@ -503,8 +538,16 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   a.U = 0;
 
   const int nrec = M * (K / 16);
-  xrec_kernel<<<(nrec + 255) / 256, 256, 0, stream>>>(xq, xs, M, K, reinterpret_cast<uint4*>(wsb + wl.xrec));
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3((nrec + 255) / 256);
+  pcfg.blockDim = dim3(256);
+  pcfg.stream = stream;
+  cudaLaunchAttribute pattr[1];
+  pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pattr[0].val.programmaticStreamSerializationAllowed = 1;
+  pcfg.attrs = pattr;
+  pcfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&pcfg, xrec_kernel, xq, xs, M, K, reinterpret_cast<uint4*>(wsb + wl.xrec));
   if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
 
   const int variant = env_int("NVFP4_GEMV_VARIANT", 0);

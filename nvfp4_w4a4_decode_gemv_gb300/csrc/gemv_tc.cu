@@ -1,0 +1,445 @@
+// Small-M NVFP4 W4A4 GEMV on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Same result as the CUDA-core kernel (gemv.cu):
+//   y[m, n] = xg * wg * sum_k e2m1(x[m,k]) e4m3(sx[m,k/16]) e2m1(w[n,k]) e4m3(sw[n,k/16]).
+//
+// The pages reject tensor cores for decode because Blackwell's NVFP4 MMA tile
+// is 128 rows along the token dimension, so at M <= 8 at most 8 of 128 rows do
+// useful work (ReSET project page, "Why a CUDA-core NVFP4 kernel?"; reading
+// note §5.1).  Swapping the operands removes that argument: the 128-row side
+// of `tcgen05.mma ... kind::mxf4nvf4.block_scale.scale_vec::4X` takes 128
+// WEIGHT rows, the tokens sit on the narrow N side (N = 16, M <= 8 used).  The
+// tensor core then consumes the E2M1 codes and the E4M3 block scales as they
+// are stored, so no CUDA-core instruction is spent per weight and the kernel
+// is a pure HBM stream.  What the pages' design wanted -- every weight tile
+// read from HBM once and used for every token (C1), no dequantized buffer (C3)
+// -- holds here by construction.
+//
+// Per 256-K stage of a 128-row tile (one TMA ring slot):
+//   producer warp   TMA: weight codes 128 x 128 B (128-byte swizzle), weight
+//                   scales 128 x 16 B, token codes 16 x 128 B (swizzled; rows
+//                   >= M arrive as zeros) and token scales 16 x 16 B.  The
+//                   weight tiles of the first stages are issued before waiting
+//                   on the preceding kernel (programmatic dependent launch), so
+//                   they overlap the quantizer that produces the tokens.
+//   4 scale warps   scale bytes -> TMEM with single-column stores.  An MMA
+//                   whose weight-scale address is column A reads the 4 block
+//                   scales of weight row r from lane r, column A + r/32 (one
+//                   byte per 16-element block); with token-scale address B it
+//                   reads token n's scales, for the accumulator rows of lane
+//                   quadrant p, from lane 32p + n, column B.  So MMA q of a
+//                   stage uses A = S0 + 4q, B = S1 + 4q; row r's word goes to
+//                   column S0 + 4q + r/32, token n's word to lane 32p + n of
+//                   column S1 + 4q in every quadrant p.
+//   MMA thread      4 MMAs of K = 64 into a 128 x 16 FP32 TMEM accumulator;
+//                   tcgen05.commit frees the slot
+//   4 epilogue warps read the accumulator (double buffered) at tile ends and
+//                   write y, or partial sums for the Stream-K fix-up
+// Work split and fix-up follow gemv.cu (Stream-K over [tile x 256-K] units,
+// the last arriver sums partials in CTA order).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kTR = 128;                    // weight rows per tile = MMA M
+constexpr int kNT = 16;                     // MMA N: token rows (M <= 8 used, rest zero)
+constexpr int kChunk = 256;                 // K per stage = 4 MMAs of K = 64
+constexpr int kCodeBytes = kTR * 128;       // 16384
+constexpr int kActCodeBytes = kNT * 128;    // 2048
+constexpr int kActScaleBytes = kNT * 16;    // 256
+constexpr int kScaleBytes = kTR * 16;       // 2048
+constexpr int kActBytes = kActCodeBytes + kActScaleBytes;   // 2304: token codes + scales per stage
+// slot: [A codes 16384][B codes 2048][B scales 256][A scales 2048], 1024-aligned slots
+constexpr int kOffB = kCodeBytes;
+constexpr int kOffSB = kOffB + kActCodeBytes;
+constexpr int kOffSA = kOffSB + kActScaleBytes;             // 18688 (128-byte aligned)
+constexpr int kSlot = ((kOffSA + kScaleBytes + 1023) / 1024) * 1024;   // 21504
+constexpr uint32_t kStageTx = kCodeBytes + kScaleBytes + kActBytes;
+constexpr int kWarps = 10;                  // 0 producer, 1 MMA, 2-5 scale writers, 6-9 epilogue
+constexpr int kThreads = 32 * kWarps;
+constexpr uint32_t kTmemCols = 256;         // D0 [0,16), D1 [16,32), 32 scale columns per stage from 32 (S <= 7)
+constexpr uint32_t kColSF = 32;             // stage s: A scales at 32+32s+[0,16), B scales at 32+32s+16+[0,13)
+// Instruction descriptor: E2M1 x E2M1 (format 1), UE4M3 scales, K-major A and B,
+// N = 16 (bits 17-22: N >> 3), M = 128 (bits 24-28: M >> 4), dense.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
+
+struct TcArgs {
+  const float* xg;
+  const float* wg;
+  float* y;
+  float* partials;               // [G][2][128][M]
+  unsigned int* counters;        // one per 32-row group
+  int M, N, K, C, RT;
+  long long U;
+};
+
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+NVFP4_DEVINL uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+NVFP4_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+NVFP4_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+NVFP4_DEVINL void mma_mxf4nvf4(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(da), "l"(db), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+// One 32-bit column for the warp's 32 lanes.
+NVFP4_DEVINL void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+NVFP4_DEVINL void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { return (q * U) / G; }
+NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { return ((x + 1) * G - 1) / U; }
+
+// ---- epilogue: accumulator rows -> y or partial sums ---------------------------
+template <int M>
+NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, long long u0, int quad, int lane, const float (&acc)[kNT]) {
+  const long long G = gridDim.x, C = a.C;
+  const long long first = cta_of_unit((long long)tile * C, a.U, G);
+  const long long last = cta_of_unit((long long)tile * C + C - 1, a.U, G);
+  const float yscale = __fmul_rn(__ldg(a.xg), __ldg(a.wg));
+  const int row0 = tile * kTR + quad * 32;
+  const int n = row0 + lane;
+  if (first == last) {
+    if (n < a.N) {
+#pragma unroll
+      for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = acc[m] * yscale;
+    }
+    return;
+  }
+  const int my_slot = (tile == (int)(u0 / C)) ? 0 : 1;
+  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * kTR + quad * 32 + lane) * M;
+#pragma unroll
+  for (int m = 0; m < M; ++m) __stcg(part + m, acc[m]);
+  __syncwarp();                 // the warp's partial stores are ordered before lane 0's release
+  unsigned int* cnt = a.counters + (size_t)(row0 / 32);
+  int is_last = 0;
+  if (lane == 0) {
+    fence_acq_rel_gpu();        // release: this warp's partials before the count
+    is_last = (atomicAdd(cnt, 1u) == (unsigned int)(last - first));
+    if (is_last) fence_acq_rel_gpu();   // acquire: every contributor's partials
+  }
+  is_last = __shfl_sync(0xffffffffu, is_last, 0);
+  if (!is_last) return;
+  __syncwarp();                 // the lanes' partial loads are ordered after lane 0's acquire
+  float sum[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) sum[m] = 0.0f;
+  for (long long q = first; q <= last; ++q) {
+    const int qslot = (tile == (int)(unit_start(q, a.U, G) / C)) ? 0 : 1;
+    const float* pq = a.partials + (((size_t)q * 2 + qslot) * kTR + quad * 32 + lane) * M;
+#pragma unroll
+    for (int m = 0; m < M; ++m) sum[m] += __ldcg(pq + m);
+  }
+  if (n < a.N) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = sum[m] * yscale;
+  }
+  if (lane == 0) *cnt = 0u;
+}
+
+template <int M, int S>
+__global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                                                              const __grid_constant__ CUtensorMap tm_scales,
+                                                              const __grid_constant__ CUtensorMap tm_xcodes,
+                                                              const __grid_constant__ CUtensorMap tm_xscales,
+                                                              const TcArgs a) {
+  static_assert(S >= 2 && kColSF + 32 * S <= kTmemCols, "scale columns must fit the TMEM allocation");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kSlot);
+  uint64_t* sf_ready = full + S;
+  uint64_t* empty = sf_ready + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long G = gridDim.x;
+  const long long u0 = unit_start(blockIdx.x, a.U, G);
+  const long long u1 = unit_start(blockIdx.x + 1, a.U, G);
+  const int nunits = (int)(u1 - u0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&sf_ready[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&acc_full[d], 1);
+      mbar_init(&acc_empty[d], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();   // the next kernel in the stream may start launching
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0 && nunits > 0) {
+      prefetch_tmap(&tm_codes);
+      prefetch_tmap(&tm_scales);
+      prefetch_tmap(&tm_xcodes);
+      prefetch_tmap(&tm_xscales);
+      const int pre = nunits < S ? nunits : S;
+      // Weight tiles do not depend on the preceding kernel: issue them first.
+      for (int k = 0; k < pre; ++k) {
+        const long long u = u0 + k;
+        const int tile = (int)(u / a.C), c = (int)(u % a.C);
+        uint8_t* slot = smem + k * kSlot;
+        mbar_arrive_expect_tx(&full[k], kStageTx);
+        tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[k]);
+        tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
+      }
+      griddep_wait();          // the token codes and scales come from the preceding quantizer
+      for (int k = 0; k < pre; ++k) {
+        const int c = (int)((u0 + k) % a.C);
+        uint8_t* slot = smem + k * kSlot;
+        tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[k]);      // rows >= M arrive as zeros
+        tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
+      }
+      int issued = pre;
+      for (int k = pre; k < nunits; ++k) {
+        const int s = k % S;
+        if (!mbar_wait(&empty[s], ((k / S) - 1) & 1)) break;
+        const long long u = u0 + k;
+        const int tile = (int)(u / a.C), c = (int)(u % a.C);
+        uint8_t* slot = smem + s * kSlot;
+        mbar_arrive_expect_tx(&full[s], kStageTx);
+        tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[s]);
+        tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
+        tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[s]);
+        tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
+        issued = k + 1;
+      }
+      for (int k = (issued > S ? issued - S : 0); k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && nunits > 0) {
+      int tile_idx = -1;
+      int cur_tile = -1;
+      bool ok = true;
+      int issued = 0;
+      for (int k = 0; k < nunits && ok; ++k) {
+        const int s = k % S;
+        const long long u = u0 + k;
+        const int tile = (int)(u / a.C);
+        const bool first_of_tile = (tile != cur_tile);
+        if (first_of_tile) {
+          cur_tile = tile;
+          ++tile_idx;
+          const int d = tile_idx & 1;
+          if (tile_idx >= 2 && !mbar_wait(&acc_empty[d], ((tile_idx >> 1) - 1) & 1)) { ok = false; break; }
+        }
+        if (!mbar_wait(&full[s], (k / S) & 1) || !mbar_wait(&sf_ready[s], (k / S) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
+        const uint32_t sa = smem_u32(smem + s * kSlot);
+        const uint32_t sfa = tmem + kColSF + 32u * s;
+        const uint32_t sfb = sfa + 16u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mma_mxf4nvf4(d_tmem, smem_desc_sw128(sa + 32 * q), smem_desc_sw128(sa + kOffB + 32 * q), sfa + 4u * q,
+                       sfb + 4u * q, (first_of_tile && q == 0) ? 0u : 1u);
+        }
+        mma_commit(&empty[s]);
+        issued = k + 1;
+        const bool last_of_tile = (k + 1 == nunits) || ((int)((u + 1) / a.C) != tile);
+        if (last_of_tile) mma_commit(&acc_full[tile_idx & 1]);
+      }
+      // Do not leave with MMAs in flight: wait (bounded) for the last commit.
+      if (issued > 0) mbar_wait(&empty[(issued - 1) % S], ((issued - 1) / S) & 1);
+    }
+  } else if (warp < 6) {
+    // ---------------- scale writers: rows 32*quad .. 32*quad + 31 ----------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    for (int k = 0; k < nunits; ++k) {
+      const int s = k % S;
+      if (!mbar_wait(&full[s], (k / S) & 1)) break;
+      const uint8_t* slot = smem + s * kSlot;
+      const uint4 sa = *reinterpret_cast<const uint4*>(slot + kOffSA + row * 16);
+      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 32u * s + (uint32_t)quad;
+      tmem_st1(ta, sa.x);
+      tmem_st1(ta + 4u, sa.y);
+      tmem_st1(ta + 8u, sa.z);
+      tmem_st1(ta + 12u, sa.w);
+      // Token scales: the MMA reads token n's scales for accumulator rows of
+      // quadrant p from lane 32p + n, so every quadrant holds a copy.
+      uint4 sb = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < kNT) sb = *reinterpret_cast<const uint4*>(slot + kOffSB + lane * 16);
+      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 32u * s + 16u;
+      tmem_st1(tb, sb.x);
+      tmem_st1(tb + 4u, sb.y);
+      tmem_st1(tb + 8u, sb.z);
+      tmem_st1(tb + 12u, sb.w);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_ready[s]);
+    }
+  } else {
+    // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
+    const int quad = warp & 3;
+    griddep_wait();
+    int tile_idx = -1, cur_tile = -1;
+    for (int k = 0; k < nunits; ++k) {
+      const long long u = u0 + k;
+      const int tile = (int)(u / a.C);
+      if (tile != cur_tile) {
+        cur_tile = tile;
+        ++tile_idx;
+      }
+      const bool last_of_tile = (k + 1 == nunits) || ((int)((u + 1) / a.C) != tile);
+      if (!last_of_tile) continue;
+      const int d = tile_idx & 1;
+      if (!mbar_wait(&acc_full[d], (tile_idx >> 1) & 1)) break;
+      tc_fence_after();
+      uint32_t r[kNT];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(d * kNT)));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[d]);
+      float acc[kNT];
+#pragma unroll
+      for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
+      tc_flush<M>(a, tile, u0, quad, lane, acc);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+template <int S>
+constexpr size_t tc_smem_bytes() {
+  return (size_t)S * kSlot + 1024 + (3 * S + 4) * sizeof(uint64_t) + 16;
+}
+
+}  // namespace
+
+// Defined in gemv.cu.
+bool nvfp4_internal_encode_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                              uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+int nvfp4_internal_device_sms();
+
+struct TcMaps {
+  CUtensorMap w_codes, w_scales, x_codes, x_scales;
+};
+
+template <int M, int S>
+static cudaError_t launch_tc(const TcMaps& mp, const TcArgs& a, cudaStream_t stream, int grid_cap,
+                             int max_ctas_per_sm) {
+  static int per_sm_fit = -1;
+  constexpr size_t smem = tc_smem_bytes<S>();
+  auto kern = gemv_tc_kernel<M, S>;
+  if (per_sm_fit < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    int dev = 0, smem_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    // CTAs per SM: shared memory (plus the 1 KB the driver reserves per CTA) and TMEM columns.
+    int by_smem = smem_sm > 0 ? (int)(smem_sm / (smem + 1024)) : 1;
+    int by_tmem = 512 / (int)kTmemCols;
+    per_sm_fit = by_smem < by_tmem ? by_smem : by_tmem;
+    if (per_sm_fit < 1) per_sm_fit = 1;
+  }
+  int per_sm = per_sm_fit < max_ctas_per_sm ? per_sm_fit : max_ctas_per_sm;
+  long long G = (long long)per_sm * nvfp4_internal_device_sms();
+  if (grid_cap > 0 && G > grid_cap) G = grid_cap;
+  if (G > a.U) G = a.U;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mp.w_codes, mp.w_scales, mp.x_codes, mp.x_scales, a);
+}
+
+template <int M>
+static cudaError_t launch_tc_m(int stages, const TcMaps& mp, const TcArgs& a, cudaStream_t stream, int grid_cap,
+                               int max_ctas_per_sm) {
+  switch (stages) {
+    case 5: return launch_tc<M, 5>(mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 6: return launch_tc<M, 6>(mp, a, stream, grid_cap, max_ctas_per_sm);
+    default: return launch_tc<M, 4>(mp, a, stream, grid_cap, max_ctas_per_sm);
+  }
+}
+
+// Tensor-core GEMV; the caller has validated the arguments.
+cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
+                                   const uint8_t* ws, const float* wg, int N, int K, float* y, float* partials,
+                                   unsigned int* counters, int grid_cap, int max_ctas_per_sm, cudaStream_t stream) {
+  const char* st = getenv("NVFP4_GEMV_TC_STAGES");   // tuning knob: 4 (default), 5 or 6
+  const int stages = st ? atoi(st) : 4;
+  TcMaps mp;
+  if (!nvfp4_internal_encode_2d(&mp.w_codes, wq, (uint64_t)K / 2, (uint64_t)N, 128, kTR, true) ||
+      !nvfp4_internal_encode_2d(&mp.w_scales, ws, (uint64_t)K / 16, (uint64_t)N, 16, kTR, false) ||
+      !nvfp4_internal_encode_2d(&mp.x_codes, xq, (uint64_t)K / 2, (uint64_t)M, 128, kNT, true) ||
+      !nvfp4_internal_encode_2d(&mp.x_scales, xs, (uint64_t)K / 16, (uint64_t)M, 16, kNT, false))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.xg = xg;
+  a.wg = wg;
+  a.y = y;
+  a.partials = partials;
+  a.counters = counters;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.C = K / kChunk;
+  a.RT = (N + kTR - 1) / kTR;
+  a.U = (long long)a.RT * a.C;
+  switch (M) {
+    case 1: return launch_tc_m<1>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 2: return launch_tc_m<2>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 3: return launch_tc_m<3>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 4: return launch_tc_m<4>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 5: return launch_tc_m<5>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 6: return launch_tc_m<6>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    case 7: return launch_tc_m<7>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+    default: return launch_tc_m<8>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+  }
+}

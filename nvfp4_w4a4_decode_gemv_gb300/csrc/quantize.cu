@@ -22,8 +22,9 @@
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxCluster = 8;
+constexpr int kThreads = 256;          // multi-launch (weight-sized) path
+constexpr int kCThreads = 512;         // single-launch cluster path
+constexpr int kMaxCluster = 16;        // non-portable cluster size, capped by the device
 constexpr float kGlobalDivisor = 2688.0f;   // 448 * 6
 
 // ---- element sources: block b of a [rows, K] tensor -> 16 floats ----------
@@ -121,15 +122,20 @@ NVFP4_DEVINL uint32_t quant_block(const float v[16], float bm, float g, uint2& c
 
 // ---- single-launch cluster path --------------------------------------------
 template <class Src, int NB>
-__global__ void __launch_bounds__(kThreads) quant_cluster_kernel(Src src, long nblocks, uint8_t* codes,
-                                                                 uint8_t* scales, float* global) {
-  __shared__ float s_warp[kThreads / 32];
+__global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long nblocks, uint8_t* codes,
+                                                                  uint8_t* scales, float* global) {
+  __shared__ float s_warp[kCThreads / 32];
   __shared__ float s_cta_max;
   __shared__ float s_amax;
+  // Programmatic dependent launch: the input may come from the preceding
+  // kernel; once it is complete, let the next kernel (the GEMV) start launching
+  // so that its weight loads overlap this one.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t rank = cluster_ctarank();
   const uint32_t csize = gridDim.x;          // the whole grid is one cluster
-  const long T = (long)csize * kThreads;
-  const long gt = (long)rank * kThreads + threadIdx.x;
+  const long T = (long)csize * kCThreads;
+  const long gt = (long)rank * kCThreads + threadIdx.x;
 
   float v[NB][16];
   float bm[NB];
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) quant_cluster_kernel(Src src, long n
   __syncthreads();
   if (threadIdx.x == 0) {
     float m = 0.0f;
-    for (int w = 0; w < kThreads / 32; ++w) m = fmaxf(m, s_warp[w]);
+    for (int w = 0; w < kCThreads / 32; ++w) m = fmaxf(m, s_warp[w]);
     s_cta_max = m;
   }
   cluster_sync();                            // every CTA's s_cta_max is visible cluster-wide
@@ -217,19 +223,53 @@ __global__ void finalize_global_kernel(float* global) {
 __global__ void zero_global_kernel(float* global) { *global = 0.0f; }
 
 template <class Src, int NB>
+int max_cluster() {
+  static int cap = 0;
+  if (cap == 0) {
+    auto kern = quant_cluster_kernel<Src, NB>;
+    cap = 8;                                    // portable size, always available
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kMaxCluster);
+      cfg.blockDim = dim3(kCThreads);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kMaxCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxPotentialClusterSize(&n, kern, &cfg) == cudaSuccess && n > cap) cap = n;
+      if (cap > kMaxCluster) cap = kMaxCluster;
+    }
+    cudaGetLastError();
+  }
+  return cap;
+}
+
+template <class Src, int NB>
 cudaError_t launch_cluster(const Src& src, long nblocks, int csize, uint8_t* codes, uint8_t* scales,
                            float* global, cudaStream_t stream) {
+  static bool non_portable = false;   // per instantiation: clusters above 8 CTAs need the opt-in
+  if (csize > 8 && !non_portable) {
+    cudaError_t e = cudaFuncSetAttribute(quant_cluster_kernel<Src, NB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    non_portable = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kCThreads);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, quant_cluster_kernel<Src, NB>, src, nblocks, codes, scales, global);
 }
 
@@ -242,16 +282,19 @@ cudaError_t quantize_dispatch(const Src& src, long nblocks, uint8_t* codes, uint
     zero_global_kernel<<<1, 1, 0, stream>>>(global);
     return cudaGetLastError();
   }
-  const long per_cta = kThreads;
-  if (nblocks <= (long)kMaxCluster * per_cta * 8) {
-    int csize = (int)((nblocks + per_cta - 1) / per_cta);
-    if (csize > kMaxCluster) csize = kMaxCluster;
-    const long T = (long)csize * per_cta;
+  // One cluster: CTAs of kCThreads threads, each thread holding NB blocks in
+  // registers; aim at <= 2 blocks per thread, up to the device's cluster limit.
+  const int cap = max_cluster<Src, 8>();
+  if (nblocks <= (long)cap * kCThreads * 8) {
+    long csize = (nblocks + 2L * kCThreads - 1) / (2L * kCThreads);
+    if (csize < 1) csize = 1;
+    if (csize > cap) csize = cap;
+    const long T = csize * kCThreads;
     const long nb = (nblocks + T - 1) / T;
-    if (nb <= 1) return launch_cluster<Src, 1>(src, nblocks, csize, codes, scales, global, stream);
-    if (nb <= 2) return launch_cluster<Src, 2>(src, nblocks, csize, codes, scales, global, stream);
-    if (nb <= 4) return launch_cluster<Src, 4>(src, nblocks, csize, codes, scales, global, stream);
-    return launch_cluster<Src, 8>(src, nblocks, csize, codes, scales, global, stream);
+    if (nb <= 1) return launch_cluster<Src, 1>(src, nblocks, (int)csize, codes, scales, global, stream);
+    if (nb <= 2) return launch_cluster<Src, 2>(src, nblocks, (int)csize, codes, scales, global, stream);
+    if (nb <= 4) return launch_cluster<Src, 4>(src, nblocks, (int)csize, codes, scales, global, stream);
+    return launch_cluster<Src, 8>(src, nblocks, (int)csize, codes, scales, global, stream);
   }
   if (g_num_sms == 0) {
     int dev = 0;

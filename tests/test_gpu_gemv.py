@@ -16,6 +16,13 @@ from tests.gpu_util import assert_within, bits, to_np
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["tc", "cc"])
+def gemv_path(request, monkeypatch):
+    """Every GEMV test runs on the tensor-core path and on the CUDA-core path."""
+    monkeypatch.setenv("NVFP4_GEMV_PATH", request.param)
+    return request.param
+
+
 def _run(M, N, K, seed, w_std=synth.W_STD):
     x = synth.activations(M, K, seed)
     w = synth.weights(N, K, seed + 1000, std=w_std)
