@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
+    ap.add_argument("--weights", default="packed", choices=["packed", "rowmajor"],
+                    help="weight layout: packed (nvfp4_pack_weights, offline) or row-major codes/scales")
     return ap.parse_args()
 
 
@@ -150,7 +152,13 @@ def max_over_ranks(world, v):
 
 
 # ---------------------------------------------------------------------------
-def build_problem(shapes, Ms, rank, only=None):
+def gemv_call(api, c, w, ws):
+    if isinstance(w, api.NVFP4PackedWeight):
+        return api.nvfp4_gemv_smallm_packed(c["xq"], w, y=c["y"], workspace=ws)
+    return api.nvfp4_gemv_smallm(c["xq"], w, y=c["y"], workspace=ws)
+
+
+def build_problem(shapes, Ms, rank, only=None, packed=True):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     dev = torch.device("cuda")
     weights = {}
@@ -160,6 +168,9 @@ def build_problem(shapes, Ms, rank, only=None):
         wb = (torch.randn((N, K), generator=g, device=dev, dtype=torch.float32) * synth.W_STD).to(torch.bfloat16)
         weights[name] = api.nvfp4_quantize_act(wb)
         del wb
+        if packed:                   # offline weight preparation, outside any timed region
+            weights[name] = api.nvfp4_pack_weights(weights[name])
+            torch.cuda.synchronize()
     calls = []
     for M in Ms:
         for i, (name, K, N) in enumerate(shapes):
@@ -178,7 +189,7 @@ def build_problem(shapes, Ms, rank, only=None):
 def run_ours(args, world, rank):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     shapes, Ms = WORKLOADS[args.workload]
-    weights, calls, ws = build_problem(shapes, Ms, rank, args.only)
+    weights, calls, ws = build_problem(shapes, Ms, rank, args.only, packed=args.weights == "packed")
     groups = {}
     for c in calls:
         groups.setdefault(c["M"], []).append(c)
@@ -190,7 +201,7 @@ def run_ours(args, world, rank):
 
     def gemv_all(cs):
         for c in cs:
-            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            gemv_call(api, c, weights[c["name"]], ws)
 
     for M in order:                  # initialises kernel attributes outside capture
         quantize_all(groups[M])
@@ -244,6 +255,12 @@ def run_ours(args, world, rank):
                        "gemv_gbs": round(sum(c["gemv_bytes"] for c in groups[M]) / (gemv_ms[M] * 1e-3) / 1e9, 1)}
              for M in order}
     peak, peak_kind = measured_peaks()
+    cuda_cores = args.weights == "rowmajor" and os.environ.get("NVFP4_GEMV_PATH", "tc").startswith("c")
+    # per call: the quantizer and the GEMV (+ the activation-record kernel on the CUDA-core path)
+    launches_per_call = 3 if cuda_cores else 2
+    gemv_name = ("nvfp4_gemv_smallm_packed (tensor-core GEMV kernel)" if args.weights == "packed" else
+                 "nvfp4_gemv_smallm (" + ("activation-record + CUDA-core GEMV kernels" if cuda_cores
+                                          else "tensor-core GEMV kernel") + ")")
     achieved = gemv_bytes_total / (gemv_ms_total * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -252,17 +269,18 @@ def run_ours(args, world, rank):
         "data": "synthetic (seeded N(0,0.02) weights; N(0,1) activations with 1% x20 outlier channels)",
         "config": {"workload": f"{args.workload} decode projections qkv/o/gate_up/down, M={Ms[0]}..{Ms[-1]}, "
                                f"quantize+GEMV per call",
-                   "calls_per_step": len(calls), "weights_resident_gb": round(sum(
-                       w.codes.numel() + w.scales.numel() for w in weights.values()) / 1e9, 3),
+                   "calls_per_step": len(calls), "weights": args.weights, "weights_resident_gb": round(sum(
+                       w.packed.numel() if hasattr(w, "packed") else w.codes.numel() + w.scales.numel()
+                       for w in weights.values()) / 1e9, 3),
                    "l2": "inputs larger than L2: >=245 MB of other weights between two uses of one matrix",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "nvfp4_gemv_smallm (activation prep + GEMV kernels): algorithmic bytes of all GEMV "
-                               "calls / their event-timed duration in the timed region",
+                     "kernel": f"{gemv_name}: algorithmic bytes of all GEMV calls / their event-timed duration "
+                               "in the timed region",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clocks,
-        "gpu_launches": len(calls) * 3 * args.steps,   # per call: quantize, activation prep, GEMV
+        "gpu_launches": len(calls) * launches_per_call * args.steps,
         "per_m": per_m,
         "per_call_cold_l2": per_call,
     }
@@ -283,7 +301,7 @@ def cold_per_call(calls, weights, ws, reps=3):
             e[0].record()
             api.nvfp4_quantize_act(c["x"], out=c["xq"])
             e[1].record()
-            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            gemv_call(api, c, weights[c["name"]], ws)
             e[2].record()
             torch.cuda.synchronize()
             q_us.append(e[0].elapsed_time(e[1]) * 1e3)
@@ -306,7 +324,7 @@ def run_e2e(args, calls, weights, ws):
         for j, c in enumerate(calls):
             dev_x[j].copy_(host_x[j], non_blocking=True)
             api.nvfp4_quantize_act(dev_x[j], out=c["xq"])
-            api.nvfp4_gemv_smallm(c["xq"], weights[c["name"]], y=c["y"], workspace=ws)
+            gemv_call(api, c, weights[c["name"]], ws)
             host_y[j].copy_(c["y"], non_blocking=True)
 
     for _ in range(max(3, args.warmup)):

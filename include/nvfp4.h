@@ -149,6 +149,39 @@ nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float
                                float* y, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/*
+ * Packed weights.  The pages quantize the weights offline, from the BF16
+ * checkpoint (ReSET reading note §6.1), and leave their memory layout to the
+ * kernel.  nvfp4_pack_weights rewrites wq/ws into blocks of
+ * 18432 bytes, one per [128-row tile t] x [256-K chunk c], stored in the order
+ * (t, c) with c fastest, so that a GEMV streams each tile chunk as one
+ * contiguous read:
+ *   bytes [0, 16384)      codes of rows 128t .. 128t+127, K-bytes [128c, 128c+128):
+ *                         the 16-byte piece j (0..7) of tile row r (0..127) at
+ *                         r*128 + ((j XOR (r mod 8)) * 16)
+ *   bytes [16384, 18432)  scales of those rows for blocks [16c, 16c+16): tile
+ *                         row r at 16384 + 16 r
+ * Rows n >= N of the last tile are zero.  The packed image holds the same
+ * bytes as wq and ws (plus the zero rows); nothing is recomputed.
+ *
+ * nvfp4_packed_weight_bytes(N, K) = ceil(N/128) * (K/256) * 18432, or 0 for an
+ * invalid shape (N 1 .. 2^20, K a positive multiple of 256).
+ * nvfp4_pack_weights: wq [N, K/2], ws [N, K/16], packed (written) of at least
+ * nvfp4_packed_weight_bytes bytes, all device, 16-byte aligned; asynchronous on
+ * `stream`; wq/ws must not overlap `packed`.
+ * nvfp4_gemv_smallm_packed: nvfp4_gemv_smallm with the weights given packed;
+ * same result bits for the same inputs on the tensor-core path, same
+ * workspace contract.
+ */
+size_t nvfp4_packed_weight_bytes(int N, int K);
+
+nvfp4_status nvfp4_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
+                                size_t packed_bytes, cudaStream_t stream);
+
+nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                                      const uint8_t* wpacked, const float* wg, int N, int K, float* y,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* BF16 GEMV (the decode step's lm_head)                                       */
 /* ------------------------------------------------------------------------ */

@@ -38,6 +38,9 @@ SIGNATURES = {
     "nvfp4_silu_mul_quantize": (_c_i, [_c_p, _c_i, _c_i, _c_p, _c_p, _c_p, _c_p]),
     "nvfp4_gemv_workspace_bytes": (_c_sz, [_c_i, _c_i, _c_i]),
     "nvfp4_gemv_smallm": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
+    "nvfp4_packed_weight_bytes": (_c_sz, [_c_i, _c_i]),
+    "nvfp4_pack_weights": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_sz, _c_p]),
+    "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_bf16_gemv": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "nvfp4_f32_to_bf16": (_c_i, [_c_p, _c_sz, _c_p, _c_p]),
     "reset_state_bytes": (_c_sz, [_c_i, _c_i]),

@@ -11,7 +11,8 @@ from ._lib import ResetParams, check, lib, ptr, stream_handle
 
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
-    "nvfp4_gemv_workspace_bytes", "nvfp4_bf16_gemv", "nvfp4_f32_to_bf16", "reset_state_bytes",
+    "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
+    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_f32_to_bf16", "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
     "NVFP4Tensor", "ResetSampler",
 ]
@@ -122,6 +123,43 @@ def nvfp4_gemv_smallm(x: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor | None = N
     check(lib().nvfp4_gemv_smallm(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.codes), ptr(w.scales),
                                   ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(), stream_handle(stream)),
           "nvfp4_gemv_smallm")
+    return y
+
+
+class NVFP4PackedWeight:
+    """An NVFP4 weight [N, K] in the packed layout of nvfp4_pack_weights: packed uint8 [bytes], global float32 [1]."""
+
+    def __init__(self, packed, global_scale, N: int, K: int):
+        self.packed, self.global_scale, self.N, self.K = packed, global_scale, N, K
+
+
+def nvfp4_packed_weight_bytes(N: int, K: int) -> int:
+    return int(lib().nvfp4_packed_weight_bytes(N, K))
+
+
+def nvfp4_pack_weights(w: NVFP4Tensor, out: torch.Tensor | None = None, stream=None) -> NVFP4PackedWeight:
+    """Row-major NVFP4 weight -> packed layout (same bytes, tile-chunk blocks of 18432 B)."""
+    N, K = w.rows, w.K
+    need = nvfp4_packed_weight_bytes(N, K)
+    if need == 0:
+        raise ValueError(f"unsupported weight shape N={N} K={K}")
+    out = out if out is not None else torch.empty(need, dtype=torch.uint8, device=w.codes.device)
+    check(lib().nvfp4_pack_weights(ptr(w.codes), ptr(w.scales), N, K, ptr(out), out.numel(), stream_handle(stream)),
+          "nvfp4_pack_weights")
+    return NVFP4PackedWeight(out, w.global_scale, N, K)
+
+
+def nvfp4_gemv_smallm_packed(x: NVFP4Tensor, w: NVFP4PackedWeight, y: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """nvfp4_gemv_smallm with the weight packed."""
+    M, N, K = x.rows, w.N, x.K
+    if w.K != K:
+        raise ValueError("x and w disagree on K")
+    y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.codes.device)
+    ws = workspace if workspace is not None else _ws_for(x.codes.device).get(M, N, K)
+    check(lib().nvfp4_gemv_smallm_packed(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.packed),
+                                         ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(),
+                                         stream_handle(stream)), "nvfp4_gemv_smallm_packed")
     return y
 
 

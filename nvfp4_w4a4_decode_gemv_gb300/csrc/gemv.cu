@@ -402,18 +402,24 @@ constexpr size_t kCounterBytes = align256((size_t)(kMaxN / 32 + 64) * sizeof(uns
 }  // namespace
 
 
+// Defined in gemv_tc.cu.
+size_t nvfp4_internal_tc_partial_bytes(int M, int N, int K);
+
 namespace {
 
-// [counters][activation records of the CUDA-core path][partial sums]
-WsLayout ws_layout(int M, int K) {
+// [counters][activation records of the CUDA-core path][partial sums of either path]
+WsLayout ws_layout(int M, int N, int K) {
   WsLayout l;
   l.counters = 0;
   l.xrec = kCounterBytes;
   l.partials = l.xrec + align256((size_t)M * (K / 16) * kRecBytes);
   const size_t gmax = (size_t)device_sms() * kMaxCtasPerSm;
-  l.total = l.partials + align256(gmax * 2 * kMaxTileRows * (size_t)M * sizeof(float));
+  const size_t cc = gmax * 2 * kMaxTileRows * (size_t)M * sizeof(float);
+  const size_t tc = nvfp4_internal_tc_partial_bytes(M, N, K);
+  l.total = l.partials + align256(cc > tc ? cc : tc);
   return l;
 }
+
 
 template <int M, int TR, int R, int S>
 cudaError_t launch_variant(const void* wq, const void* wsc, GemvArgs a, cudaStream_t stream, int grid_cap) {
@@ -476,8 +482,12 @@ nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
 bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
-                                   const uint8_t* ws, const float* wg, int N, int K, float* y, float* partials,
-                                   unsigned int* counters, int grid_cap, int max_ctas_per_sm, cudaStream_t stream);
+                                   const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
+                                   float* partials, unsigned int* counters, int grid_cap, int max_ctas_per_sm,
+                                   cudaStream_t stream);
+size_t nvfp4_internal_packed_bytes(int N, int K);
+cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
+                                        cudaStream_t stream);
 
 bool nvfp4_internal_encode_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                               uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
@@ -499,7 +509,7 @@ bool use_tensor_cores(int M) {
 
 extern "C" size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
-  return ws_layout(M, K).total;
+  return ws_layout(M, N, K).total;
 }
 
 extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
@@ -512,7 +522,7 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
       !nvfp4_internal_aligned(ws, 16) || !nvfp4_internal_aligned(y, 16) || !nvfp4_internal_aligned(xg, 4) ||
       !nvfp4_internal_aligned(wg, 4) || !nvfp4_internal_aligned(workspace, 256))
     return NVFP4_ERR_ALIGN;
-  const WsLayout wl = ws_layout(M, K);
+  const WsLayout wl = ws_layout(M, N, K);
   if (workspace_bytes < wl.total) return NVFP4_ERR_SHAPE;
   nvfp4_status ds = nvfp4_internal_check_device();
   if (ds != NVFP4_OK) return ds;
@@ -520,7 +530,7 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   if (use_tensor_cores(M)) {
     return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
-        xq, xs, xg, M, wq, ws, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
+        xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
         reinterpret_cast<unsigned int*>(wsb + wl.counters), env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
   }
   GemvArgs a;
@@ -563,4 +573,41 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
     default: e = launch_m<8>(variant, wq, ws, a, stream, grid_cap); break;
   }
   return nvfp4_internal_cuda_status(e);
+}
+
+extern "C" size_t nvfp4_packed_weight_bytes(int N, int K) {
+  if (N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
+  return nvfp4_internal_packed_bytes(N, K);
+}
+
+extern "C" nvfp4_status nvfp4_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
+                                           size_t packed_bytes, cudaStream_t stream) {
+  if (!wq || !ws || !packed) return NVFP4_ERR_NULL;
+  if (N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return NVFP4_ERR_SHAPE;
+  if (packed_bytes < nvfp4_internal_packed_bytes(N, K)) return NVFP4_ERR_SHAPE;
+  if (!nvfp4_internal_aligned(wq, 16) || !nvfp4_internal_aligned(ws, 16) || !nvfp4_internal_aligned(packed, 16))
+    return NVFP4_ERR_ALIGN;
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  return nvfp4_internal_cuda_status(nvfp4_internal_pack_weights(wq, ws, N, K, packed, stream));
+}
+
+extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                                                 const uint8_t* wpacked, const float* wg, int N, int K, float* y,
+                                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!xq || !xs || !xg || !wpacked || !wg || !y || !workspace) return NVFP4_ERR_NULL;
+  if (M < 1 || M > kMaxM) return NVFP4_ERR_RANGE;
+  if (N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return NVFP4_ERR_SHAPE;
+  if (!nvfp4_internal_aligned(xq, 16) || !nvfp4_internal_aligned(xs, 16) || !nvfp4_internal_aligned(wpacked, 16) ||
+      !nvfp4_internal_aligned(y, 16) || !nvfp4_internal_aligned(xg, 4) || !nvfp4_internal_aligned(wg, 4) ||
+      !nvfp4_internal_aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  const WsLayout wl = ws_layout(M, N, K);
+  if (workspace_bytes < wl.total) return NVFP4_ERR_SHAPE;
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
+      xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
+      reinterpret_cast<unsigned int*>(wsb + wl.counters), env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
 }

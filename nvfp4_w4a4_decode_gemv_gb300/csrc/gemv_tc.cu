@@ -39,6 +39,8 @@
 // the last arriver sums partials in CTA order).
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 
@@ -52,30 +54,34 @@ constexpr int kActCodeBytes = kNT * 128;    // 2048
 constexpr int kActScaleBytes = kNT * 16;    // 256
 constexpr int kScaleBytes = kTR * 16;       // 2048
 constexpr int kActBytes = kActCodeBytes + kActScaleBytes;   // 2304: token codes + scales per stage
-// slot: [A codes 16384][B codes 2048][B scales 256][A scales 2048], 1024-aligned slots
-constexpr int kOffB = kCodeBytes;
-constexpr int kOffSB = kOffB + kActCodeBytes;
-constexpr int kOffSA = kOffSB + kActScaleBytes;             // 18688 (128-byte aligned)
-constexpr int kSlot = ((kOffSA + kScaleBytes + 1023) / 1024) * 1024;   // 21504
+// slot: [A codes 16384][A scales 2048][B codes 2048][B scales 256], 1024-aligned slots.
+// The first 18432 bytes are one block of the packed weight layout (see
+// nvfp4_pack_weights), so a packed stage is one contiguous bulk copy.
+constexpr int kOffSA = kCodeBytes;                          // 16384
+constexpr int kOffB = kOffSA + kScaleBytes;                 // 18432 (1024-aligned: swizzled operand)
+constexpr int kOffSB = kOffB + kActCodeBytes;               // 20480
+constexpr int kSlot = ((kOffSB + kActScaleBytes + 1023) / 1024) * 1024;   // 21504
+constexpr int kPackedBlock = kCodeBytes + kScaleBytes;      // 18432 bytes per [128-row tile x 256-K chunk]
 constexpr uint32_t kStageTx = kCodeBytes + kScaleBytes + kActBytes;
 constexpr int kWarps = 10;                  // 0 producer, 1 MMA, 2-5 scale writers, 6-9 epilogue
 constexpr int kThreads = 32 * kWarps;
-constexpr uint32_t kTmemCols = 256;         // D0 [0,16), D1 [16,32), 32 scale columns per stage from 32 (S <= 7)
+constexpr uint32_t kTmemCols = 256;         // D0 [0,16), D1 [16,32), then 32 scale columns per stage (S <= 7)
 constexpr uint32_t kColSF = 32;             // stage s: A scales at 32+32s+[0,16), B scales at 32+32s+16+[0,13)
 // Instruction descriptor: E2M1 x E2M1 (format 1), UE4M3 scales, K-major A and B,
 // N = 16 (bits 17-22: N >> 3), M = 128 (bits 24-28: M >> 4), dense.
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
 
 struct TcArgs {
+  const uint8_t* wpacked;        // packed weights, or null: weights through the two tensor maps
   const float* xg;
   const float* wg;
   float* y;
-  float* partials;               // [G][2][128][M]
-  unsigned int* counters;        // one per 32-row group
+  float* partials;               // [G][2][128][M]: a CTA's first and last partial tile
+  unsigned int* counters;        // arrivals per (tile, 32-row quarter), zero between calls
   int M, N, K, C, RT;
-  long long U;
+  int l2_units;                  // packed weights: units beyond the ring prefetched to L2 up front
+  long long U;                   // units = RT * C, numbered tile-major
 };
-
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 NVFP4_DEVINL uint64_t smem_desc_sw128(uint32_t saddr) {
@@ -105,18 +111,36 @@ NVFP4_DEVINL void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion to wait for).
+NVFP4_DEVINL void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Bounded wait by a whole warp: lane 0 polls, the outcome is broadcast so that
+// the warp stays converged (also when the wait gives up).
+NVFP4_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Stream-K split: CTA q of G owns units [q U / G, (q+1) U / G).
 NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { return (q * U) / G; }
 NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { return ((x + 1) * G - 1) / U; }
 
-// ---- epilogue: accumulator rows -> y or partial sums ---------------------------
+// ---- epilogue: accumulator rows of one tile segment -> y, or a partial record ----
+// A tile that one CTA covers whole goes straight to y.  Otherwise each CTA
+// overlapping it writes a record (slot 0 for the CTA's first tile, slot 1 for
+// its last); the last to arrive (per 32-row quarter) adds the records in CTA
+// order, so the result does not depend on timing.
 template <int M>
-NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, long long u0, int quad, int lane, const float (&acc)[kNT]) {
+NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, int my_slot, int quad, int lane, const float (&acc)[kNT]) {
   const long long G = gridDim.x, C = a.C;
   const long long first = cta_of_unit((long long)tile * C, a.U, G);
   const long long last = cta_of_unit((long long)tile * C + C - 1, a.U, G);
   const float yscale = __fmul_rn(__ldg(a.xg), __ldg(a.wg));
-  const int row0 = tile * kTR + quad * 32;
-  const int n = row0 + lane;
+  const int row = quad * 32 + lane;
+  const int n = tile * kTR + row;
   if (first == last) {
     if (n < a.N) {
 #pragma unroll
@@ -124,12 +148,11 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, long long u0, int quad, in
     }
     return;
   }
-  const int my_slot = (tile == (int)(u0 / C)) ? 0 : 1;
-  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * kTR + quad * 32 + lane) * M;
+  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * kTR + row) * M;
 #pragma unroll
   for (int m = 0; m < M; ++m) __stcg(part + m, acc[m]);
   __syncwarp();                 // the warp's partial stores are ordered before lane 0's release
-  unsigned int* cnt = a.counters + (size_t)(row0 / 32);
+  unsigned int* cnt = a.counters + (size_t)tile * 4 + quad;
   int is_last = 0;
   if (lane == 0) {
     fence_acq_rel_gpu();        // release: this warp's partials before the count
@@ -139,14 +162,30 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, long long u0, int quad, in
   is_last = __shfl_sync(0xffffffffu, is_last, 0);
   if (!is_last) return;
   __syncwarp();                 // the lanes' partial loads are ordered after lane 0's acquire
+  // Only the first contributor can have started before this tile (then the
+  // tile is its slot 1); every later one starts inside it (slot 0).
+  const int first_slot = (unit_start(first, a.U, G) < (long long)tile * C) ? 1 : 0;
   float sum[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) sum[m] = 0.0f;
-  for (long long q = first; q <= last; ++q) {
-    const int qslot = (tile == (int)(unit_start(q, a.U, G) / C)) ? 0 : 1;
-    const float* pq = a.partials + (((size_t)q * 2 + qslot) * kTR + quad * 32 + lane) * M;
+  // Records in CTA order, four at a time with their loads issued together.
+  for (long long q = first; q <= last; q += 4) {
+    float v[4][M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) sum[m] += __ldcg(pq + m);
+    for (int i = 0; i < 4; ++i) {
+      const long long qq = q + i;
+      const int qs = (qq == first) ? first_slot : 0;
+      const float* pq = a.partials + (((size_t)qq * 2 + qs) * kTR + row) * M;
+#pragma unroll
+      for (int m = 0; m < M; ++m) v[i][m] = (qq <= last) ? __ldcg(pq + m) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (q + i <= last) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) sum[m] += v[i][m];
+      }
+    }
   }
   if (n < a.N) {
 #pragma unroll
@@ -156,7 +195,7 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, long long u0, int quad, in
 }
 
 template <int M, int S>
-__global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
+__global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                               const __grid_constant__ CUtensorMap tm_scales,
                                                               const __grid_constant__ CUtensorMap tm_xcodes,
                                                               const __grid_constant__ CUtensorMap tm_xscales,
@@ -200,79 +239,109 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch_dependents();   // the next kernel in the stream may start launching
 
+  // Every role walks the CTA's units u0 .. u1-1 in order, keeping the unit's
+  // (tile, chunk) and its ring slot and phase incrementally: no division in the loops.
+  const int C = a.C;
+  const int tile0 = (int)(u0 / C), chunk0 = (int)(u0 % C);
+
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0 && nunits > 0) {
-      prefetch_tmap(&tm_codes);
-      prefetch_tmap(&tm_scales);
+      if (!a.wpacked) {
+        prefetch_tmap(&tm_codes);
+        prefetch_tmap(&tm_scales);
+      }
       prefetch_tmap(&tm_xcodes);
       prefetch_tmap(&tm_xscales);
       const int pre = nunits < S ? nunits : S;
-      // Weight tiles do not depend on the preceding kernel: issue them first.
-      for (int k = 0; k < pre; ++k) {
-        const long long u = u0 + k;
-        const int tile = (int)(u / a.C), c = (int)(u % a.C);
-        uint8_t* slot = smem + k * kSlot;
-        mbar_arrive_expect_tx(&full[k], kStageTx);
-        tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[k]);
-        tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
+      const uint8_t* wp = a.wpacked ? a.wpacked + (size_t)u0 * kPackedBlock : nullptr;
+      // Weight tiles do not depend on the preceding kernel: issue the first
+      // stages, and ask L2 for the units after them, before waiting on it.
+      {
+        int tile = tile0, c = chunk0;
+        for (int k = 0; k < pre; ++k) {
+          uint8_t* slot = smem + k * kSlot;
+          mbar_arrive_expect_tx(&full[k], kStageTx);
+          if (wp) {
+            bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[k]);
+          } else {
+            tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[k]);
+            tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
+          }
+          if (++c == C) { c = 0; ++tile; }
+        }
+        if (wp) {
+          const int l2_end = (pre + a.l2_units < nunits) ? pre + a.l2_units : nunits;
+          for (int k = pre; k < l2_end; ++k) prefetch_l2(wp + (size_t)k * kPackedBlock, kPackedBlock);
+        }
       }
-      griddep_wait();          // the token codes and scales come from the preceding quantizer
+      griddep_wait();          // the token codes and scales come from the preceding kernel
+      int tile = tile0, c = chunk0;
       for (int k = 0; k < pre; ++k) {
-        const int c = (int)((u0 + k) % a.C);
         uint8_t* slot = smem + k * kSlot;
         tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[k]);      // rows >= M arrive as zeros
         tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
+        if (++c == C) { c = 0; ++tile; }
       }
       int issued = pre;
+      int s = pre % S;
+      uint32_t phase = (pre / S) & 1;                    // phase of the slot's next fill
       for (int k = pre; k < nunits; ++k) {
-        const int s = k % S;
-        if (!mbar_wait(&empty[s], ((k / S) - 1) & 1)) break;
-        const long long u = u0 + k;
-        const int tile = (int)(u / a.C), c = (int)(u % a.C);
+        if (!mbar_wait(&empty[s], phase ^ 1u)) break;   // the slot's previous use has been consumed
         uint8_t* slot = smem + s * kSlot;
         mbar_arrive_expect_tx(&full[s], kStageTx);
-        tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[s]);
-        tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
+        if (wp) {
+          bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[s]);
+        } else {
+          tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[s]);
+          tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
+        }
         tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[s]);
         tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
         issued = k + 1;
+        if (++c == C) { c = 0; ++tile; }
+        if (++s == S) { s = 0; phase ^= 1u; }
       }
+      // Do not leave the CTA with copies still in flight: wait (bounded) for the
+      // last stages issued; on the normal path they have long completed.
       for (int k = (issued > S ? issued - S : 0); k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0 && nunits > 0) {
+      // Descriptors of slot 0; the start-address field (bits 0-13, address / 16)
+      // moves by (slot offset + 32 q) / 16 within the 14-bit field.
+      const uint64_t da0 = smem_desc_sw128(smem_u32(smem));
+      const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB));
       int tile_idx = -1;
-      int cur_tile = -1;
-      bool ok = true;
+      int c = chunk0;
+      int s = 0;
+      uint32_t phase = 0;
       int issued = 0;
-      for (int k = 0; k < nunits && ok; ++k) {
-        const int s = k % S;
-        const long long u = u0 + k;
-        const int tile = (int)(u / a.C);
-        const bool first_of_tile = (tile != cur_tile);
+      for (int k = 0; k < nunits; ++k) {
+        const bool first_of_tile = (k == 0) || (c == 0);
         if (first_of_tile) {
-          cur_tile = tile;
           ++tile_idx;
-          const int d = tile_idx & 1;
-          if (tile_idx >= 2 && !mbar_wait(&acc_empty[d], ((tile_idx >> 1) - 1) & 1)) { ok = false; break; }
+          if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) break;
         }
-        if (!mbar_wait(&full[s], (k / S) & 1) || !mbar_wait(&sf_ready[s], (k / S) & 1)) { ok = false; break; }
+        // The scale writers arrive on sf_ready only after they have seen the
+        // slot full, so sf_ready also orders the slot's data before the MMAs.
+        if (!mbar_wait(&sf_ready[s], phase)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
-        const uint32_t sa = smem_u32(smem + s * kSlot);
+        const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
         const uint32_t sfa = tmem + kColSF + 32u * s;
         const uint32_t sfb = sfa + 16u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          mma_mxf4nvf4(d_tmem, smem_desc_sw128(sa + 32 * q), smem_desc_sw128(sa + kOffB + 32 * q), sfa + 4u * q,
-                       sfb + 4u * q, (first_of_tile && q == 0) ? 0u : 1u);
+          mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, sfa + 4u * q, sfb + 4u * q,
+                       (first_of_tile && q == 0) ? 0u : 1u);
         }
         mma_commit(&empty[s]);
         issued = k + 1;
-        const bool last_of_tile = (k + 1 == nunits) || ((int)((u + 1) / a.C) != tile);
-        if (last_of_tile) mma_commit(&acc_full[tile_idx & 1]);
+        if (++c == C) c = 0;
+        if (k + 1 == nunits || c == 0) mma_commit(&acc_full[tile_idx & 1]);   // last unit of this tile
+        if (++s == S) { s = 0; phase ^= 1u; }
       }
       // Do not leave with MMAs in flight: wait (bounded) for the last commit.
       if (issued > 0) mbar_wait(&empty[(issued - 1) % S], ((issued - 1) / S) & 1);
@@ -281,12 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     // ---------------- scale writers: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    const uint32_t ta0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + (uint32_t)quad;
+    const uint32_t tb0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 16u;
+    int s = 0;
+    uint32_t phase = 0;
     for (int k = 0; k < nunits; ++k) {
-      const int s = k % S;
-      if (!mbar_wait(&full[s], (k / S) & 1)) break;
+      if (!mbar_wait_warp(&full[s], phase)) break;
       const uint8_t* slot = smem + s * kSlot;
       const uint4 sa = *reinterpret_cast<const uint4*>(slot + kOffSA + row * 16);
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 32u * s + (uint32_t)quad;
+      const uint32_t ta = ta0 + 32u * s;
       tmem_st1(ta, sa.x);
       tmem_st1(ta + 4u, sa.y);
       tmem_st1(ta + 8u, sa.z);
@@ -295,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       // quadrant p from lane 32p + n, so every quadrant holds a copy.
       uint4 sb = make_uint4(0u, 0u, 0u, 0u);
       if (lane < kNT) sb = *reinterpret_cast<const uint4*>(slot + kOffSB + lane * 16);
-      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 32u * s + 16u;
+      const uint32_t tb = tb0 + 32u * s;
       tmem_st1(tb, sb.x);
       tmem_st1(tb + 4u, sb.y);
       tmem_st1(tb + 8u, sb.z);
@@ -304,23 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sf_ready[s]);
+      if (++s == S) { s = 0; phase ^= 1u; }
     }
   } else {
     // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
-    griddep_wait();
-    int tile_idx = -1, cur_tile = -1;
-    for (int k = 0; k < nunits; ++k) {
-      const long long u = u0 + k;
-      const int tile = (int)(u / a.C);
-      if (tile != cur_tile) {
-        cur_tile = tile;
-        ++tile_idx;
-      }
-      const bool last_of_tile = (k + 1 == nunits) || ((int)((u + 1) / a.C) != tile);
-      if (!last_of_tile) continue;
+    griddep_wait();            // y, the partial records and the counters belong to the preceding kernel's era
+    const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
+    for (int tile = tile0, tile_idx = 0; tile <= tile_last; ++tile, ++tile_idx) {
       const int d = tile_idx & 1;
-      if (!mbar_wait(&acc_full[d], (tile_idx >> 1) & 1)) break;
+      if (!mbar_wait_warp(&acc_full[d], (tile_idx >> 1) & 1)) break;
       tc_fence_after();
       uint32_t r[kNT];
       asm volatile(
@@ -335,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       float acc[kNT];
 #pragma unroll
       for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
-      tc_flush<M>(a, tile, u0, quad, lane, acc);
+      tc_flush<M>(a, tile, tile == tile0 ? 0 : 1, quad, lane, acc);
     }
   }
   tc_fence_before();
@@ -358,13 +423,22 @@ bool nvfp4_internal_encode_2d(CUtensorMap* map, const void* base, uint64_t inner
                               uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 int nvfp4_internal_device_sms();
 
+// CTAs of the tensor-core GEMV per device (two per SM at the default depth).
+static int tc_grid_max() { return 2 * nvfp4_internal_device_sms(); }
+
+// Partial records: two of 128 x M floats per CTA.
+size_t nvfp4_internal_tc_partial_bytes(int M, int N, int K) {
+  (void)N;
+  (void)K;
+  return (size_t)tc_grid_max() * 2 * kTR * (size_t)M * sizeof(float);
+}
+
 struct TcMaps {
   CUtensorMap w_codes, w_scales, x_codes, x_scales;
 };
 
 template <int M, int S>
-static cudaError_t launch_tc(const TcMaps& mp, const TcArgs& a, cudaStream_t stream, int grid_cap,
-                             int max_ctas_per_sm) {
+static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm) {
   static int per_sm_fit = -1;
   constexpr size_t smem = tc_smem_bytes<S>();
   auto kern = gemv_tc_kernel<M, S>;
@@ -375,10 +449,18 @@ static cudaError_t launch_tc(const TcMaps& mp, const TcArgs& a, cudaStream_t str
     int dev = 0, smem_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    // CTAs per SM: shared memory (plus the 1 KB the driver reserves per CTA) and TMEM columns.
+    // CTAs per SM: shared memory (plus the 1 KB the driver reserves per CTA),
+    // TMEM columns and registers (allocated per warp in units of 256).
     int by_smem = smem_sm > 0 ? (int)(smem_sm / (smem + 1024)) : 1;
     int by_tmem = 512 / (int)kTmemCols;
+    cudaFuncAttributes fa;
+    int by_regs = 2;
+    if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs > 0) {
+      const int per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+      by_regs = 65536 / (per_warp * kWarps);
+    }
     per_sm_fit = by_smem < by_tmem ? by_smem : by_tmem;
+    if (by_regs < per_sm_fit) per_sm_fit = by_regs;
     if (per_sm_fit < 1) per_sm_fit = 1;
   }
   int per_sm = per_sm_fit < max_ctas_per_sm ? per_sm_fit : max_ctas_per_sm;
@@ -408,19 +490,25 @@ static cudaError_t launch_tc_m(int stages, const TcMaps& mp, const TcArgs& a, cu
   }
 }
 
-// Tensor-core GEMV; the caller has validated the arguments.
+// Tensor-core GEMV; the caller has validated the arguments.  Weights come either
+// packed (wpacked != null, nvfp4_pack_weights layout) or as the row-major
+// codes and scales wq, ws.  `counters` holds RT * 4 tile counters (zero between calls).
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
-                                   const uint8_t* ws, const float* wg, int N, int K, float* y, float* partials,
-                                   unsigned int* counters, int grid_cap, int max_ctas_per_sm, cudaStream_t stream) {
+                                   const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
+                                   float* partials, unsigned int* counters, int grid_cap, int max_ctas_per_sm,
+                                   cudaStream_t stream) {
   const char* st = getenv("NVFP4_GEMV_TC_STAGES");   // tuning knob: 4 (default), 5 or 6
   const int stages = st ? atoi(st) : 4;
   TcMaps mp;
-  if (!nvfp4_internal_encode_2d(&mp.w_codes, wq, (uint64_t)K / 2, (uint64_t)N, 128, kTR, true) ||
-      !nvfp4_internal_encode_2d(&mp.w_scales, ws, (uint64_t)K / 16, (uint64_t)N, 16, kTR, false) ||
-      !nvfp4_internal_encode_2d(&mp.x_codes, xq, (uint64_t)K / 2, (uint64_t)M, 128, kNT, true) ||
+  memset(&mp, 0, sizeof(mp));   // the weight maps stay unused (and are never prefetched) for packed weights
+  if (!wpacked && (!nvfp4_internal_encode_2d(&mp.w_codes, wq, (uint64_t)K / 2, (uint64_t)N, 128, kTR, true) ||
+                   !nvfp4_internal_encode_2d(&mp.w_scales, ws, (uint64_t)K / 16, (uint64_t)N, 16, kTR, false)))
+    return cudaErrorInvalidValue;
+  if (!nvfp4_internal_encode_2d(&mp.x_codes, xq, (uint64_t)K / 2, (uint64_t)M, 128, kNT, true) ||
       !nvfp4_internal_encode_2d(&mp.x_scales, xs, (uint64_t)K / 16, (uint64_t)M, 16, kNT, false))
     return cudaErrorInvalidValue;
   TcArgs a;
+  a.wpacked = wpacked;
   a.xg = xg;
   a.wg = wg;
   a.y = y;
@@ -432,6 +520,8 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
   a.C = K / kChunk;
   a.RT = (N + kTR - 1) / kTR;
   a.U = (long long)a.RT * a.C;
+  const char* l2 = getenv("NVFP4_GEMV_L2_UNITS");   // tuning knob: units prefetched to L2 per CTA (default 0: it delays the first stages)
+  a.l2_units = l2 ? atoi(l2) : 0;
   switch (M) {
     case 1: return launch_tc_m<1>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     case 2: return launch_tc_m<2>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
@@ -442,4 +532,49 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
     case 7: return launch_tc_m<7>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     default: return launch_tc_m<8>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
   }
+}
+
+// ---- weight packing -------------------------------------------------------------
+namespace {
+// One thread per 16-byte piece of the packed image: per block (tile t, chunk c)
+// 1024 code pieces (row r, piece j stored at r*128 + ((j ^ (r & 7)) << 4)) and
+// 128 scale pieces (row r at 16384 + 16 r); rows >= N are zero.
+__global__ void __launch_bounds__(256) pack_weights_kernel(const uint8_t* __restrict__ wq,
+                                                           const uint8_t* __restrict__ ws, int N, int K,
+                                                           long long nblocks, uint8_t* __restrict__ packed) {
+  constexpr int kPieces = kCodeBytes / 16 + kScaleBytes / 16;   // 1152
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nblocks * kPieces) return;
+  const long long blk = i / kPieces;
+  const int p = (int)(i % kPieces);
+  const int C = K / kChunk;
+  const int t = (int)(blk / C), c = (int)(blk % C);
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  size_t dst = (size_t)blk * kPackedBlock;
+  if (p < kCodeBytes / 16) {
+    const int r = p >> 3, j = p & 7;
+    const long long n = (long long)t * kTR + r;
+    if (n < N) v = __ldg(reinterpret_cast<const uint4*>(wq + (size_t)n * (K / 2) + (size_t)c * 128 + j * 16));
+    dst += (size_t)r * 128 + (size_t)((j ^ (r & 7)) << 4);
+  } else {
+    const int r = p - kCodeBytes / 16;
+    const long long n = (long long)t * kTR + r;
+    if (n < N) v = __ldg(reinterpret_cast<const uint4*>(ws + (size_t)n * (K / 16) + (size_t)c * 16));
+    dst += (size_t)kCodeBytes + (size_t)r * 16;
+  }
+  *reinterpret_cast<uint4*>(packed + dst) = v;
+}
+}  // namespace
+
+size_t nvfp4_internal_packed_bytes(int N, int K) {
+  return (size_t)((N + kTR - 1) / kTR) * (size_t)(K / kChunk) * kPackedBlock;
+}
+
+cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
+                                        cudaStream_t stream) {
+  const long long nblocks = (long long)((N + kTR - 1) / kTR) * (K / kChunk);
+  const long long pieces = nblocks * (kCodeBytes / 16 + kScaleBytes / 16);
+  const long long grid = (pieces + 255) / 256;
+  pack_weights_kernel<<<(unsigned)grid, 256, 0, stream>>>(wq, ws, N, K, nblocks, packed);
+  return cudaGetLastError();
 }

@@ -127,11 +127,13 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
   __shared__ float s_warp[kCThreads / 32];
   __shared__ float s_cta_max;
   __shared__ float s_amax;
-  // Programmatic dependent launch: the input may come from the preceding
-  // kernel; once it is complete, let the next kernel (the GEMV) start launching
-  // so that its weight loads overlap this one.
-  griddep_wait();
+  // Programmatic dependent launch: let the next kernel (the GEMV) start
+  // launching at once -- it reads only weights until it waits on this grid, so
+  // its CTAs take over SMs as the preceding GEMV's CTAs leave and prefetch their
+  // first weight tiles -- then wait for the preceding kernel, which may produce
+  // this kernel's input.
   griddep_launch_dependents();
+  griddep_wait();
   const uint32_t rank = cluster_ctarank();
   const uint32_t csize = gridDim.x;          // the whole grid is one cluster
   const long T = (long)csize * kCThreads;

@@ -72,6 +72,22 @@ def test_gemv_argument_errors(lib):
     assert lib.nvfp4_gemv_workspace_bytes(1, 256, 100) == 0
 
 
+def test_packed_weight_argument_errors(lib):
+    assert lib.nvfp4_packed_weight_bytes(1000, 768) == 8 * 3 * 18432      # ceil(1000/128) tiles x 3 chunks
+    assert lib.nvfp4_packed_weight_bytes(128, 256) == 18432
+    assert lib.nvfp4_packed_weight_bytes(0, 256) == 0
+    assert lib.nvfp4_packed_weight_bytes(128, 200) == 0
+    assert lib.nvfp4_pack_weights(FAKE, FAKE, 128, 256, FAKE, 18431, None) == 2   # output too small
+    assert lib.nvfp4_pack_weights(None, FAKE, 128, 256, FAKE, 18432, None) == 1
+    assert lib.nvfp4_pack_weights(FAKE, FAKE, 128, 264, FAKE, 1 << 30, None) == 2
+    assert lib.nvfp4_pack_weights(FAKE, FAKE + 8, 128, 256, FAKE, 1 << 30, None) == 3
+    args = lambda M, N, K, w=FAKE: (FAKE, FAKE, FAKE, M, w, FAKE, N, K, FAKE, FAKE, 1 << 30, None)
+    assert lib.nvfp4_gemv_smallm_packed(*args(9, 256, 256)) == 4
+    assert lib.nvfp4_gemv_smallm_packed(*args(1, 256, 300)) == 2
+    assert lib.nvfp4_gemv_smallm_packed(*args(1, 256, 256, w=None)) == 1
+    assert lib.nvfp4_gemv_smallm_packed(*args(1, 256, 256, w=FAKE + 8)) == 3
+
+
 def test_reset_argument_errors(lib):
     from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams
     p = ResetParams(0.6, 0.3, 1.0, 8)
