@@ -10,13 +10,15 @@ step streams >= 245 MB of other weights, more than the 129 MB L2, so every
 call reads its weights from HBM (no flush kernel needed).
 
 value = algorithmic HBM bytes of the step (weight codes + scales, activation
-in/out, outputs) / device time of the step, in GB/s.  For each M the four
-quantizations and the four GEMVs are captured as two CUDA graphs; the timed
-region replays them back to back with events recorded between the graph
-launches, so the same region gives the GEMV time for the roofline.  A cold-L2
-breakdown per (projection, M) follows (512 MB flush before each call).  `e2e`
-repeats the step through the eager C-ABI calls with the activations copied
-from pinned host memory and the outputs copied back inside the timed region.
+in/out, outputs) / device time of the step, in GB/s.  For each M the step is
+captured as one CUDA graph in decode-chain order (quantize -> GEMV, four
+times, with programmatic dependent launches so that each GEMV prefetches its
+weights while its quantizer runs).  The roofline times the GEMV kernels alone:
+graphs of the same GEMV launches, replayed right after the timed steps with
+events between them.  A cold-L2 breakdown per (projection, M) follows (512 MB
+flush before each call).  `e2e` repeats the step through the eager C-ABI calls
+with the activations copied from pinned host memory and the outputs copied
+back inside the timed region.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (for N > 1 under torch.distributed.run: N independent replicas, weak scaling).
@@ -195,50 +197,54 @@ def run_ours(args, world, rank):
         groups.setdefault(c["M"], []).append(c)
     order = sorted(groups)
 
-    def quantize_all(cs):
-        for c in cs:
-            api.nvfp4_quantize_act(c["x"], out=c["xq"])
-
     def gemv_all(cs):
         for c in cs:
             gemv_call(api, c, weights[c["name"]], ws)
 
+    def step_m(cs):                  # the decode-chain order: quantize, project, quantize, project, ...
+        for c in cs:
+            api.nvfp4_quantize_act(c["x"], out=c["xq"])
+            gemv_call(api, c, weights[c["name"]], ws)
+
     for M in order:                  # initialises kernel attributes outside capture
-        quantize_all(groups[M])
-        gemv_all(groups[M])
+        step_m(groups[M])
     torch.cuda.synchronize()
-    # Per M: one graph with that M's quantizations, one with its GEMVs.  Events
-    # recorded between the graph launches bracket the GEMVs on the GPU.
+    # Per M: one graph of the chained step (quantize -> GEMV, x4, programmatic
+    # dependent launches between them), and one of the GEMVs alone whose
+    # replays, bracketed by events, time the GEMV kernel for the roofline.
     stream = torch.cuda.Stream()
-    graphs = {}
+    graphs, ggraphs = {}, {}
     with torch.cuda.stream(stream):
         for M in order:
-            gq, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gq, stream=stream):
-                quantize_all(groups[M])
+            g, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_m(groups[M])
             with torch.cuda.graph(gg, stream=stream):
                 gemv_all(groups[M])
-            graphs[M] = (gq, gg)
+            graphs[M], ggraphs[M] = g, gg
     torch.cuda.synchronize()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in order]
            for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             for M in order:
-                graphs[M][0].replay()
-                graphs[M][1].replay()
+                graphs[M].replay()
+            for M in order:
+                ggraphs[M].replay()
     barrier(world)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         with torch.cuda.stream(stream):
             t0.record()
-            for k in range(args.steps):
-                for i, M in enumerate(order):
-                    graphs[M][0].replay()
-                    evs[k][i][0].record()
-                    graphs[M][1].replay()
-                    evs[k][i][1].record()
+            for k in range(args.steps):          # the timed steps
+                for M in order:
+                    graphs[M].replay()
             t1.record()
+            for k in range(args.steps):          # the GEMV kernels alone, same launches, for the roofline
+                for i, M in enumerate(order):
+                    evs[k][i][0].record()
+                    ggraphs[M].replay()
+                    evs[k][i][1].record()
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(world, t0.elapsed_time(t1))
@@ -277,7 +283,7 @@ def run_ours(args, world, rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": f"{gemv_name}: algorithmic bytes of all GEMV calls / their event-timed duration "
-                               "in the timed region",
+                               "(graphs of the GEMV launches alone, replayed right after the timed steps)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clocks,
         "gpu_launches": len(calls) * launches_per_call * args.steps,
