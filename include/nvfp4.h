@@ -187,10 +187,27 @@ nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, cons
 /* ------------------------------------------------------------------------ */
 /*
  * y[m, n] = sum_k x[m, k] * w[n, k], BF16 inputs, FP32 accumulation and output.
- * M 1..8, K a multiple of 8, all pointers 16-byte aligned.
+ * M 1..8, K a multiple of 8 with M * K <= 51200 (x is held in shared memory as
+ * FP32), all pointers 16-byte aligned.  Larger M * K returns NVFP4_ERR_SHAPE.
  */
 nvfp4_status nvfp4_bf16_gemv(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
                              cudaStream_t stream);
+
+/*
+ * RMS normalization of FP32 rows to BF16 (no gain):
+ *   out[r, k] = BF16( x[r, k] / sqrt( (1/K) sum_k x[r, k]^2 + eps ) )
+ * Row r of the input starts at x + r * ld (ld >= K, in floats); out is
+ * [rows, K] row-major.  The sum of squares is FP32 (in a fixed order per K),
+ * the square root and the division IEEE; results are within one BF16 rounding
+ * of the exact value.  K a multiple of 4, ld a multiple of 4, x 16-byte and
+ * out 8-byte aligned, eps >= 0.
+ * The pages' decode step runs inside a Qwen3 decoder, whose layers normalize
+ * their inputs (ReSET reading note §6.1: Qwen3 models); the synthetic decode
+ * step puts this in front of the qkv and gate_up projections so that a chain
+ * of many layers keeps its magnitude (SiLU(gate)*up squares it otherwise).
+ */
+nvfp4_status nvfp4_rms_norm_bf16(const float* x, int rows, int K, int ld, float eps, uint16_t* out,
+                                 cudaStream_t stream);
 
 /* FP32 -> BF16 (RNE) elementwise cast of n values; x, y 16-byte aligned, n a multiple of 8. */
 nvfp4_status nvfp4_f32_to_bf16(const float* x, size_t n, uint16_t* y, cudaStream_t stream);

@@ -12,7 +12,7 @@ from ._lib import ResetParams, check, lib, ptr, stream_handle
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
-    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_f32_to_bf16", "reset_state_bytes",
+    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_rms_norm_bf16", "nvfp4_f32_to_bf16", "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
     "NVFP4Tensor", "ResetSampler",
 ]
@@ -171,6 +171,20 @@ def nvfp4_bf16_gemv(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = N
     y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
     check(lib().nvfp4_bf16_gemv(ptr(x), M, ptr(w), N, K, ptr(y), stream_handle(stream)), "nvfp4_bf16_gemv")
     return y
+
+
+def nvfp4_rms_norm_bf16(x: torch.Tensor, K: int | None = None, eps: float = 1e-6, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """FP32 rows (first K columns of a row-major [rows, ld] tensor) -> BF16 RMS-normalized [rows, K]."""
+    _need_cuda(x)
+    if x.dtype != torch.float32 or x.dim() != 2:
+        raise ValueError("x must be a 2-D float32 tensor")
+    rows, ld = x.shape
+    K = ld if K is None else K
+    out = out if out is not None else torch.empty((rows, K), dtype=torch.bfloat16, device=x.device)
+    check(lib().nvfp4_rms_norm_bf16(ptr(x), rows, K, ld, float(eps), ptr(out), stream_handle(stream)),
+          "nvfp4_rms_norm_bf16")
+    return out
 
 
 def nvfp4_f32_to_bf16(x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:

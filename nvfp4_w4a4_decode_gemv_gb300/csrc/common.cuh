@@ -131,6 +131,10 @@ NVFP4_DEVINL void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work placed between them.
+NVFP4_DEVINL void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+NVFP4_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 NVFP4_DEVINL uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t out;

@@ -1,5 +1,5 @@
-// Decode-step glue around the NVFP4 projections: the BF16 lm_head GEMV and an
-// FP32 -> BF16 cast.  A Qwen3-style decoder ends in a BF16 lm_head whose logits
+// Decode-step glue around the NVFP4 projections: the BF16 lm_head GEMV, an
+// FP32 -> BF16 cast and an RMS normalization of FP32 rows to BF16.  A Qwen3-style decoder ends in a BF16 lm_head whose logits
 // feed the sampler (ReSET reading note §6.4: end-to-end decode on the whole
 // model; the lm_head itself is not NVFP4 there).
 //
@@ -82,6 +82,50 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ x, size_t n8, uint
   }
 }
 
+// RMS normalization of FP32 rows to BF16, one CTA per row:
+//   out[r, k] = BF16( x[r, k] / sqrt( sum_k x[r, k]^2 / K + eps ) )
+// Sum of squares in FP32 (per-thread strided partial sums, then a fixed tree
+// over the CTA); sqrt and the division are IEEE (sqrtf, __fdiv_rn).
+constexpr int kNormThreads = 256;
+
+__global__ void __launch_bounds__(kNormThreads) rms_norm_bf16_kernel(const float* __restrict__ x, int K, long ld,
+                                                                     float eps, uint16_t* __restrict__ out) {
+  __shared__ float s_warp[kNormThreads / 32];
+  __shared__ float s_inv;
+  griddep_launch_dependents();
+  griddep_wait();             // the input comes from the preceding kernel
+  const float* xr = x + (long)blockIdx.x * ld;
+  float ss = 0.0f;
+  for (int k = threadIdx.x * 4; k < K; k += kNormThreads * 4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
+    ss = __fmaf_rn(v.x, v.x, ss);
+    ss = __fmaf_rn(v.y, v.y, ss);
+    ss = __fmaf_rn(v.z, v.z, ss);
+    ss = __fmaf_rn(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < kNormThreads / 32 ? s_warp[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) s_inv = __fdiv_rn(1.0f, sqrtf(__fadd_rn(__fdiv_rn(t, (float)K), eps)));
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  uint16_t* orow = out + (long)blockIdx.x * K;
+  for (int k = threadIdx.x * 4; k < K; k += kNormThreads * 4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v.x, inv))) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v.y, inv))) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v.z, inv))) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v.w, inv))) << 16);
+    *reinterpret_cast<uint2*>(orow + k) = make_uint2(lo, hi);
+  }
+}
+
 template <int M>
 cudaError_t launch_bf16(const uint16_t* x, const uint16_t* w, int N, int K, float* y, cudaStream_t stream) {
   static int sms = 0;
@@ -138,4 +182,25 @@ extern "C" nvfp4_status nvfp4_f32_to_bf16(const float* x, size_t n, uint16_t* y,
   f32_to_bf16_kernel<<<(unsigned)grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(x), n8,
                                                          reinterpret_cast<uint4*>(y));
   return nvfp4_internal_cuda_status(cudaGetLastError());
+}
+
+extern "C" nvfp4_status nvfp4_rms_norm_bf16(const float* x, int rows, int K, int ld, float eps, uint16_t* out,
+                                           cudaStream_t stream) {
+  if (rows == 0) return NVFP4_OK;
+  if (!x || !out) return NVFP4_ERR_NULL;
+  if (rows < 0 || K < 4 || (K % 4) != 0 || ld < K || (ld % 4) != 0) return NVFP4_ERR_SHAPE;
+  if (!(eps >= 0.0f)) return NVFP4_ERR_RANGE;
+  if (!nvfp4_internal_aligned(x, 16) || !nvfp4_internal_aligned(out, 8)) return NVFP4_ERR_ALIGN;
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return nvfp4_internal_cuda_status(cudaLaunchKernelEx(&cfg, rms_norm_bf16_kernel, x, K, (long)ld, eps, out));
 }

@@ -157,18 +157,24 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
   for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
   if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = local;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = 0.0f;
-    for (int w = 0; w < kCThreads / 32; ++w) m = fmaxf(m, s_warp[w]);
-    s_cta_max = m;
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < kCThreads / 32 ? s_warp[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) s_cta_max = m;
   }
   cluster_sync();                            // every CTA's s_cta_max is visible cluster-wide
-  if (threadIdx.x == 0) {
-    float m = 0.0f;
-    for (uint32_t r = 0; r < csize; ++r) m = fmaxf(m, ld_dsmem_f32(dsmem_addr(&s_cta_max, r)));
-    s_amax = m;
+  // Warp 0 gathers the CTA maxima (one remote read per lane), then this CTA
+  // signals that it is done reading its peers; the matching wait sits at the
+  // end, so that no CTA leaves while a peer may still read its shared memory.
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < csize ? ld_dsmem_f32(dsmem_addr(&s_cta_max, threadIdx.x)) : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) s_amax = m;
   }
-  cluster_sync();                            // reads done before any CTA may exit; s_amax visible
+  cluster_arrive();
+  __syncthreads();                           // s_amax visible to the CTA
   const float g = __fdiv_rn(s_amax, kGlobalDivisor);
   if (rank == 0 && threadIdx.x == 0) *global = g;
 #pragma unroll
@@ -181,6 +187,7 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
       scales[b] = static_cast<uint8_t>(s);
     }
   }
+  cluster_wait();
 }
 
 // ---- multi-launch path for large tensors -----------------------------------
@@ -285,10 +292,11 @@ cudaError_t quantize_dispatch(const Src& src, long nblocks, uint8_t* codes, uint
     return cudaGetLastError();
   }
   // One cluster: CTAs of kCThreads threads, each thread holding NB blocks in
-  // registers; aim at <= 2 blocks per thread, up to the device's cluster limit.
+  // registers; one block per thread while the device's cluster limit allows
+  // (the work after the amax is a chain of IEEE divisions per block).
   const int cap = max_cluster<Src, 8>();
   if (nblocks <= (long)cap * kCThreads * 8) {
-    long csize = (nblocks + 2L * kCThreads - 1) / (2L * kCThreads);
+    long csize = (nblocks + kCThreads - 1) / kCThreads;
     if (csize < 1) csize = 1;
     if (csize > cap) csize = cap;
     const long T = csize * kCThreads;

@@ -10,7 +10,10 @@ re-quantized to NVFP4 as the next input:
   * between gate_up and down sits SiLU(gate) * up, with gate = the first half
     of the gate_up columns and up = the second half;
   * after the last layer a BF16 lm_head GEMV produces the logits that feed the
-    ReSET sampler.
+    ReSET sampler;
+  * the inputs of the qkv and gate_up projections (and of the lm_head) are RMS
+    normalized first, as in the Qwen3 decoders the pages run (reading note
+    §6.1); without it SiLU(gate)*up squares the magnitude at every layer.
 
 Where the CUDA path rounds an FP32 result to BF16 (a decision that feeds the
 next quantizer), the oracle rounds its FP64 result to FP32 first and then to
@@ -46,3 +49,9 @@ def bf16_gemv(x_bits: np.ndarray, w_bits: np.ndarray):
     x = bf16_bits_to_f32(x_bits).astype(np.float64)
     w = bf16_bits_to_f32(w_bits).astype(np.float64)
     return x @ w.T, np.abs(x) @ np.abs(w).T
+
+
+def rms_norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """x[r, k] / sqrt(mean_k x[r, k]^2 + eps) in FP64 (no gain)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)

@@ -101,4 +101,11 @@ def test_reset_argument_errors(lib):
     assert lib.reset_state_bytes(8, 8) > 0 and lib.reset_state_bytes(8, 0) == 0
     assert lib.reset_workspace_bytes(8, 151936) > 0
     assert lib.nvfp4_bf16_gemv(FAKE, 9, FAKE, 10, 64, FAKE, None) == 4
+    assert lib.nvfp4_bf16_gemv(FAKE, 8, FAKE, 10, 8192, FAKE, None) == 2    # M * K > 51200
     assert lib.nvfp4_f32_to_bf16(FAKE, 12, FAKE, None) == 2
+    norm = lib.nvfp4_rms_norm_bf16
+    assert norm(FAKE, 2, 6, 8, 1e-6, FAKE, None) == 2                  # K % 4
+    assert norm(FAKE, 2, 8, 4, 1e-6, FAKE, None) == 2                  # ld < K
+    assert norm(FAKE, 2, 8, 8, -1.0, FAKE, None) == 4                  # eps < 0
+    assert norm(None, 2, 8, 8, 1e-6, FAKE, None) == 1
+    assert norm(FAKE + 8, 2, 8, 8, 1e-6, FAKE, None) == 3

@@ -1,0 +1,84 @@
+"""GPU decode-step glue vs the oracle: the BF16 lm_head GEMV, the FP32 -> BF16
+cast and the RMS normalization.
+
+* BF16 GEMV: FP32 accumulation of at most K products, so
+  |y - y_ref| <= 1e-4 * sum_k |x_k w_k| + 1e-6 (an FP32 sum of K terms in
+  any order is within about K * 2^-24 of the exact sum, relative to the sum of
+  magnitudes; each lane here sums K/256 terms, then a 32-lane tree).
+* Cast: bit-exact against round-to-nearest-even.
+* RMS norm: the kernel's FP32 sum of squares and its IEEE sqrt and division
+  are within a few FP32 ulps of the exact value, so an element whose exact
+  value lies within 8 FP32 ulps of a BF16 rounding boundary may take either
+  BF16 neighbour; every other element must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as D
+from oracle import nvfp4 as Q
+from nvfp4_w4a4_decode_gemv_gb300 import api, synth
+from tests.gpu_util import assert_within, bits, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 512), (4, 4096, 5120), (8, 333, 6400), (3, 8, 8), (1, 77, 51200)])
+def test_bf16_gemv(M, N, K):
+    x = synth.activations(M, K, seed=M + N)
+    w = synth.weights(N, K, seed=K)
+    y = to_np(api.nvfp4_bf16_gemv(x.cuda(), w.cuda()))
+    ref, scale = D.bf16_gemv(bits(x), bits(w))
+    assert_within(y, ref, scale, rel=1e-4)
+
+
+def test_bf16_gemv_lm_head_sampled_rows():
+    """The decode step's lm_head shape (5120 -> 151936) at M = 8: the GPU computes
+    all logits, the oracle checks 64 sampled vocabulary rows."""
+    M, K, V = 8, 5120, synth.LM_HEAD_VOCAB
+    x = synth.activations(M, K, seed=5, outliers=False)
+    w = synth.weights(V, K, seed=6)
+    y = to_np(api.nvfp4_bf16_gemv(x.cuda(), w.cuda()))
+    rows = np.random.default_rng(1).choice(V, 64, replace=False)
+    ref, scale = D.bf16_gemv(bits(x), bits(w[rows]))
+    assert_within(y[:, rows], ref, scale, rel=1e-4)
+
+
+def test_f32_to_bf16_bit_exact():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(4096, generator=g) * torch.logspace(-30, 30, 4096)
+    y = api.nvfp4_f32_to_bf16(x.cuda())
+    assert np.array_equal(bits(y), Q.f32_to_bf16_bits(x.numpy()))
+
+
+def _decisive(a64, bf16_bits):
+    lo = D.to_bf16_bits(a64 * (1 - 8 * 2.0 ** -24))
+    hi = D.to_bf16_bits(a64 * (1 + 8 * 2.0 ** -24))
+    return (lo == hi) & (lo == bf16_bits)
+
+
+@pytest.mark.parametrize("rows,K,ld", [(1, 5120, 5120), (8, 5120, 5120), (4, 8192, 10240), (3, 25600, 25600), (2, 4, 4)])
+def test_rms_norm(rows, K, ld):
+    g = torch.Generator().manual_seed(rows * K)
+    x = torch.randn((rows, ld), generator=g) * 3.0
+    x[:, :: max(1, K // 50)] *= 20.0                                    # outlier columns
+    out = api.nvfp4_rms_norm_bf16(x.cuda(), K=K, eps=1e-6)
+    a = D.rms_norm(x[:, :K].numpy(), 1e-6)
+    mid = D.to_bf16_bits(a)
+    dec = _decisive(a, mid)
+    assert dec.mean() > 0.99
+    got = bits(out)
+    assert np.array_equal(got[dec], mid[dec])
+    # the rest are one of the two neighbours of the exact value
+    nd = ~dec
+    lo = D.to_bf16_bits(a * (1 - 8 * 2.0 ** -24))[nd]
+    hi = D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24))[nd]
+    assert np.all((got[nd] == lo) | (got[nd] == hi))
+
+
+def test_rms_norm_zero_row_and_eps():
+    x = torch.zeros((2, 64))
+    x[1] = 2.0
+    out = Q.bf16_bits_to_f32(bits(api.nvfp4_rms_norm_bf16(x.cuda(), eps=0.25)))
+    assert np.all(out[0] == 0)
+    assert np.all(out[1] == Q.bf16_bits_to_f32(D.to_bf16_bits(np.full(64, 2 / np.sqrt(4.25)))))

@@ -45,3 +45,18 @@ def test_table4_fixture_shapes():
     for model, layer, N, K, ours, theirs in rows:
         assert int(K) % 256 == 0 and int(N) % 256 == 0
         assert 1.5 < float(theirs) / float(ours) < 2.6
+
+
+def test_rms_norm_closed_forms():
+    # a row [3, 4]: mean square 12.5, so the values are 3/sqrt(12.5), 4/sqrt(12.5)
+    r = D.rms_norm(np.array([[3.0, 4.0]]), 0.0)
+    assert np.allclose(r, [[3 / np.sqrt(12.5), 4 / np.sqrt(12.5)]], rtol=0, atol=1e-15)
+    # a constant row c with eps: c / sqrt(c^2 + eps); rows are independent
+    r = D.rms_norm(np.array([[2.0] * 8, [-0.5] * 8]), 0.25)
+    assert np.allclose(r[0], 2 / np.sqrt(4.25)) and np.allclose(r[1], -0.5 / np.sqrt(0.5))
+    # scale invariance at eps = 0, and the output has mean square 1
+    x = np.random.default_rng(0).standard_normal((3, 64))
+    assert np.allclose(D.rms_norm(x, 0.0), D.rms_norm(7.5 * x, 0.0))
+    assert np.allclose(np.mean(D.rms_norm(x, 0.0) ** 2, axis=1), 1.0)
+    # a zero row stays zero when eps > 0
+    assert np.all(D.rms_norm(np.zeros((1, 16)), 1e-6) == 0)
