@@ -41,7 +41,9 @@ sys.path.insert(0, ROOT)
 from nvfp4_w4a4_decode_gemv_gb300 import synth  # noqa: E402
 
 METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Qwen3 shapes"
-WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8])}
+WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8]),
+             "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8])}
+DECODE_METRIC = "Qwen3-32B-shaped decode step latency (64 NVFP4 layers + BF16 lm_head + ReSET sampler, one CUDA graph)"
 
 
 def parse():
@@ -55,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
+    ap.add_argument("--m", type=int, default=None, help="decode workload: the number of tokens M (1, 4 or 8)")
+    ap.add_argument("--layers", type=int, default=64, help="decode workload: decoder layers")
     ap.add_argument("--weights", default="packed", choices=["packed", "rowmajor"],
                     help="weight layout: packed (nvfp4_pack_weights, offline) or row-major codes/scales")
     return ap.parse_args()
@@ -350,6 +354,59 @@ def run_e2e(args, calls, weights, ws):
             "d2h_bytes_per_step": int(sum(c["y"].numel() * 4 for c in calls))}
 
 
+def run_decode(args, world, rank):
+    """The synthetic decode step: `--layers` layers of the four projections,
+    the lm_head and the sampler, captured as one CUDA graph and replayed
+    `--steps` times (per-step latency)."""
+    from nvfp4_w4a4_decode_gemv_gb300.decode_step import DecodeStep
+    M = args.m or 1
+    st = DecodeStep(M=M, layers=args.layers, seed=rank)
+    st.h_in.copy_(synth.activations(M, st.hidden, seed=100 + M).float().cuda())
+    us = torch.from_numpy(synth.reset_uniforms(args.steps + args.warmup + 1, M)).cuda()
+    st.u.copy_(us[0])
+    st.run()                         # sets kernel attributes outside the capture
+    torch.cuda.synchronize()
+    g = st.capture()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            st.u.copy_(us[1 + i], non_blocking=True)
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                st.u.copy_(us[1 + args.warmup + i], non_blocking=True)
+                evs[i][0].record()
+                g.replay()
+                evs[i][1].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = np.array([a.elapsed_time(b) for a, b in evs])
+    ms_mean = max_over_ranks(world, float(ms.mean()))
+    weight_bytes = sum(w.packed.numel() for layer in st.weights for w in layer.values())
+    step_bytes = weight_bytes + st.lm_head.numel() * 2 + st.logits.numel() * 4 * 2
+    peak, peak_kind = measured_peaks()
+    return {
+        "metric": DECODE_METRIC, "value": round(ms_mean, 4), "unit": "ms/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_mean, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 w4a4 projections, bf16 lm_head, fp32 sampler",
+        "data": "synthetic (seeded random weights; fixed N(0,1) input hidden state; seeded uniforms)",
+        "config": {"workload": f"qwen3-32b decode step, M={M}, {args.layers} layers, lm_head 5120->151936, "
+                               f"ReSET sampler", "parallelism": f"replicas x{world}"},
+        "p50_ms": round(float(np.percentile(ms, 50)), 4), "p99_ms": round(float(np.percentile(ms, 99)), 4),
+        "tokens_per_s": round(world * M * 1000.0 / ms_mean, 1),
+        "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms_mean * 1e-3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(step_bytes / (ms_mean * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                     "kernel": "whole step: weight, lm_head and logits bytes / step time",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "clocks": clk.summary(),
+        "gpu_launches": (args.layers * 10 + 3) * args.steps,   # per layer: 2 norms, 4 quantizers, 4 GEMVs
+    }
+
+
 # ---------------------------------------------------------------------------
 def cpu_oracle_sample(args, seconds):
     """The oracle as it stands, on the host: per call, quantize the activation
@@ -406,6 +463,13 @@ def main():
                                  "sample": sample},
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return
+    if args.workload == "qwen3-32b-decode":
+        line = run_decode(args, world, rank)
+        if rank == 0:
+            print(json.dumps(line))
+        if world > 1:
+            torch.distributed.destroy_process_group()
         return
     result, calls, weights, ws = run_ours(args, world, rank)
     if not args.no_e2e:
