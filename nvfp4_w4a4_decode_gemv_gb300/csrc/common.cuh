@@ -111,6 +111,15 @@ NVFP4_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32
 // __threadfence).
 NVFP4_DEVINL void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// GPU-scope atomic add with acquire-release semantics: the calling thread's
+// earlier writes (and those ordered before them) are visible before the add,
+// and writes visible to the add are visible to the thread after it.
+NVFP4_DEVINL unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's completion and
 // memory, and let the next grid start launching.
 NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

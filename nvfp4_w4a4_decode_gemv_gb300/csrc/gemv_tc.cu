@@ -65,8 +65,8 @@ constexpr int kPackedBlock = kCodeBytes + kScaleBytes;      // 18432 bytes per [
 constexpr uint32_t kStageTx = kCodeBytes + kScaleBytes + kActBytes;
 constexpr int kWarps = 10;                  // 0 producer, 1 MMA, 2-5 scale writers, 6-9 epilogue
 constexpr int kThreads = 32 * kWarps;
-constexpr uint32_t kTmemCols = 256;         // D0 [0,16), D1 [16,32), then 32 scale columns per stage (S <= 7)
-constexpr uint32_t kColSF = 32;             // stage s: A scales at 32+32s+[0,16), B scales at 32+32s+16+[0,13)
+constexpr uint32_t kTmemCols = 256;         // D0 [0,16), D1 [16,32), D_last [32,48), 32 scale columns per stage (S <= 6)
+constexpr uint32_t kColSF = 48;             // stage s: A scales at 48+32s+[0,16), B scales at 48+32s+16+[0,13)
 // Instruction descriptor: E2M1 x E2M1 (format 1), UE4M3 scales, K-major A and B,
 // N = 16 (bits 17-22: N >> 3), M = 128 (bits 24-28: M >> 4), dense.
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
@@ -148,16 +148,18 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, int my_slot, int quad, int
     }
     return;
   }
-  float* part = a.partials + (((size_t)blockIdx.x * 2 + my_slot) * kTR + row) * M;
+  // Records are [CTA][slot][m][128 rows]: for each m the warp's 32 lanes touch
+  // 128 contiguous bytes.
+  float* part = a.partials + ((size_t)blockIdx.x * 2 + my_slot) * (size_t)(M * kTR) + row;
 #pragma unroll
-  for (int m = 0; m < M; ++m) __stcg(part + m, acc[m]);
+  for (int m = 0; m < M; ++m) __stcg(part + m * kTR, acc[m]);
   __syncwarp();                 // the warp's partial stores are ordered before lane 0's release
   unsigned int* cnt = a.counters + (size_t)tile * 4 + quad;
   int is_last = 0;
   if (lane == 0) {
-    fence_acq_rel_gpu();        // release: this warp's partials before the count
-    is_last = (atomicAdd(cnt, 1u) == (unsigned int)(last - first));
-    if (is_last) fence_acq_rel_gpu();   // acquire: every contributor's partials
+    // acquire-release add: this warp's partials are visible before the count,
+    // and the last contributor sees every other contributor's partials
+    is_last = (atom_add_acq_rel_gpu(cnt, 1u) == (unsigned int)(last - first));
   }
   is_last = __shfl_sync(0xffffffffu, is_last, 0);
   if (!is_last) return;
@@ -175,9 +177,9 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, int my_slot, int quad, int
     for (int i = 0; i < 4; ++i) {
       const long long qq = q + i;
       const int qs = (qq == first) ? first_slot : 0;
-      const float* pq = a.partials + (((size_t)qq * 2 + qs) * kTR + row) * M;
+      const float* pq = a.partials + ((size_t)qq * 2 + qs) * (size_t)(M * kTR) + row;
 #pragma unroll
-      for (int m = 0; m < M; ++m) v[i][m] = (qq <= last) ? __ldcg(pq + m) : 0.0f;
+      for (int m = 0; m < M; ++m) v[i][m] = (qq <= last) ? __ldcg(pq + m * kTR) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -194,6 +196,22 @@ NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, int my_slot, int quad, int
   if (lane == 0) *cnt = 0u;
 }
 
+// Read a quadrant's 16 accumulator columns of buffer d, then release the buffer.
+NVFP4_DEVINL void read_acc(uint32_t tmem, int quad, int d, uint64_t* acc_empty_d, float (&acc)[kNT]) {
+  uint32_t r[kNT];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(d * kNT)));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0 && acc_empty_d) mbar_arrive(acc_empty_d);
+#pragma unroll
+  for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
+}
+
 template <int M, int S>
 __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                               const __grid_constant__ CUtensorMap tm_scales,
@@ -206,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kSlot);
   uint64_t* sf_ready = full + S;
   uint64_t* empty = sf_ready + S;
-  uint64_t* acc_full = empty + S;
-  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* acc_full = empty + S;           // [0], [1]: alternating tiles; [2]: the CTA's last tile
+  uint64_t* acc_empty = acc_full + 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,10 +240,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       mbar_init(&sf_ready[s], 4);
       mbar_init(&empty[s], 1);
     }
-    for (int d = 0; d < 2; ++d) {
-      mbar_init(&acc_full[d], 1);
-      mbar_init(&acc_empty[d], 4);
-    }
+    for (int d = 0; d < 3; ++d) mbar_init(&acc_full[d], 1);
+    for (int d = 0; d < 2; ++d) mbar_init(&acc_empty[d], 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -313,22 +329,30 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       // moves by (slot offset + 32 q) / 16 within the 14-bit field.
       const uint64_t da0 = smem_desc_sw128(smem_u32(smem));
       const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB));
+      // The CTA's last tile accumulates in its own buffer (D_last), flushed by
+      // the scale writers; the others alternate between D0 and D1.
+      const int last_idx = (int)((u1 - 1) / C) - tile0;
       int tile_idx = -1;
       int c = chunk0;
       int s = 0;
       uint32_t phase = 0;
       int issued = 0;
+      uint32_t d_tmem = tmem;
       for (int k = 0; k < nunits; ++k) {
         const bool first_of_tile = (k == 0) || (c == 0);
         if (first_of_tile) {
           ++tile_idx;
-          if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) break;
+          if (tile_idx == last_idx) {
+            d_tmem = tmem + (uint32_t)(2 * kNT);
+          } else {
+            if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) break;
+            d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
+          }
         }
         // The scale writers arrive on sf_ready only after they have seen the
         // slot full, so sf_ready also orders the slot's data before the MMAs.
         if (!mbar_wait(&sf_ready[s], phase)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
         const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
         const uint32_t sfa = tmem + kColSF + 32u * s;
         const uint32_t sfb = sfa + 16u;
@@ -340,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         mma_commit(&empty[s]);
         issued = k + 1;
         if (++c == C) c = 0;
-        if (k + 1 == nunits || c == 0) mma_commit(&acc_full[tile_idx & 1]);   // last unit of this tile
+        if (k + 1 == nunits || c == 0)                                          // last unit of this tile
+          mma_commit(&acc_full[tile_idx == last_idx ? 2 : (tile_idx & 1)]);
         if (++s == S) { s = 0; phase ^= 1u; }
       }
       // Do not leave with MMAs in flight: wait (bounded) for the last commit.
@@ -378,28 +403,30 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       if (lane == 0) mbar_arrive(&sf_ready[s]);
       if (++s == S) { s = 0; phase ^= 1u; }
     }
+    // The CTA's last tile is flushed here, by warps that are idle once the
+    // scales are written, so it does not wait behind the earlier tiles' flushes.
+    if (nunits > 0) {
+      griddep_wait();
+      const int tile_last = (int)((u1 - 1) / C);
+      if (mbar_wait_warp(&acc_full[2], 0)) {
+        tc_fence_after();
+        float acc[kNT];
+        read_acc(tmem, quad, 2, nullptr, acc);
+        tc_flush<M>(a, tile_last, tile_last == tile0 ? 0 : 1, quad, lane, acc);
+      }
+    }
   } else {
     // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
     griddep_wait();            // y, the partial records and the counters belong to the preceding kernel's era
+    // Every tile but the CTA's last (that one is flushed by the scale writers).
     const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
-    for (int tile = tile0, tile_idx = 0; tile <= tile_last; ++tile, ++tile_idx) {
+    for (int tile = tile0, tile_idx = 0; tile < tile_last; ++tile, ++tile_idx) {
       const int d = tile_idx & 1;
       if (!mbar_wait_warp(&acc_full[d], (tile_idx >> 1) & 1)) break;
       tc_fence_after();
-      uint32_t r[kNT];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(d * kNT)));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[d]);
       float acc[kNT];
-#pragma unroll
-      for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
+      read_acc(tmem, quad, d, &acc_empty[d], acc);
       tc_flush<M>(a, tile, tile == tile0 ? 0 : 1, quad, lane, acc);
     }
   }
@@ -413,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
 
 template <int S>
 constexpr size_t tc_smem_bytes() {
-  return (size_t)S * kSlot + 1024 + (3 * S + 4) * sizeof(uint64_t) + 16;
+  return (size_t)S * kSlot + 1024 + (3 * S + 5) * sizeof(uint64_t) + 16;
 }
 
 }  // namespace
