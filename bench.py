@@ -10,15 +10,15 @@ step streams >= 245 MB of other weights, more than the 129 MB L2, so every
 call reads its weights from HBM (no flush kernel needed).
 
 value = algorithmic HBM bytes of the step (weight codes + scales, activation
-in/out, outputs) / device time of the step, in GB/s.  For each M the step is
-captured as one CUDA graph in decode-chain order (quantize -> GEMV, four
-times, with programmatic dependent launches so that each GEMV prefetches its
-weights while its quantizer runs).  The roofline times the GEMV kernels alone:
-graphs of the same GEMV launches, replayed right after the timed steps with
-events between them.  A cold-L2 breakdown per (projection, M) follows (512 MB
-flush before each call).  `e2e` repeats the step through the eager C-ABI calls
-with the activations copied from pinned host memory and the outputs copied
-back inside the timed region.
+in/out, outputs) / device time of the step, in GB/s.  The step is one CUDA
+graph in decode-chain order (quantize -> GEMV, 32 times, with programmatic
+dependent launches so that each GEMV prefetches its weights while its
+quantizer runs).  The roofline times the GEMV kernels alone: one graph of the
+same GEMV launches, replayed right after the timed steps; per-M graphs of the
+GEMVs give the per-M breakdown.  A cold-L2 breakdown per (projection, M)
+follows (512 MB flush before each call).  `e2e` repeats the step through the
+eager C-ABI calls with the activations copied from pinned host memory and the
+outputs copied back inside the timed region.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (for N > 1 under torch.distributed.run: N independent replicas, weak scaling).
@@ -213,53 +213,61 @@ def run_ours(args, world, rank):
     for M in order:                  # initialises kernel attributes outside capture
         step_m(groups[M])
     torch.cuda.synchronize()
-    # Per M: one graph of the chained step (quantize -> GEMV, x4, programmatic
-    # dependent launches between them), and one of the GEMVs alone whose
-    # replays, bracketed by events, time the GEMV kernel for the roofline.
+    # The whole step (every M, decode-chain order: quantize -> GEMV with
+    # programmatic dependent launches) is one CUDA graph; so are the GEMV
+    # launches alone, whose replays time the GEMV kernel for the roofline.  Per
+    # M, a graph of its GEMVs alone gives the per-M breakdown.
     stream = torch.cuda.Stream()
-    graphs, ggraphs = {}, {}
     with torch.cuda.stream(stream):
-        for M in order:
-            g, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
+        g_step, g_gemv = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=stream):
+            for M in order:
                 step_m(groups[M])
+        with torch.cuda.graph(g_gemv, stream=stream):
+            for M in order:
+                gemv_all(groups[M])
+        ggraphs = {}
+        for M in order:
+            gg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gg, stream=stream):
                 gemv_all(groups[M])
-            graphs[M], ggraphs[M] = g, gg
+            ggraphs[M] = gg
     torch.cuda.synchronize()
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in order]
-           for _ in range(args.steps)]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    ev_gemv = [(ev(), ev()) for _ in range(args.steps)]
+    ev_m = [[(ev(), ev()) for _ in order] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            for M in order:
-                graphs[M].replay()
-            for M in order:
-                ggraphs[M].replay()
+            g_step.replay()
+            g_gemv.replay()
     barrier(world)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0, t1 = ev(), ev()
     with ClockSampler(torch.cuda.current_device()) as clk:
         with torch.cuda.stream(stream):
             t0.record()
             for k in range(args.steps):          # the timed steps
-                for M in order:
-                    graphs[M].replay()
+                g_step.replay()
             t1.record()
             for k in range(args.steps):          # the GEMV kernels alone, same launches, for the roofline
+                ev_gemv[k][0].record()
+                g_gemv.replay()
+                ev_gemv[k][1].record()
+            for k in range(args.steps):          # per-M breakdown
                 for i, M in enumerate(order):
-                    evs[k][i][0].record()
+                    ev_m[k][i][0].record()
                     ggraphs[M].replay()
-                    evs[k][i][1].record()
+                    ev_m[k][i][1].record()
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(world, t0.elapsed_time(t1))
     clocks = clk.summary()
-    gemv_ms = {M: float(np.mean([evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)]))
+    gemv_ms_total = float(np.mean([a.elapsed_time(b) for a, b in ev_gemv]))
+    gemv_ms = {M: float(np.mean([ev_m[k][i][0].elapsed_time(ev_m[k][i][1]) for k in range(args.steps)]))
                for i, M in enumerate(order)}
     per_call = cold_per_call(calls, weights, ws, reps=3)
 
     step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
     value_gbs = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
-    gemv_ms_total = sum(gemv_ms.values())
     gemv_bytes_total = sum(c["gemv_bytes"] for c in calls)
     per_m = {f"M{M}": {"gemv_us_per_call": round(gemv_ms[M] * 1e3 / len(groups[M]), 2),
                        "gemv_gbs": round(sum(c["gemv_bytes"] for c in groups[M]) / (gemv_ms[M] * 1e-3) / 1e9, 1)}
@@ -287,7 +295,7 @@ def run_ours(args, world, rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": f"{gemv_name}: algorithmic bytes of all GEMV calls / their event-timed duration "
-                               "(graphs of the GEMV launches alone, replayed right after the timed steps)",
+                               "(one graph of the step's GEMV launches alone, replayed right after the timed steps)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clocks,
         "gpu_launches": len(calls) * launches_per_call * args.steps,
