@@ -63,7 +63,8 @@ int nvfp4_version(void);
 
 /*
  * Reads and clears the device error word of the current device.  A kernel sets
- * it (non-zero) when one of its bounded waits on an mbarrier gave up; the
+ * it (non-zero) when one of its bounded waits gave up: bit 0, a wait on an
+ * mbarrier; bit 2, a GEMV CTA's wait for another CTA's partial sum.  The
  * kernel then returned early and its outputs are incomplete.  Synchronous
  * (it copies 4 bytes from the device); not for use inside stream capture.
  */

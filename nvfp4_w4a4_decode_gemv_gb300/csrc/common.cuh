@@ -35,7 +35,18 @@ enum : unsigned int {
   NVFP4_DEVERR_NONE = 0,
   NVFP4_DEVERR_MBAR_TIMEOUT = 1,   // an mbarrier wait exceeded its iteration limit
   NVFP4_DEVERR_STATE_W = 2,        // reset_sample called with a window larger than the state's
+  NVFP4_DEVERR_FLAG_TIMEOUT = 4,   // a wait for another CTA's partial sum exceeded its iteration limit
 };
+
+// Release store / acquire load of a flag word at GPU scope.
+NVFP4_DEVINL void st_release_gpu(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+NVFP4_DEVINL unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // ~ 2^26 polls of try_wait (each try_wait itself suspends for a while): seconds,
 // far beyond any legitimate wait of these microsecond kernels.

@@ -397,7 +397,9 @@ struct WsLayout {
 // rows), so that calls of any shape that share a workspace find them at the
 // same place, and zero.
 constexpr int kMaxN = 1 << 20;
-constexpr size_t kCounterBytes = align256((size_t)(kMaxN / 32 + 64) * sizeof(unsigned int));
+constexpr int kFlagBase = kMaxN / 32 + 64;      // then 4 flag words per CTA of the tensor-core path
+constexpr int kMaxFlagCtas = 4096;
+constexpr size_t kCounterBytes = align256((size_t)(kFlagBase + 4 * kMaxFlagCtas) * sizeof(unsigned int));
 
 }  // namespace
 
@@ -483,8 +485,8 @@ bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
-                                   float* partials, unsigned int* counters, int grid_cap, int max_ctas_per_sm,
-                                   cudaStream_t stream);
+                                   float* partials, unsigned int* counters, unsigned int* flags, int grid_cap,
+                                   int max_ctas_per_sm, cudaStream_t stream);
 size_t nvfp4_internal_packed_bytes(int N, int K);
 cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
                                         cudaStream_t stream);
@@ -531,7 +533,8 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   if (use_tensor_cores(M)) {
     return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
         xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
-        reinterpret_cast<unsigned int*>(wsb + wl.counters), env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
+        reinterpret_cast<unsigned int*>(wsb + wl.counters), reinterpret_cast<unsigned int*>(wsb + wl.counters) + kFlagBase,
+        env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
   }
   GemvArgs a;
   a.xrec = wsb + wl.xrec;
@@ -609,5 +612,6 @@ extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
       xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
-      reinterpret_cast<unsigned int*>(wsb + wl.counters), env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
+      reinterpret_cast<unsigned int*>(wsb + wl.counters), reinterpret_cast<unsigned int*>(wsb + wl.counters) + kFlagBase,
+      env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
 }

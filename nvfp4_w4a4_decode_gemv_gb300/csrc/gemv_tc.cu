@@ -76,8 +76,9 @@ struct TcArgs {
   const float* xg;
   const float* wg;
   float* y;
-  float* partials;               // [G][2][128][M]: a CTA's first and last partial tile
-  unsigned int* counters;        // arrivals per (tile, 32-row quarter), zero between calls
+  float* partials;               // [G][2][M][128]: a CTA's records of its first and last tile
+  unsigned int* counters;        // arrivals per (tile, 32-row quarter); zero between calls
+  unsigned int* flags;           // one per (CTA, 32-row quarter); zero between calls
   int M, N, K, C, RT;
   int l2_units;                  // packed weights: units beyond the ring prefetched to L2 up front
   long long U;                   // units = RT * C, numbered tile-major
@@ -128,71 +129,130 @@ NVFP4_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
 NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { return (q * U) / G; }
 NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { return ((x + 1) * G - 1) / U; }
 
-// ---- epilogue: accumulator rows of one tile segment -> y, or a partial record ----
-// A tile that one CTA covers whole goes straight to y.  Otherwise each CTA
-// overlapping it writes a record (slot 0 for the CTA's first tile, slot 1 for
-// its last); the last to arrive (per 32-row quarter) adds the records in CTA
-// order, so the result does not depend on timing.
+// ---- Stream-K fix-up ---------------------------------------------------------------
+// A tile that one CTA covers whole goes straight to y.  A split tile's
+// contributors are the consecutive CTAs `first` .. `last`; each keeps a record
+// of its partial sums ([CTA][slot][m][128 rows]; slot 0 for the CTA's first
+// tile, slot 1 for its last).  Two ways to finish a split tile, chosen from the
+// split alone (so every contributor agrees):
+//  * two contributors, the second of which reaches the tile at the START of its
+//    range and goes on past it: the first contributor -- which reaches the tile
+//    at the END of its range -- finalizes.  The second stores its record and
+//    sets its flag (release); the first waits for the flag (acquire; normally
+//    long set, and it is read while its own last MMAs run), adds the record to
+//    its own sums and writes y.
+//  * otherwise: every contributor stores its record and counts itself on the
+//    tile's counter (acquire-release); the last to arrive adds the records in
+//    CTA order and writes y.
+// Flags and counters are reset by their reader, so all are zero between calls.
+// Either way the order of the additions is fixed by the split, so the result
+// does not depend on timing.
+constexpr uint32_t kFlagSpinLimit = 1u << 24;
+
+struct Split {                  // a tile's contributors and how the tile is finished
+  long long first, last;
+  bool whole, pair;
+};
+
+NVFP4_DEVINL Split split_of(const TcArgs& a, int tile, long long G) {
+  Split sp;
+  const long long C = a.C, t0 = (long long)tile * C;
+  sp.first = cta_of_unit(t0, a.U, G);
+  sp.last = cta_of_unit(t0 + C - 1, a.U, G);
+  sp.whole = sp.first == sp.last;
+  sp.pair = !sp.whole && sp.last == sp.first + 1 && unit_start(sp.last + 1, a.U, G) > t0 + C;
+  return sp;
+}
+
 template <int M>
-NVFP4_DEVINL void tc_flush(const TcArgs& a, int tile, int my_slot, int quad, int lane, const float (&acc)[kNT]) {
-  const long long G = gridDim.x, C = a.C;
-  const long long first = cta_of_unit((long long)tile * C, a.U, G);
-  const long long last = cta_of_unit((long long)tile * C + C - 1, a.U, G);
+NVFP4_DEVINL void store_y(const TcArgs& a, int tile, int row, const float (&v)[kNT]) {
   const float yscale = __fmul_rn(__ldg(a.xg), __ldg(a.wg));
-  const int row = quad * 32 + lane;
   const int n = tile * kTR + row;
-  if (first == last) {
-    if (n < a.N) {
+  if (n < a.N) {
 #pragma unroll
-      for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = acc[m] * yscale;
-    }
-    return;
+    for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = v[m] * yscale;
   }
-  // Records are [CTA][slot][m][128 rows]: for each m the warp's 32 lanes touch
-  // 128 contiguous bytes.
-  float* part = a.partials + ((size_t)blockIdx.x * 2 + my_slot) * (size_t)(M * kTR) + row;
+}
+
+template <int M>
+NVFP4_DEVINL float* record(const TcArgs& a, long long q, int slot, int row) {
+  return a.partials + ((size_t)q * 2 + slot) * (size_t)(M * kTR) + row;
+}
+
+template <int M>
+NVFP4_DEVINL void store_record(const TcArgs& a, int slot, int row, const float (&acc)[kNT]) {
+  float* rec = record<M>(a, blockIdx.x, slot, row);
 #pragma unroll
-  for (int m = 0; m < M; ++m) __stcg(part + m * kTR, acc[m]);
-  __syncwarp();                 // the warp's partial stores are ordered before lane 0's release
+  for (int m = 0; m < M; ++m) __stcg(rec + m * kTR, acc[m]);
+}
+
+// Second of a pair: record (slot 0) and flag.
+template <int M>
+NVFP4_DEVINL void publish_pair(const TcArgs& a, int quad, int lane, const float (&acc)[kNT]) {
+  store_record<M>(a, 0, quad * 32 + lane, acc);
+  __syncwarp();                 // the warp's record stores are ordered before lane 0's release
+  if (lane == 0) st_release_gpu(a.flags + (size_t)blockIdx.x * 4 + quad, 1u);
+}
+
+// First of a pair: the partner's record, once its flag is set.
+template <int M>
+NVFP4_DEVINL void gather_pair(const TcArgs& a, long long partner, int quad, int lane, float (&other)[kNT]) {
+  if (lane == 0) {
+    unsigned int* f = a.flags + (size_t)partner * 4 + quad;
+    uint32_t i = 0;
+    while (ld_acquire_gpu(f) == 0u) {
+      if (++i >= kFlagSpinLimit) {
+        atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    *f = 0u;                    // free for the next call
+  }
+  __syncwarp();                 // the lanes' record loads are ordered after lane 0's acquire
+  const float* rec = record<M>(a, partner, 0, quad * 32 + lane);
+#pragma unroll
+  for (int m = 0; m < kNT; ++m) other[m] = m < M ? __ldcg(rec + m * kTR) : 0.0f;
+}
+
+// Counted finish: record, count, and the last to arrive adds the records in CTA order.
+template <int M>
+NVFP4_DEVINL void counted_finish(const TcArgs& a, int tile, const Split& sp, int my_slot, int quad, int lane,
+                                 const float (&acc)[kNT]) {
+  const long long G = gridDim.x;
+  const int row = quad * 32 + lane;
+  store_record<M>(a, my_slot, row, acc);
+  __syncwarp();                 // the warp's record stores are ordered before lane 0's release
   unsigned int* cnt = a.counters + (size_t)tile * 4 + quad;
   int is_last = 0;
-  if (lane == 0) {
-    // acquire-release add: this warp's partials are visible before the count,
-    // and the last contributor sees every other contributor's partials
-    is_last = (atom_add_acq_rel_gpu(cnt, 1u) == (unsigned int)(last - first));
-  }
+  if (lane == 0) is_last = (atom_add_acq_rel_gpu(cnt, 1u) == (unsigned int)(sp.last - sp.first));
   is_last = __shfl_sync(0xffffffffu, is_last, 0);
   if (!is_last) return;
-  __syncwarp();                 // the lanes' partial loads are ordered after lane 0's acquire
+  __syncwarp();                 // the lanes' record loads are ordered after lane 0's acquire
   // Only the first contributor can have started before this tile (then the
   // tile is its slot 1); every later one starts inside it (slot 0).
-  const int first_slot = (unit_start(first, a.U, G) < (long long)tile * C) ? 1 : 0;
-  float sum[M];
+  const int first_slot = (unit_start(sp.first, a.U, G) < (long long)tile * a.C) ? 1 : 0;
+  float sum[kNT];
 #pragma unroll
-  for (int m = 0; m < M; ++m) sum[m] = 0.0f;
-  // Records in CTA order, four at a time with their loads issued together.
-  for (long long q = first; q <= last; q += 4) {
+  for (int m = 0; m < kNT; ++m) sum[m] = 0.0f;
+  for (long long q = sp.first; q <= sp.last; q += 4) {   // four records' loads issued together
     float v[4][M];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const long long qq = q + i;
-      const int qs = (qq == first) ? first_slot : 0;
-      const float* pq = a.partials + ((size_t)qq * 2 + qs) * (size_t)(M * kTR) + row;
+      const float* pq = record<M>(a, qq <= sp.last ? qq : sp.first, qq == sp.first ? first_slot : 0, row);
 #pragma unroll
-      for (int m = 0; m < M; ++m) v[i][m] = (qq <= last) ? __ldcg(pq + m * kTR) : 0.0f;
+      for (int m = 0; m < M; ++m) v[i][m] = (qq <= sp.last) ? __ldcg(pq + m * kTR) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      if (q + i <= last) {
+      if (q + i <= sp.last) {
 #pragma unroll
         for (int m = 0; m < M; ++m) sum[m] += v[i][m];
       }
     }
   }
-  if (n < a.N) {
-#pragma unroll
-    for (int m = 0; m < M; ++m) a.y[(size_t)m * a.N + n] = sum[m] * yscale;
-  }
+  store_y<M>(a, tile, row, sum);
   if (lane == 0) *cnt = 0u;
 }
 
@@ -408,11 +468,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     if (nunits > 0) {
       griddep_wait();
       const int tile_last = (int)((u1 - 1) / C);
+      const Split sp = split_of(a, tile_last, G);
+      const bool is_first = sp.first == (long long)blockIdx.x;
+      float other[kNT];
+      if (sp.pair && is_first) gather_pair<M>(a, sp.last, quad, lane, other);   // while the last MMAs run
       if (mbar_wait_warp(&acc_full[2], 0)) {
         tc_fence_after();
         float acc[kNT];
         read_acc(tmem, quad, 2, nullptr, acc);
-        tc_flush<M>(a, tile_last, tile_last == tile0 ? 0 : 1, quad, lane, acc);
+        if (sp.whole) {
+          store_y<M>(a, tile_last, quad * 32 + lane, acc);
+        } else if (sp.pair && is_first) {
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[m] += other[m];
+          store_y<M>(a, tile_last, quad * 32 + lane, acc);
+        } else if (sp.pair) {
+          publish_pair<M>(a, quad, lane, acc);           // (cannot happen: the pair's second goes past the tile)
+        } else {
+          counted_finish<M>(a, tile_last, sp, tile_last == tile0 ? 0 : 1, quad, lane, acc);
+        }
       }
     }
   } else {
@@ -427,7 +501,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       tc_fence_after();
       float acc[kNT];
       read_acc(tmem, quad, d, &acc_empty[d], acc);
-      tc_flush<M>(a, tile, tile == tile0 ? 0 : 1, quad, lane, acc);
+      // A tile before the last is whole, except the first when the range starts inside it.
+      if (tile == tile0 && u0 > (long long)tile0 * C) {
+        const Split sp = split_of(a, tile, G);
+        if (sp.pair) publish_pair<M>(a, quad, lane, acc);
+        else counted_finish<M>(a, tile, sp, 0, quad, lane, acc);
+      } else {
+        store_y<M>(a, tile, quad * 32 + lane, acc);
+      }
     }
   }
   tc_fence_before();
@@ -494,6 +575,7 @@ static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, in
   long long G = (long long)per_sm * nvfp4_internal_device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
+  if (G > 4096) G = 4096;                    // flag words exist for 4096 CTAs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
@@ -519,11 +601,12 @@ static cudaError_t launch_tc_m(int stages, const TcMaps& mp, const TcArgs& a, cu
 
 // Tensor-core GEMV; the caller has validated the arguments.  Weights come either
 // packed (wpacked != null, nvfp4_pack_weights layout) or as the row-major
-// codes and scales wq, ws.  `counters` holds RT * 4 tile counters (zero between calls).
+// codes and scales wq, ws.  `counters` holds RT * 4 tile counters and `flags`
+// 4 words per CTA (all zero between calls).
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
-                                   float* partials, unsigned int* counters, int grid_cap, int max_ctas_per_sm,
-                                   cudaStream_t stream) {
+                                   float* partials, unsigned int* counters, unsigned int* flags, int grid_cap,
+                                   int max_ctas_per_sm, cudaStream_t stream) {
   const char* st = getenv("NVFP4_GEMV_TC_STAGES");   // tuning knob: 4 (default), 5 or 6
   const int stages = st ? atoi(st) : 4;
   TcMaps mp;
@@ -541,6 +624,7 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
   a.y = y;
   a.partials = partials;
   a.counters = counters;
+  a.flags = flags;
   a.M = M;
   a.N = N;
   a.K = K;
