@@ -66,6 +66,16 @@ def test_full_size_sequence_prefix():
          synth.reset_uniforms(steps, M))
 
 
+def test_long_sequence_2048_steps():
+    """The sampler workload's length: M = 8 rows over 2048 positions, step
+    boundaries with gaps ~ Geometric(1/30) (long steps exercise the in-step mean
+    after the first w positions), sigma per position from {1, 3, 8}; V = 4096
+    keeps the oracle fast -- the state rules do not depend on V, and the full
+    vocabulary is covered by test_full_size_sequence_prefix."""
+    M, V, steps = 8, 4096, 2048
+    _run(M, V, steps, synth.reset_sigmas(steps), synth.reset_boundaries(steps, M), synth.reset_uniforms(steps, M))
+
+
 @pytest.mark.parametrize("V", [1, 2, 2047, 2048, 2049, 4096 + 5])
 def test_ragged_and_tiny_vocab(V):
     M, steps = 3, 6
