@@ -41,6 +41,26 @@ sys.path.insert(0, ROOT)
 from nvfp4_w4a4_decode_gemv_gb300 import synth  # noqa: E402
 
 METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Qwen3 shapes"
+
+# DRAM traffic of the tensor-core GEMV from one ncu capture of this bench (the
+# launch list in profiles/launch_list_qwen3-32b_sweep_tc.md): mean read + write
+# bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
+# source is the one that was measured.
+TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
+                  "sha256": "279574521b85bf58df439216edb9ad12635c9f70e011fbd3ada82b961478ddfe",
+                  "workload": "qwen3-32b", "bytes_per_launch": 68784872}
+
+
+def recorded_traffic(workload):
+    import hashlib
+    path = os.path.join(ROOT, TRAFFIC_RECORD["source"])
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    if digest != TRAFFIC_RECORD["sha256"] or workload != TRAFFIC_RECORD["workload"]:
+        return None
+    return TRAFFIC_RECORD["bytes_per_launch"]
 WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8]),
              "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8])}
 DECODE_METRIC = "Qwen3-32B-shaped decode step latency (64 NVFP4 layers + BF16 lm_head + ReSET sampler, one CUDA graph)"
@@ -293,7 +313,10 @@ def run_ours(args, world, rank):
                    "l2": "inputs larger than L2: >=245 MB of other weights between two uses of one matrix",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(args.workload) if args.weights == "packed" and not cuda_cores else None,
+                     "traffic_unit": "bytes per GEMV launch (ncu dram__bytes_read + dram__bytes_write, sweep mean)",
+                     "algorithmic_bytes_per_launch": round(gemv_bytes_total / len(calls)),
                      "kernel": f"{gemv_name}: algorithmic bytes of all GEMV calls / their event-timed duration "
                                "(one graph of the step's GEMV launches alone, replayed right after the timed steps)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
