@@ -47,8 +47,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "279574521b85bf58df439216edb9ad12635c9f70e011fbd3ada82b961478ddfe",
-                  "workload": "qwen3-32b", "bytes_per_launch": 68784872}
+                  "sha256": "ea42f453afe4b26dc96678d51a910742ce7f0e5f548ae165e72d8f4a382fabc6",
+                  "workload": "qwen3-32b", "bytes_per_launch": 68769699}
 
 
 def recorded_traffic(workload):

@@ -80,7 +80,6 @@ struct TcArgs {
   unsigned int* counters;        // arrivals per (tile, 32-row quarter); zero between calls
   unsigned int* flags;           // one per (CTA, 32-row quarter); zero between calls
   int M, N, K, C, RT;
-  int l2_units;                  // packed weights: units beyond the ring prefetched to L2 up front
   long long U;                   // units = RT * C, numbered tile-major
 };
 
@@ -112,10 +111,6 @@ NVFP4_DEVINL void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Bulk prefetch of global memory into L2 (no completion to wait for).
-NVFP4_DEVINL void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Bounded wait by a whole warp: lane 0 polls, the outcome is broadcast so that
 // the warp stays converged (also when the wait gives up).
@@ -332,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       const int pre = nunits < S ? nunits : S;
       const uint8_t* wp = a.wpacked ? a.wpacked + (size_t)u0 * kPackedBlock : nullptr;
       // Weight tiles do not depend on the preceding kernel: issue the first
-      // stages, and ask L2 for the units after them, before waiting on it.
+      // stages before waiting on it.
       {
         int tile = tile0, c = chunk0;
         for (int k = 0; k < pre; ++k) {
@@ -345,10 +340,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
             tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
           }
           if (++c == C) { c = 0; ++tile; }
-        }
-        if (wp) {
-          const int l2_end = (pre + a.l2_units < nunits) ? pre + a.l2_units : nunits;
-          for (int k = pre; k < l2_end; ++k) prefetch_l2(wp + (size_t)k * kPackedBlock, kPackedBlock);
         }
       }
       griddep_wait();          // the token codes and scales come from the preceding kernel
@@ -631,8 +622,6 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
   a.C = K / kChunk;
   a.RT = (N + kTR - 1) / kTR;
   a.U = (long long)a.RT * a.C;
-  const char* l2 = getenv("NVFP4_GEMV_L2_UNITS");   // tuning knob: units prefetched to L2 per CTA (default 0: it delays the first stages)
-  a.l2_units = l2 ? atoi(l2) : 0;
   switch (M) {
     case 1: return launch_tc_m<1>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     case 2: return launch_tc_m<2>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);

@@ -106,6 +106,14 @@ NVFP4_DEVINL uint32_t quant_block(const float v[16], float bm, float g, uint2& c
   const float t = (d > 0.0f) ? __fdiv_rn(bm, d) : 0.0f;
   const uint32_t s = f32x2_to_e4m3x2(0.0f, t) & 0xFFu;
   const float S = __fmul_rn(e4m3_to_f32(s), g);
+  // The code of v = x / S (IEEE quotient) is that of p = x * r with r = 1/S
+  // (IEEE reciprocal) unless an E2M1 decision point (0.25, 0.75, ..., 5) lies
+  // within the few ulps that separate p from v: |p - v| < 1.5 * 2^-23 |v|.  So
+  // when the codes of p (1 - 2^-20) and p (1 + 2^-20) agree, every value in
+  // between -- v among them -- has that code; otherwise divide.
+  const float r = (S > 0.0f) ? __frcp_rn(S) : 0.0f;
+  const bool fast = r > 0.0f && r < 1.0e38f;
+  constexpr float kLo = 1.0f - 0x1.0p-20f, kHi = 1.0f + 0x1.0p-20f;
   uint32_t packed[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -113,7 +121,14 @@ NVFP4_DEVINL uint32_t quant_block(const float v[16], float bm, float g, uint2& c
     const uint32_t sgn = ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
     uint32_t byte = sgn;
     if (S > 0.0f) {
-      const uint32_t q = f32x2_to_e2m1x2(__fdiv_rn(hi, S), __fdiv_rn(lo, S));
+      uint32_t q = 0x100u;           // no code yet
+      if (fast) {
+        const float pl = __fmul_rn(lo, r), ph = __fmul_rn(hi, r);
+        const uint32_t qa = f32x2_to_e2m1x2(__fmul_rn(ph, kLo), __fmul_rn(pl, kLo));
+        const uint32_t qb = f32x2_to_e2m1x2(__fmul_rn(ph, kHi), __fmul_rn(pl, kHi));
+        if (qa == qb) q = qa;
+      }
+      if (q == 0x100u) q = f32x2_to_e2m1x2(__fdiv_rn(hi, S), __fdiv_rn(lo, S));
       byte = (q & 0x77u) | sgn;       // magnitude from the conversion, sign from x
     }
     packed[i >> 2] |= byte << (8 * (i & 3));
