@@ -136,6 +136,11 @@ NVFP4_DEVINL unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) 
 NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Ask L2 for the line holding p (a hint: no effect on what a later load sees).
+NVFP4_DEVINL void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 NVFP4_DEVINL void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -35,6 +35,7 @@ struct SrcBF16 {
   const uint16_t* x;
   int nbr;      // blocks per row = K / 16
   int K;
+  __device__ void prefetch(long b) const { prefetch_l2(x + (b / nbr) * (long)K + (b % nbr) * 16); }
   __device__ void load(long b, float v[16]) const {
     const long r = b / nbr, c = b % nbr;
     const uint4* p = reinterpret_cast<const uint4*>(x + r * (long)K + c * 16);
@@ -56,6 +57,7 @@ struct SrcF32 {
   const float* x;
   int nbr;
   long ld;
+  __device__ void prefetch(long b) const { prefetch_l2(x + (b / nbr) * ld + (b % nbr) * 16); }
   __device__ void load(long b, float v[16]) const {
     const long r = b / nbr, c = b % nbr;
     const float4* p = reinterpret_cast<const float4*>(x + r * ld + c * 16);
@@ -75,6 +77,11 @@ struct SrcSiluMul {
   const float* gu;
   int nbr;   // I / 16
   int I;
+  __device__ void prefetch(long b) const {
+    const float* pg = gu + (b / nbr) * 2L * I + (b % nbr) * 16;
+    prefetch_l2(pg);
+    prefetch_l2(pg + I);
+  }
   __device__ void load(long b, float v[16]) const {
     const long r = b / nbr, c = b % nbr;
     const float4* pg = reinterpret_cast<const float4*>(gu + r * 2L * I + c * 16);
@@ -149,12 +156,19 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
   // its CTAs take over SMs as the preceding GEMV's CTAs leave and prefetch their
   // first weight tiles -- then wait for the preceding kernel, which may produce
   // this kernel's input.
+  // Before that wait, ask L2 for this thread's input: when the input does not
+  // come from the preceding kernel, its HBM latency overlaps that kernel's
+  // tail; when it does, the hint is harmless (the loads below come after the
+  // wait and see the preceding kernel's writes).
   if (!trigger_late) griddep_launch_dependents();
-  griddep_wait();
   const uint32_t rank = cluster_ctarank();
   const uint32_t csize = gridDim.x;          // the whole grid is one cluster
   const long T = (long)csize * kCThreads;
   const long gt = (long)rank * kCThreads + threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < NB; ++i)
+    if (gt + i * T < nblocks) src.prefetch(gt + i * T);
+  griddep_wait();
 
   float v[NB][16];
   float bm[NB];
