@@ -48,6 +48,16 @@ NVFP4_DEVINL unsigned int ld_acquire_gpu(const unsigned int* p) {
   return v;
 }
 
+// Relaxed GPU-scope word store / load: single-copy atomic, no ordering.
+NVFP4_DEVINL void st_relaxed_gpu(unsigned int* p, unsigned int v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+NVFP4_DEVINL unsigned int ld_relaxed_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ~ 2^26 polls of try_wait (each try_wait itself suspends for a while): seconds,
 // far beyond any legitimate wait of these microsecond kernels.
 constexpr uint32_t kMbarSpinLimit = 1u << 26;

@@ -390,35 +390,36 @@ constexpr int kMaxTileRows = 128;
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t xrec, counters, partials, total;
+  size_t xrec, counters, tcrec, partials, total;
 };
 
 // Counters sit first, in a fixed-size region (one per 32-row group of weight
 // rows), so that calls of any shape that share a workspace find them at the
 // same place, and zero.
 constexpr int kMaxN = 1 << 20;
-constexpr int kFlagBase = kMaxN / 32 + 64;      // then 4 flag words per CTA of the tensor-core path
-constexpr int kMaxFlagCtas = 4096;
-constexpr size_t kCounterBytes = align256((size_t)(kFlagBase + 4 * kMaxFlagCtas) * sizeof(unsigned int));
+constexpr size_t kCounterBytes = align256((size_t)(kMaxN / 32 + 64) * sizeof(unsigned int));
 
 }  // namespace
 
 
 // Defined in gemv_tc.cu.
-size_t nvfp4_internal_tc_partial_bytes(int M, int N, int K);
+size_t nvfp4_internal_tc_record_bytes();
 
 namespace {
 
-// [counters][activation records of the CUDA-core path][partial sums of either path]
+// [counters][records of the tensor-core path][activation records of the
+// CUDA-core path][partial sums of the CUDA-core path].  The first two sit at
+// fixed places (their size does not depend on the shape) because they must be
+// zero at the start of every call, whatever the shape of the previous one.
 WsLayout ws_layout(int M, int N, int K) {
+  (void)N;
   WsLayout l;
   l.counters = 0;
-  l.xrec = kCounterBytes;
+  l.tcrec = kCounterBytes;
+  l.xrec = l.tcrec + align256(nvfp4_internal_tc_record_bytes());
   l.partials = l.xrec + align256((size_t)M * (K / 16) * kRecBytes);
   const size_t gmax = (size_t)device_sms() * kMaxCtasPerSm;
-  const size_t cc = gmax * 2 * kMaxTileRows * (size_t)M * sizeof(float);
-  const size_t tc = nvfp4_internal_tc_partial_bytes(M, N, K);
-  l.total = l.partials + align256(cc > tc ? cc : tc);
+  l.total = l.partials + align256(gmax * 2 * kMaxTileRows * (size_t)M * sizeof(float));
   return l;
 }
 
@@ -485,8 +486,7 @@ bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
-                                   float* partials, unsigned int* counters, unsigned int* flags, int grid_cap,
-                                   int max_ctas_per_sm, cudaStream_t stream);
+                                   unsigned int* records, int grid_cap, int max_ctas_per_sm, cudaStream_t stream);
 size_t nvfp4_internal_packed_bytes(int N, int K);
 cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
                                         cudaStream_t stream);
@@ -532,8 +532,7 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   if (use_tensor_cores(M)) {
     return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
-        xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
-        reinterpret_cast<unsigned int*>(wsb + wl.counters), reinterpret_cast<unsigned int*>(wsb + wl.counters) + kFlagBase,
+        xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
         env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
   }
   GemvArgs a;
@@ -611,7 +610,6 @@ extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_
   if (ds != NVFP4_OK) return ds;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
-      xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<float*>(wsb + wl.partials),
-      reinterpret_cast<unsigned int*>(wsb + wl.counters), reinterpret_cast<unsigned int*>(wsb + wl.counters) + kFlagBase,
+      xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
       env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
 }

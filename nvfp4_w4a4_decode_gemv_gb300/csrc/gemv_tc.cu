@@ -35,8 +35,8 @@
 //                   tcgen05.commit frees the slot
 //   4 epilogue warps read the accumulator (double buffered) at tile ends and
 //                   write y, or partial sums for the Stream-K fix-up
-// Work split and fix-up follow gemv.cu (Stream-K over [tile x 256-K] units,
-// the last arriver sums partials in CTA order).
+// Work split as in gemv.cu (Stream-K over [tile x 256-K] units); a split tile
+// is finished by its first contributor (see the fix-up section below).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
@@ -76,9 +76,7 @@ struct TcArgs {
   const float* xg;
   const float* wg;
   float* y;
-  float* partials;               // [G][2][M][128]: a CTA's records of its first and last tile
-  unsigned int* counters;        // arrivals per (tile, 32-row quarter); zero between calls
-  unsigned int* flags;           // one per (CTA, 32-row quarter); zero between calls
+  unsigned int* records;         // [G][M][128] words: a CTA's partial sums of its first tile; zero between calls
   int M, N, K, C, RT;
   long long U;                   // units = RT * C, numbered tile-major
 };
@@ -126,27 +124,20 @@ NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { retu
 
 // ---- Stream-K fix-up ---------------------------------------------------------------
 // A tile that one CTA covers whole goes straight to y.  A split tile's
-// contributors are the consecutive CTAs `first` .. `last`; each keeps a record
-// of its partial sums ([CTA][slot][m][128 rows]; slot 0 for the CTA's first
-// tile, slot 1 for its last).  Two ways to finish a split tile, chosen from the
-// split alone (so every contributor agrees):
-//  * two contributors, the second of which reaches the tile at the START of its
-//    range and goes on past it: the first contributor -- which reaches the tile
-//    at the END of its range -- finalizes.  The second stores its record and
-//    sets its flag (release); the first waits for the flag (acquire; normally
-//    long set, and it is read while its own last MMAs run), adds the record to
-//    its own sums and writes y.
-//  * otherwise: every contributor stores its record and counts itself on the
-//    tile's counter (acquire-release); the last to arrive adds the records in
-//    CTA order and writes y.
-// Flags and counters are reset by their reader, so all are zero between calls.
-// Either way the order of the additions is fixed by the split, so the result
-// does not depend on timing.
+// contributors are the consecutive CTAs `first` .. `last`.  For every one but
+// the first the tile is the first of its range: it writes its partial sums to
+// its record and is done.  For the first the tile is the last of its range: it
+// adds the others' records, in CTA order, to its own sums and writes y.
+// A record word holds the bitwise complement of an FP32 partial sum; a finite
+// value never encodes to zero, so a word is ready once it is non-zero and needs
+// no flag, counter or fence, and the reader puts the zero back.  Records are
+// therefore zero between calls, and the order of the additions is fixed by
+// the split alone, so the result does not depend on timing.
 constexpr uint32_t kFlagSpinLimit = 1u << 24;
 
-struct Split {                  // a tile's contributors and how the tile is finished
+struct Split {                  // a tile's contributors
   long long first, last;
-  bool whole, pair;
+  bool whole;
 };
 
 NVFP4_DEVINL Split split_of(const TcArgs& a, int tile, long long G) {
@@ -155,7 +146,6 @@ NVFP4_DEVINL Split split_of(const TcArgs& a, int tile, long long G) {
   sp.first = cta_of_unit(t0, a.U, G);
   sp.last = cta_of_unit(t0 + C - 1, a.U, G);
   sp.whole = sp.first == sp.last;
-  sp.pair = !sp.whole && sp.last == sp.first + 1 && unit_start(sp.last + 1, a.U, G) > t0 + C;
   return sp;
 }
 
@@ -170,85 +160,53 @@ NVFP4_DEVINL void store_y(const TcArgs& a, int tile, int row, const float (&v)[k
 }
 
 template <int M>
-NVFP4_DEVINL float* record(const TcArgs& a, long long q, int slot, int row) {
-  return a.partials + ((size_t)q * 2 + slot) * (size_t)(M * kTR) + row;
+NVFP4_DEVINL unsigned int* record(const TcArgs& a, long long q, int row) {
+  return a.records + (size_t)q * (size_t)(M * kTR) + row;
 }
 
+// A contributor other than the first: its partial sums, encoded.
 template <int M>
-NVFP4_DEVINL void store_record(const TcArgs& a, int slot, int row, const float (&acc)[kNT]) {
-  float* rec = record<M>(a, blockIdx.x, slot, row);
+NVFP4_DEVINL void publish_record(const TcArgs& a, int row, const float (&acc)[kNT]) {
+  unsigned int* rec = record<M>(a, blockIdx.x, row);
 #pragma unroll
-  for (int m = 0; m < M; ++m) __stcg(rec + m * kTR, acc[m]);
+  for (int m = 0; m < M; ++m) st_relaxed_gpu(rec + m * kTR, ~__float_as_uint(acc[m]));
 }
 
-// Second of a pair: record (slot 0) and flag.
+// The records of contributors q0 .. q0+3 (those <= last), once every word is
+// written (bounded wait); each word read is reset to zero.
 template <int M>
-NVFP4_DEVINL void publish_pair(const TcArgs& a, int quad, int lane, const float (&acc)[kNT]) {
-  store_record<M>(a, 0, quad * 32 + lane, acc);
-  __syncwarp();                 // the warp's record stores are ordered before lane 0's release
-  if (lane == 0) st_release_gpu(a.flags + (size_t)blockIdx.x * 4 + quad, 1u);
-}
-
-// First of a pair: the partner's record, once its flag is set.
-template <int M>
-NVFP4_DEVINL void gather_pair(const TcArgs& a, long long partner, int quad, int lane, float (&other)[kNT]) {
-  if (lane == 0) {
-    unsigned int* f = a.flags + (size_t)partner * 4 + quad;
-    uint32_t i = 0;
-    while (ld_acquire_gpu(f) == 0u) {
-      if (++i >= kFlagSpinLimit) {
-        atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-    *f = 0u;                    // free for the next call
-  }
-  __syncwarp();                 // the lanes' record loads are ordered after lane 0's acquire
-  const float* rec = record<M>(a, partner, 0, quad * 32 + lane);
-#pragma unroll
-  for (int m = 0; m < kNT; ++m) other[m] = m < M ? __ldcg(rec + m * kTR) : 0.0f;
-}
-
-// Counted finish: record, count, and the last to arrive adds the records in CTA order.
-template <int M>
-NVFP4_DEVINL void counted_finish(const TcArgs& a, int tile, const Split& sp, int my_slot, int quad, int lane,
-                                 const float (&acc)[kNT]) {
-  const long long G = gridDim.x;
-  const int row = quad * 32 + lane;
-  store_record<M>(a, my_slot, row, acc);
-  __syncwarp();                 // the warp's record stores are ordered before lane 0's release
-  unsigned int* cnt = a.counters + (size_t)tile * 4 + quad;
-  int is_last = 0;
-  if (lane == 0) is_last = (atom_add_acq_rel_gpu(cnt, 1u) == (unsigned int)(sp.last - sp.first));
-  is_last = __shfl_sync(0xffffffffu, is_last, 0);
-  if (!is_last) return;
-  __syncwarp();                 // the lanes' record loads are ordered after lane 0's acquire
-  // Only the first contributor can have started before this tile (then the
-  // tile is its slot 1); every later one starts inside it (slot 0).
-  const int first_slot = (unit_start(sp.first, a.U, G) < (long long)tile * a.C) ? 1 : 0;
-  float sum[kNT];
-#pragma unroll
-  for (int m = 0; m < kNT; ++m) sum[m] = 0.0f;
-  for (long long q = sp.first; q <= sp.last; q += 4) {   // four records' loads issued together
-    float v[4][M];
+NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, int row, float (&v)[4][M]) {
+  unsigned int w[4][M];
+  uint32_t spins = 0;
+  for (;;) {
+    bool ready = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const long long qq = q + i;
-      const float* pq = record<M>(a, qq <= sp.last ? qq : sp.first, qq == sp.first ? first_slot : 0, row);
+      const bool live = q0 + i <= last;
+      const unsigned int* rec = record<M>(a, live ? q0 + i : q0, row);
 #pragma unroll
-      for (int m = 0; m < M; ++m) v[i][m] = (qq <= sp.last) ? __ldcg(pq + m * kTR) : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (q + i <= sp.last) {
-#pragma unroll
-        for (int m = 0; m < M; ++m) sum[m] += v[i][m];
+      for (int m = 0; m < M; ++m) {
+        w[i][m] = live ? ld_relaxed_gpu(rec + m * kTR) : ~0u;
+        ready = ready && w[i][m] != 0u;
       }
     }
+    if (ready) break;
+    if (++spins >= kFlagSpinLimit) {
+      atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
+      break;
+    }
+    __nanosleep(32);
   }
-  store_y<M>(a, tile, row, sum);
-  if (lane == 0) *cnt = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool live = q0 + i <= last;
+    unsigned int* rec = record<M>(a, live ? q0 + i : q0, row);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      v[i][m] = __uint_as_float(~w[i][m]);
+      if (live) st_relaxed_gpu(rec + m * kTR, 0u);
+    }
+  }
 }
 
 // Read a quadrant's 16 accumulator columns of buffer d, then release the buffer.
@@ -459,31 +417,44 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     if (nunits > 0) {
       griddep_wait();
       const int tile_last = (int)((u1 - 1) / C);
+      const int row = quad * 32 + lane;
       const Split sp = split_of(a, tile_last, G);
-      const bool is_first = sp.first == (long long)blockIdx.x;
-      float other[kNT];
-      if (sp.pair && is_first) gather_pair<M>(a, sp.last, quad, lane, other);   // while the last MMAs run
+      const bool fin = !sp.whole && sp.first == (long long)blockIdx.x;   // this CTA finishes the tile
+      float pre[4][M];
+      if (fin) take_records<M>(a, sp.first + 1, sp.last, row, pre);      // while the last MMAs run
       if (mbar_wait_warp(&acc_full[2], 0)) {
         tc_fence_after();
         float acc[kNT];
         read_acc(tmem, quad, 2, nullptr, acc);
         if (sp.whole) {
-          store_y<M>(a, tile_last, quad * 32 + lane, acc);
-        } else if (sp.pair && is_first) {
+          store_y<M>(a, tile_last, row, acc);
+        } else if (fin) {
 #pragma unroll
-          for (int m = 0; m < M; ++m) acc[m] += other[m];
-          store_y<M>(a, tile_last, quad * 32 + lane, acc);
-        } else if (sp.pair) {
-          publish_pair<M>(a, quad, lane, acc);           // (cannot happen: the pair's second goes past the tile)
+          for (int i = 0; i < 4; ++i)
+            if (sp.first + 1 + i <= sp.last) {
+#pragma unroll
+              for (int m = 0; m < M; ++m) acc[m] += pre[i][m];
+            }
+          for (long long q = sp.first + 5; q <= sp.last; q += 4) {
+            float v[4][M];
+            take_records<M>(a, q, sp.last, row, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (q + i <= sp.last) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[m] += v[i][m];
+              }
+          }
+          store_y<M>(a, tile_last, row, acc);
         } else {
-          counted_finish<M>(a, tile_last, sp, tile_last == tile0 ? 0 : 1, quad, lane, acc);
+          publish_record<M>(a, row, acc);
         }
       }
     }
   } else {
     // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
-    griddep_wait();            // y, the partial records and the counters belong to the preceding kernel's era
+    griddep_wait();            // y and the records belong to the preceding kernel's era
     // Every tile but the CTA's last (that one is flushed by the scale writers).
     const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
     for (int tile = tile0, tile_idx = 0; tile < tile_last; ++tile, ++tile_idx) {
@@ -492,11 +463,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       tc_fence_after();
       float acc[kNT];
       read_acc(tmem, quad, d, &acc_empty[d], acc);
-      // A tile before the last is whole, except the first when the range starts inside it.
+      // A tile before the last is whole, except the first when the range
+      // starts inside it: then this CTA is not the tile's first contributor.
       if (tile == tile0 && u0 > (long long)tile0 * C) {
-        const Split sp = split_of(a, tile, G);
-        if (sp.pair) publish_pair<M>(a, quad, lane, acc);
-        else counted_finish<M>(a, tile, sp, 0, quad, lane, acc);
+        publish_record<M>(a, quad * 32 + lane, acc);
       } else {
         store_y<M>(a, tile, quad * 32 + lane, acc);
       }
@@ -525,12 +495,9 @@ int nvfp4_internal_device_sms();
 // CTAs of the tensor-core GEMV per device (two per SM at the default depth).
 static int tc_grid_max() { return 2 * nvfp4_internal_device_sms(); }
 
-// Partial records: two of 128 x M floats per CTA.
-size_t nvfp4_internal_tc_partial_bytes(int M, int N, int K) {
-  (void)N;
-  (void)K;
-  return (size_t)tc_grid_max() * 2 * kTR * (size_t)M * sizeof(float);
-}
+// Records: 128 x 8 words per CTA, at a fixed place in the workspace (they
+// must stay zero between calls of any shape).
+size_t nvfp4_internal_tc_record_bytes() { return (size_t)tc_grid_max() * kTR * 8 * sizeof(unsigned int); }
 
 struct TcMaps {
   CUtensorMap w_codes, w_scales, x_codes, x_scales;
@@ -566,7 +533,7 @@ static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, in
   long long G = (long long)per_sm * nvfp4_internal_device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
-  if (G > 4096) G = 4096;                    // flag words exist for 4096 CTAs
+  if (G > tc_grid_max()) G = tc_grid_max();  // records exist for that many CTAs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
@@ -592,12 +559,11 @@ static cudaError_t launch_tc_m(int stages, const TcMaps& mp, const TcArgs& a, cu
 
 // Tensor-core GEMV; the caller has validated the arguments.  Weights come either
 // packed (wpacked != null, nvfp4_pack_weights layout) or as the row-major
-// codes and scales wq, ws.  `counters` holds RT * 4 tile counters and `flags`
-// 4 words per CTA (all zero between calls).
+// codes and scales wq, ws.  `records` holds nvfp4_internal_tc_record_bytes()
+// bytes, zero between calls.
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
-                                   float* partials, unsigned int* counters, unsigned int* flags, int grid_cap,
-                                   int max_ctas_per_sm, cudaStream_t stream) {
+                                   unsigned int* records, int grid_cap, int max_ctas_per_sm, cudaStream_t stream) {
   const char* st = getenv("NVFP4_GEMV_TC_STAGES");   // tuning knob: 4 (default), 5 or 6
   const int stages = st ? atoi(st) : 4;
   TcMaps mp;
@@ -613,9 +579,7 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
   a.xg = xg;
   a.wg = wg;
   a.y = y;
-  a.partials = partials;
-  a.counters = counters;
-  a.flags = flags;
+  a.records = records;
   a.M = M;
   a.N = N;
   a.K = K;
