@@ -177,8 +177,12 @@ NVFP4_DEVINL void publish_record(const TcArgs& a, int row, const float (&acc)[kN
 template <int M>
 NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, int row, float (&v)[4][M]) {
   unsigned int w[4][M];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m) w[i][m] = 0u;
   uint32_t spins = 0;
-  for (;;) {
+  for (;;) {                    // load the words not seen yet (all of them the first time)
     bool ready = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -186,7 +190,7 @@ NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, in
       const unsigned int* rec = record<M>(a, live ? q0 + i : q0, row);
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        w[i][m] = live ? ld_relaxed_gpu(rec + m * kTR) : ~0u;
+        if (w[i][m] == 0u) w[i][m] = live ? ld_relaxed_gpu(rec + m * kTR) : ~0u;
         ready = ready && w[i][m] != 0u;
       }
     }
