@@ -434,6 +434,25 @@ def run_decode(args, world, rank):
     barrier(world)
     ms = np.array([a.elapsed_time(b) for a, b in evs])
     ms_mean = max_over_ranks(world, float(ms.mean()))
+    # End to end: every step copies its inputs (hidden state, uniforms) in from
+    # pinned host memory, replays the step and copies the tokens, entropies and
+    # temperatures back.
+    host_h = st.h_in.cpu().pin_memory()
+    host_u = us.cpu().pin_memory()
+    host_out = torch.empty(3 * M, dtype=torch.int32).pin_memory()
+    outs = (st.sampler.token, st.sampler.H.view(torch.int32), st.sampler.T.view(torch.int32))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for i in range(args.steps):
+            st.h_in.copy_(host_h, non_blocking=True)
+            st.u.copy_(host_u[1 + args.warmup + i], non_blocking=True)
+            g.replay()
+            for k, t in enumerate(outs):
+                host_out[k * M:(k + 1) * M].copy_(t, non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
     weight_bytes = sum(w.packed.numel() for layer in st.weights for w in layer.values())
     step_bytes = weight_bytes + st.lm_head.numel() * 2 + st.logits.numel() * 4 * 2
     peak, peak_kind = measured_peaks()
@@ -450,6 +469,8 @@ def run_decode(args, world, rank):
                      "unit": "GB/s", "frac": round(step_bytes / (ms_mean * 1e-3) / 1e9 / peak, 4), "traffic": None,
                      "kernel": "whole step: weight, lm_head and logits bytes / step time",
                      "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms/step", "h2d_bytes_per_step": host_h.numel() * 4 + M * 4,
+                "d2h_bytes_per_step": 3 * M * 4},
         "clocks": clk.summary(),
         "gpu_launches": (args.layers * 10 + 3) * args.steps,   # per layer: 2 norms, 4 quantizers, 4 GEMVs
     }

@@ -177,6 +177,10 @@ NVFP4_DEVINL uint32_t dsmem_addr(const void* local, uint32_t rank) {
   return out;
 }
 
+NVFP4_DEVINL void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 NVFP4_DEVINL float ld_dsmem_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

@@ -149,8 +149,12 @@ template <class Src, int NB>
 __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long nblocks, uint8_t* codes,
                                                                   uint8_t* scales, float* global, int trigger_late) {
   __shared__ float s_warp[kCThreads / 32];
-  __shared__ float s_cta_max;
-  __shared__ float s_amax;
+  __shared__ float s_peer[kMaxCluster];      // slot r: the maximum of CTA r of the cluster
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t csize = gridDim.x;          // the whole grid is one cluster
+  // Peers may write into this CTA's shared memory only once it runs: arrive
+  // now, wait just before the first remote store.
+  if (csize > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // Programmatic dependent launch: let the next kernel (the GEMV) start
   // launching at once -- it reads only weights until it waits on this grid, so
   // its CTAs take over SMs as the preceding GEMV's CTAs leave and prefetch their
@@ -161,8 +165,6 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
   // tail; when it does, the hint is harmless (the loads below come after the
   // wait and see the preceding kernel's writes).
   if (!trigger_late) griddep_launch_dependents();
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t csize = gridDim.x;          // the whole grid is one cluster
   const long T = (long)csize * kCThreads;
   const long gt = (long)rank * kCThreads + threadIdx.x;
 #pragma unroll
@@ -189,25 +191,23 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
   for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
   if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = local;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float m = threadIdx.x < kCThreads / 32 ? s_warp[threadIdx.x] : 0.0f;
+  // Every warp reduces the warp maxima itself: no second block barrier.
+  const int lane = threadIdx.x & 31;
+  float amax = lane < kCThreads / 32 ? s_warp[lane] : 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (threadIdx.x == 0) s_cta_max = m;
-  }
-  cluster_sync();                            // every CTA's s_cta_max is visible cluster-wide
-  // Warp 0 gathers the CTA maxima (one remote read per lane), then this CTA
-  // signals that it is done reading its peers; the matching wait sits at the
-  // end, so that no CTA leaves while a peer may still read its shared memory.
-  if (threadIdx.x < 32) {
-    float m = threadIdx.x < csize ? ld_dsmem_f32(dsmem_addr(&s_cta_max, threadIdx.x)) : 0.0f;
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (csize > 1) {
+    // Push this CTA's maximum into slot `rank` of every CTA, then one cluster
+    // barrier (release / acquire); after it each CTA reads only its own shared
+    // memory, so no CTA touches a peer's once the barrier has passed.
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (threadIdx.x < csize) st_dsmem_f32(dsmem_addr(&s_peer[rank], threadIdx.x), amax);
+    cluster_sync();
+    amax = lane < (int)csize ? s_peer[lane] : 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (threadIdx.x == 0) s_amax = m;
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   }
-  cluster_arrive();
-  __syncthreads();                           // s_amax visible to the CTA
-  const float g = __fdiv_rn(s_amax, kGlobalDivisor);
+  const float g = __fdiv_rn(amax, kGlobalDivisor);
   if (rank == 0 && threadIdx.x == 0) *global = g;
 #pragma unroll
   for (int i = 0; i < NB; ++i) {
@@ -219,7 +219,6 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
       scales[b] = static_cast<uint8_t>(s);
     }
   }
-  cluster_wait();
 }
 
 // ---- multi-launch path for large tensors -----------------------------------
