@@ -472,7 +472,7 @@ def run_decode(args, world, rank):
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/step", "h2d_bytes_per_step": host_h.numel() * 4 + M * 4,
                 "d2h_bytes_per_step": 3 * M * 4},
         "clocks": clk.summary(),
-        "gpu_launches": (args.layers * 10 + 3) * args.steps,   # per layer: 2 norms, 4 quantizers, 4 GEMVs
+        "gpu_launches": (args.layers * 8 + 3) * args.steps,   # per layer: 2 norm+quantize, 2 quantizers, 4 GEMVs
     }
 
 

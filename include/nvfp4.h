@@ -210,6 +210,30 @@ nvfp4_status nvfp4_bf16_gemv(const uint16_t* x, int M, const uint16_t* w, int N,
 nvfp4_status nvfp4_rms_norm_bf16(const float* x, int rows, int K, int ld, float eps, uint16_t* out,
                                  cudaStream_t stream);
 
+/*
+ * nvfp4_rms_norm_bf16 followed by nvfp4_quantize_act, in one launch: the BF16
+ * rows r = BF16(x / sqrt((1/K) sum x^2 + eps)) are quantized by the recipe of
+ * nvfp4_quantize_act (one global scale over all rows) into codes [rows, K/2],
+ * scales [rows, K/16] and global_scale.  The decode step's normalization in
+ * front of the qkv and gate_up projections (see nvfp4_rms_norm_bf16).
+ * The row's sum of squares is FP32 in a fixed order (it may differ from
+ * nvfp4_rms_norm_bf16's order, so r may differ from that function's output by
+ * one BF16 rounding where the exact value is that close to a boundary); the
+ * codes are exactly nvfp4_quantize_act of r.  r_out, if not null, receives r
+ * ([rows, K] BF16, 16-byte aligned).
+ *   rows     0..8 (one CTA per row, the rows forming one thread-block cluster)
+ *   K        16..16384, multiple of 16;  ld >= K, multiple of 4 (floats)
+ *   eps      >= 0 (a zero row needs eps > 0)
+ *   x        device FP32, row r at x + r * ld, 16-byte aligned
+ *   codes    16-byte aligned; scales, global_scale 4-byte aligned (written)
+ * Errors: NVFP4_ERR_SHAPE (K, ld), NVFP4_ERR_RANGE (rows > 8, eps < 0 or NaN),
+ * NVFP4_ERR_NULL, NVFP4_ERR_ALIGN, NVFP4_ERR_CUDA (launch).  rows == 0 writes
+ * global_scale = 0.
+ */
+nvfp4_status nvfp4_rms_norm_quantize(const float* x, int rows, int K, int ld, float eps, uint8_t* codes,
+                                     uint8_t* scales, float* global_scale, uint16_t* r_out,
+                                     cudaStream_t stream);
+
 /* FP32 -> BF16 (RNE) elementwise cast of n values; x, y 16-byte aligned, n a multiple of 8. */
 nvfp4_status nvfp4_f32_to_bf16(const float* x, size_t n, uint16_t* y, cudaStream_t stream);
 

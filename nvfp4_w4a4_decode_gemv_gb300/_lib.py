@@ -43,6 +43,7 @@ SIGNATURES = {
     "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_bf16_gemv": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "nvfp4_rms_norm_bf16": (_c_i, [_c_p, _c_i, _c_i, _c_i, ctypes.c_float, _c_p, _c_p]),
+    "nvfp4_rms_norm_quantize": (_c_i, [_c_p, _c_i, _c_i, _c_i, ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "nvfp4_f32_to_bf16": (_c_i, [_c_p, _c_sz, _c_p, _c_p]),
     "reset_state_bytes": (_c_sz, [_c_i, _c_i]),
     "reset_state_init": (_c_i, [_c_p, _c_i, _c_i, _c_p]),

@@ -12,7 +12,8 @@ from ._lib import ResetParams, check, lib, ptr, stream_handle
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
-    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_rms_norm_bf16", "nvfp4_f32_to_bf16", "reset_state_bytes",
+    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
+    "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
     "NVFP4Tensor", "ResetSampler",
 ]
@@ -184,6 +185,25 @@ def nvfp4_rms_norm_bf16(x: torch.Tensor, K: int | None = None, eps: float = 1e-6
     out = out if out is not None else torch.empty((rows, K), dtype=torch.bfloat16, device=x.device)
     check(lib().nvfp4_rms_norm_bf16(ptr(x), rows, K, ld, float(eps), ptr(out), stream_handle(stream)),
           "nvfp4_rms_norm_bf16")
+    return out
+
+
+def nvfp4_rms_norm_quantize(x: torch.Tensor, K: int | None = None, eps: float = 1e-6, out: NVFP4Tensor | None = None,
+                            r_out: torch.Tensor | None = None, stream=None) -> NVFP4Tensor:
+    """FP32 rows (first K columns of a row-major [rows, ld] tensor) -> BF16 RMS-normalized -> NVFP4, one launch;
+    the BF16 rows also go to r_out when it is given."""
+    _need_cuda(x)
+    if x.dtype != torch.float32 or x.dim() != 2:
+        raise ValueError("x must be a 2-D float32 tensor")
+    rows, ld = x.shape
+    K = ld if K is None else K
+    if r_out is not None and (r_out.dtype != torch.bfloat16 or tuple(r_out.shape) != (rows, K)
+                              or not r_out.is_contiguous()):
+        raise ValueError("r_out must be a contiguous [rows, K] bfloat16 tensor")
+    out = out or NVFP4Tensor.empty(rows, K, x.device)
+    check(lib().nvfp4_rms_norm_quantize(ptr(x), rows, K, ld, float(eps), ptr(out.codes), ptr(out.scales),
+                                        ptr(out.global_scale), ptr(r_out), stream_handle(stream)),
+          "nvfp4_rms_norm_quantize")
     return out
 
 

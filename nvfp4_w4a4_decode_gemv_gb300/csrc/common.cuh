@@ -146,7 +146,11 @@ NVFP4_DEVINL unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) 
 NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 NVFP4_DEVINL void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Ask L2 for the line holding p (a hint: no effect on what a later load sees).
+// Ask L2 for the line holding p.  A hint, but not an invisible one: when the
+// line is rewritten afterwards (by a kernel still running while this one
+// waits on it), a later non-coherent load (ld.global.nc) on this SM was
+// measured to return the prefetched data.  Pair it with L2-coherent loads
+// (ld.global.cg) only.
 NVFP4_DEVINL void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }

@@ -31,6 +31,10 @@ constexpr float kGlobalDivisor = 2688.0f;   // 448 * 6
 
 // ---- element sources: block b of a [rows, K] tensor -> 16 floats ----------
 // Each source returns values that are exactly representable in BF16.
+// Loads are L2-only (ld.global.cg): the kernels ask L2 for their input before
+// waiting on the preceding kernel, which may still be writing it, and a
+// non-coherent load after the wait was measured to return pre-wait data in
+// that case; L2 is coherent.
 struct SrcBF16 {
   const uint16_t* x;
   int nbr;      // blocks per row = K / 16
@@ -39,7 +43,7 @@ struct SrcBF16 {
   __device__ void load(long b, float v[16]) const {
     const long r = b / nbr, c = b % nbr;
     const uint4* p = reinterpret_cast<const uint4*>(x + r * (long)K + c * 16);
-    const uint4 a = __ldg(p), d = __ldg(p + 1);
+    const uint4 a = __ldcg(p), d = __ldcg(p + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -63,7 +67,7 @@ struct SrcF32 {
     const float4* p = reinterpret_cast<const float4*>(x + r * ld + c * 16);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 q = __ldg(p + i);
+      const float4 q = __ldcg(p + i);
       v[4 * i] = round_bf16(q.x);
       v[4 * i + 1] = round_bf16(q.y);
       v[4 * i + 2] = round_bf16(q.z);
@@ -88,7 +92,7 @@ struct SrcSiluMul {
     const float4* pu = reinterpret_cast<const float4*>(gu + r * 2L * I + I + c * 16);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 g = __ldg(pg + i), u = __ldg(pu + i);
+      const float4 g = __ldcg(pg + i), u = __ldcg(pu + i);
       const float gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -218,6 +222,98 @@ __global__ void __launch_bounds__(kCThreads) quant_cluster_kernel(Src src, long 
       reinterpret_cast<uint2*>(codes)[b] = c;
       scales[b] = static_cast<uint8_t>(s);
     }
+  }
+}
+
+// ---- RMS normalization fused with the quantizer ----------------------------
+// One CTA per row, the call's rows forming one cluster.  Thread t of CTA r owns
+// block t of row r (16 FP32 values, kept in registers from the load to the
+// codes).  The row's sum of squares is reduced in the CTA (each thread's 16
+// squares in order, then a fixed shuffle tree), the normalized values are
+// rounded to BF16 exactly as nvfp4_rms_norm_bf16 rounds them
+// (BF16(x * (1 / sqrt(ss / K + eps))), IEEE division and square root), and
+// the tensor amax of those BF16 values goes through the cluster as in
+// quant_cluster_kernel.  The BF16 row can be written out as well.
+constexpr int kMaxNormQRows = 8;           // cluster size: portable
+constexpr int kMaxNormQThreads = 1024;     // K / 16 <= 1024
+
+__global__ void __launch_bounds__(kMaxNormQThreads) rms_norm_quant_kernel(const float* __restrict__ x, int K, long ld,
+                                                                          float eps, uint8_t* codes, uint8_t* scales,
+                                                                          float* global, uint16_t* r_out) {
+  __shared__ float s_ss[kMaxNormQThreads / 32];
+  __shared__ float s_mx[kMaxNormQThreads / 32];
+  __shared__ float s_peer[kMaxNormQRows];
+  const uint32_t row = cluster_ctarank();
+  const uint32_t csize = gridDim.x;          // the whole grid is one cluster
+  if (csize > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  griddep_launch_dependents();
+  const int nbr = K / 16;
+  const int t = threadIdx.x, lane = t & 31, nw = blockDim.x >> 5;
+  const bool live = t < nbr;
+  const float* xb = x + (long)row * ld + (long)t * 16;
+  if (live) prefetch_l2(xb);
+  griddep_wait();                            // the input comes from the preceding kernel
+
+  float v[16];
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(xb) + i);
+      v[4 * i] = q.x;
+      v[4 * i + 1] = q.y;
+      v[4 * i + 2] = q.z;
+      v[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = __fmaf_rn(v[i], v[i], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) s_ss[t >> 5] = ss;
+  __syncthreads();
+  float tot = lane < nw ? s_ss[lane] : 0.0f;   // every warp reduces the same values the same way
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float inv = __fdiv_rn(1.0f, sqrtf(__fadd_rn(__fdiv_rn(tot, (float)K), eps)));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = round_bf16(__fmul_rn(v[i], inv));
+  if (live && r_out) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = (__float_as_uint(v[2 * i]) >> 16) | (__float_as_uint(v[2 * i + 1]) & 0xFFFF0000u);
+    uint4* dst = reinterpret_cast<uint4*>(r_out + (long)row * K + (long)t * 16);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  const float bm = block_absmax(v);          // 0 for the padding threads
+  float amax = bm;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) s_mx[t >> 5] = amax;
+  __syncthreads();
+  amax = lane < nw ? s_mx[lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (csize > 1) {                           // as in quant_cluster_kernel
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (t < (int)csize) st_dsmem_f32(dsmem_addr(&s_peer[row], t), amax);
+    cluster_sync();
+    amax = lane < (int)csize ? s_peer[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  }
+  const float g = __fdiv_rn(amax, kGlobalDivisor);
+  if (row == 0 && t == 0) *global = g;
+  if (live) {
+    uint2 c;
+    const uint32_t sc = quant_block(v, bm, g, c);
+    const long b = (long)row * nbr + t;
+    reinterpret_cast<uint2*>(codes)[b] = c;
+    scales[b] = static_cast<uint8_t>(sc);
   }
 }
 
@@ -400,4 +496,36 @@ extern "C" nvfp4_status nvfp4_silu_mul_quantize(const float* gate_up, int rows, 
     return NVFP4_ERR_ALIGN;
   SrcSiluMul src{gate_up, I / 16, I};
   return nvfp4_internal_cuda_status(quantize_dispatch(src, nblocks, codes, scales, global_scale, stream));
+}
+
+extern "C" nvfp4_status nvfp4_rms_norm_quantize(const float* x, int rows, int K, int ld, float eps, uint8_t* codes,
+                                                uint8_t* scales, float* global_scale, uint16_t* r_out,
+                                                cudaStream_t stream) {
+  if (rows < 0 || K < 16 || (K % 16) != 0 || K / 16 > kMaxNormQThreads || ld < K || (ld % 4) != 0)
+    return NVFP4_ERR_SHAPE;
+  if (rows > kMaxNormQRows || !(eps >= 0.0f)) return NVFP4_ERR_RANGE;
+  if (!global_scale) return NVFP4_ERR_NULL;
+  if (rows > 0 && (!x || !codes || !scales)) return NVFP4_ERR_NULL;
+  if (!nvfp4_internal_aligned(x, 16) || !nvfp4_internal_aligned(codes, 16) || !nvfp4_internal_aligned(scales, 4) ||
+      !nvfp4_internal_aligned(global_scale, 4) || !nvfp4_internal_aligned(r_out, 16))
+    return NVFP4_ERR_ALIGN;
+  if (rows == 0) {
+    zero_global_kernel<<<1, 1, 0, stream>>>(global_scale);
+    return nvfp4_internal_cuda_status(cudaGetLastError());
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3((unsigned)(((K / 16) + 31) / 32 * 32));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)rows;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return nvfp4_internal_cuda_status(cudaLaunchKernelEx(&cfg, rms_norm_quant_kernel, x, K, (long)ld, eps, codes, scales,
+                                                       global_scale, r_out));
 }

@@ -3,12 +3,11 @@
 Per layer (the four NVFP4 projections of a Qwen3 decoder layer, ReSET project
 page "Core contribution"; reading note §6.1 setup):
 
-    r    = RMSNorm(h)                      nvfp4_rms_norm_bf16        FP32 -> BF16
-    xq   = NVFP4(r)                        nvfp4_quantize_act
+    xq   = NVFP4(BF16(RMSNorm(h)))         nvfp4_rms_norm_quantize    (one launch)
     qkv  = xq . Wqkv^T                     nvfp4_gemv_smallm_packed   FP32 [M, 10240]
     xo   = NVFP4(BF16(qkv[:, :8192]))      nvfp4_quantize_f32         (the query part; no attention)
     o    = xo . Wo^T                                                  FP32 [M, 5120]
-    r2   = RMSNorm(o),  xg = NVFP4(r2)
+    xg   = NVFP4(BF16(RMSNorm(o)))         nvfp4_rms_norm_quantize
     gu   = xg . Wgate_up^T                                            FP32 [M, 51200]
     xd   = NVFP4(BF16(SiLU(gate) * up))    nvfp4_silu_mul_quantize
     h    = xd . Wdown^T                                               FP32 [M, 5120] -> next layer
@@ -76,8 +75,7 @@ class DecodeStep:
     # ---- the chain ------------------------------------------------------------
     def _layer(self, layer: int, h_in: torch.Tensor, stream, trace):
         w = self.weights[layer]
-        api.nvfp4_rms_norm_bf16(h_in, eps=self.eps, out=self.r, stream=stream)
-        api.nvfp4_quantize_act(self.r, out=self.xq, stream=stream)
+        api.nvfp4_rms_norm_quantize(h_in, eps=self.eps, out=self.xq, r_out=self.r_out(trace), stream=stream)
         api.nvfp4_gemv_smallm_packed(self.xq, w["qkv"], y=self.y_qkv, workspace=self.ws, stream=stream)
         api.nvfp4_quantize_f32(self.y_qkv, K=self.k_o, out=self.xq_o, stream=stream)
         api.nvfp4_gemv_smallm_packed(self.xq_o, w["o"], y=self.y_o, workspace=self.ws, stream=stream)
@@ -85,8 +83,7 @@ class DecodeStep:
             nv = lambda t: (t.codes.clone(), t.scales.clone(), t.global_scale.clone())
             trace.append({"h_in": h_in.clone(), "r": self.r.clone(), "xq": nv(self.xq), "y_qkv": self.y_qkv.clone(),
                           "xq_o": nv(self.xq_o), "y_o": self.y_o.clone()})
-        api.nvfp4_rms_norm_bf16(self.y_o, eps=self.eps, out=self.r, stream=stream)
-        api.nvfp4_quantize_act(self.r, out=self.xq_gu, stream=stream)
+        api.nvfp4_rms_norm_quantize(self.y_o, eps=self.eps, out=self.xq_gu, r_out=self.r_out(trace), stream=stream)
         api.nvfp4_gemv_smallm_packed(self.xq_gu, w["gate_up"], y=self.y_gu, workspace=self.ws, stream=stream)
         api.nvfp4_silu_mul_quantize(self.y_gu, out=self.xq_d, stream=stream)
         api.nvfp4_gemv_smallm_packed(self.xq_d, w["down"], y=self.h, workspace=self.ws, stream=stream)
@@ -95,6 +92,11 @@ class DecodeStep:
                               "xq_d": (self.xq_d.codes.clone(), self.xq_d.scales.clone(),
                                        self.xq_d.global_scale.clone()),
                               "h_out": self.h.clone()})
+
+    def r_out(self, trace):
+        """Where the fused normalize+quantize launches put their BF16 rows: only
+        traced runs keep them (the projections read the NVFP4 codes)."""
+        return self.r if trace is not None else None
 
     def run(self, stream=None, trace=None):
         """Issue one decode step on `stream` (the current stream by default):

@@ -109,3 +109,17 @@ def test_reset_argument_errors(lib):
     assert norm(FAKE, 2, 8, 8, -1.0, FAKE, None) == 4                  # eps < 0
     assert norm(None, 2, 8, 8, 1e-6, FAKE, None) == 1
     assert norm(FAKE + 8, 2, 8, 8, 1e-6, FAKE, None) == 3
+
+
+def test_rms_norm_quantize_argument_errors(lib):
+    nq = lib.nvfp4_rms_norm_quantize
+    assert nq(FAKE, 2, 24, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 2          # K % 16
+    assert nq(FAKE, 2, 8, 8, 1e-6, FAKE, FAKE, FAKE, None, None) == 2            # K < 16
+    assert nq(FAKE, 2, 16400, 16400, 1e-6, FAKE, FAKE, FAKE, None, None) == 2    # K / 16 > 1024
+    assert nq(FAKE, 2, 32, 16, 1e-6, FAKE, FAKE, FAKE, None, None) == 2          # ld < K
+    assert nq(FAKE, 9, 32, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 4          # rows > 8
+    assert nq(FAKE, 2, 32, 32, -1.0, FAKE, FAKE, FAKE, None, None) == 4          # eps < 0
+    assert nq(FAKE, 2, 32, 32, 1e-6, FAKE, FAKE, None, None, None) == 1          # global
+    assert nq(None, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 1
+    assert nq(FAKE + 8, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 3      # x alignment
+    assert nq(FAKE, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, FAKE + 8, None) == 3      # r_out alignment

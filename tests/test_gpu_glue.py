@@ -82,3 +82,61 @@ def test_rms_norm_zero_row_and_eps():
     out = Q.bf16_bits_to_f32(bits(api.nvfp4_rms_norm_bf16(x.cuda(), eps=0.25)))
     assert np.all(out[0] == 0)
     assert np.all(out[1] == Q.bf16_bits_to_f32(D.to_bf16_bits(np.full(64, 2 / np.sqrt(4.25)))))
+
+
+def _rms_input(rows, K, ld):
+    g = torch.Generator().manual_seed(rows * K + 7)
+    x = torch.randn((rows, ld), generator=g) * 3.0
+    x[:, :: max(1, K // 50)] *= 20.0                                    # outlier columns
+    return x
+
+
+@pytest.mark.parametrize("rows,K,ld", [(1, 5120, 5120), (4, 5120, 5120), (8, 5120, 5120), (3, 16384, 16400),
+                                       (2, 16, 16), (5, 8192, 10240), (7, 4000, 4004)])
+def test_rms_norm_quantize(rows, K, ld):
+    """The fused launch: its BF16 rows pass the RMS-norm check, and its codes,
+    scales and global scale are exactly the quantizer's recipe on those rows."""
+    x = _rms_input(rows, K, ld)
+    r = torch.empty((rows, K), dtype=torch.bfloat16, device="cuda")
+    q = api.nvfp4_rms_norm_quantize(x.cuda(), K=K, eps=1e-6, r_out=r)
+    a = D.rms_norm(x[:, :K].numpy(), 1e-6)
+    mid = D.to_bf16_bits(a)
+    dec = _decisive(a, mid)
+    assert dec.mean() > 0.99
+    got = bits(r)
+    assert np.array_equal(got[dec], mid[dec])
+    nd = ~dec
+    lo = D.to_bf16_bits(a * (1 - 8 * 2.0 ** -24))[nd]
+    hi = D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24))[nd]
+    assert np.all((got[nd] == lo) | (got[nd] == hi))
+    rc, rs, rg = Q.quantize_bf16(got)
+    assert np.array_equal(to_np(q.codes), rc)
+    assert np.array_equal(to_np(q.scales), rs)
+    assert to_np(q.global_scale)[0] == rg
+    # without r_out: the same codes
+    q2 = api.nvfp4_rms_norm_quantize(x.cuda(), K=K, eps=1e-6)
+    assert torch.equal(q2.codes, q.codes) and torch.equal(q2.scales, q.scales)
+    assert torch.equal(q2.global_scale, q.global_scale)
+    assert api.device_status() == 0
+
+
+def test_rms_norm_quantize_matches_two_launches_where_rows_agree():
+    """Against nvfp4_rms_norm_bf16 + nvfp4_quantize_act: the BF16 rows agree
+    except where the exact value sits on a rounding boundary, and where they
+    agree everywhere the codes agree too."""
+    x = _rms_input(8, 5120, 5120).cuda()
+    r = torch.empty((8, 5120), dtype=torch.bfloat16, device="cuda")
+    q = api.nvfp4_rms_norm_quantize(x, eps=1e-6, r_out=r)
+    r2 = api.nvfp4_rms_norm_bf16(x, eps=1e-6)
+    same = bits(r) == bits(r2)
+    assert same.mean() > 0.999
+    if same.all():
+        q2 = api.nvfp4_quantize_act(r2)
+        assert torch.equal(q.codes, q2.codes) and torch.equal(q.scales, q2.scales)
+        assert torch.equal(q.global_scale, q2.global_scale)
+
+
+def test_rms_norm_quantize_zero_rows():
+    x = torch.empty((0, 64), device="cuda")
+    q = api.nvfp4_rms_norm_quantize(x)
+    assert to_np(q.global_scale)[0] == 0.0
