@@ -195,6 +195,26 @@ nvfp4_status nvfp4_bf16_gemv(const uint16_t* x, int M, const uint16_t* w, int N,
                              cudaStream_t stream);
 
 /*
+ * The same BF16 GEMV on the tensor cores (tcgen05 kind::f16, BF16 x BF16 ->
+ * FP32 accumulator in TMEM), on the NVFP4 GEMV's kernel: weight tiles of
+ * [128 rows x 64 K] streamed through a shared-memory ring by TMA, Stream-K
+ * split over the tiles' K chunks, the same deterministic fix-up.  It needs
+ * the records region of a GEMV workspace:
+ *   nvfp4_bf16_gemv_workspace_bytes(M, N, K): bytes of workspace needed (0 for
+ *   an invalid shape); any buffer that satisfies nvfp4_gemv_workspace_bytes
+ *   for the same M also satisfies it, so one zeroed workspace serves both.
+ *   x [M, K], w [N, K] BF16 row-major, y [M, N] FP32, all device, 16-byte
+ *   aligned; M 1..8, N 1 .. 2^20, K a positive multiple of 64; workspace
+ *   256-byte aligned, ZEROED ONCE before its first use, left ready for the
+ *   next call.  FP32 accumulation: within 1e-4 * sum_k |x_k w_k| + 1e-6 of
+ *   the exact product.  Errors as nvfp4_gemv_smallm.
+ */
+size_t nvfp4_bf16_gemv_workspace_bytes(int M, int N, int K);
+
+nvfp4_status nvfp4_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * RMS normalization of FP32 rows to BF16 (no gain):
  *   out[r, k] = BF16( x[r, k] / sqrt( (1/K) sum_k x[r, k]^2 + eps ) )
  * Row r of the input starts at x + r * ld (ld >= K, in floats); out is

@@ -42,6 +42,8 @@ SIGNATURES = {
     "nvfp4_pack_weights": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_sz, _c_p]),
     "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_bf16_gemv": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p]),
+    "nvfp4_bf16_gemv_workspace_bytes": (ctypes.c_size_t, [_c_i, _c_i, _c_i]),
+    "nvfp4_bf16_gemv_tc": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p, ctypes.c_size_t, _c_p]),
     "nvfp4_rms_norm_bf16": (_c_i, [_c_p, _c_i, _c_i, _c_i, ctypes.c_float, _c_p, _c_p]),
     "nvfp4_rms_norm_quantize": (_c_i, [_c_p, _c_i, _c_i, _c_i, ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "nvfp4_f32_to_bf16": (_c_i, [_c_p, _c_sz, _c_p, _c_p]),

@@ -12,7 +12,8 @@ from ._lib import ResetParams, check, lib, ptr, stream_handle
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
-    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
+    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
+    "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
     "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
     "NVFP4Tensor", "ResetSampler",
@@ -171,6 +172,25 @@ def nvfp4_bf16_gemv(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = N
     N = w.shape[0]
     y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
     check(lib().nvfp4_bf16_gemv(ptr(x), M, ptr(w), N, K, ptr(y), stream_handle(stream)), "nvfp4_bf16_gemv")
+    return y
+
+
+def nvfp4_bf16_gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_bf16_gemv_workspace_bytes(M, N, K))
+
+
+def nvfp4_bf16_gemv_tc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ w[N, K]^T for BF16 x, w on the tensor cores; FP32 result.  `workspace`: a zeroed
+    uint8 device tensor of at least nvfp4_bf16_gemv_workspace_bytes(M, N, K) bytes (a GEMV workspace serves)."""
+    _need_cuda(x, w)
+    M, K = x.shape
+    N = w.shape[0]
+    y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if workspace is None:            # the per-device GEMV workspace (its records region is what this call uses)
+        workspace = _ws_for(x.device).get(M, N, 256)
+    check(lib().nvfp4_bf16_gemv_tc(ptr(x), M, ptr(w), N, K, ptr(y), ptr(workspace), workspace.numel(),
+                                   stream_handle(stream)), "nvfp4_bf16_gemv_tc")
     return y
 
 

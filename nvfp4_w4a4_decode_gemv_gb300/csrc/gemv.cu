@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(256) xrec_kernel(const uint8_t* __restrict__ x
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M * nb) return;
   const int m = i / nb, b = i % nb;
-  const uint2 cw = __ldg(reinterpret_cast<const uint2*>(xq + (size_t)m * (K / 2)) + b);
-  const uint32_t s = __ldg(xs + (size_t)m * nb + b);
+  // L2-coherent loads: the codes come from the preceding kernel (see prefetch_l2).
+  const uint2 cw = __ldcg(reinterpret_cast<const uint2*>(xq + (size_t)m * (K / 2)) + b);
+  const uint32_t s = __ldcg(xs + (size_t)m * nb + b);
   uint32_t words[4] = {0u, 0u, 0u, 0u};
   int sum = 0;
 #pragma unroll
@@ -202,7 +203,7 @@ NVFP4_DEVINL void flush_tile(const GemvArgs& a, int tile, long long first_unit_o
   const long long C = a.C;
   const long long first = cta_of_unit((long long)tile * C, a.U, G);
   const long long last = cta_of_unit((long long)tile * C + C - 1, a.U, G);
-  const float yscale = __fmul_rn(__fmul_rn(__ldg(a.xg), __ldg(a.wg)), 1152921504606846976.0f /* 2^60 */);
+  const float yscale = __fmul_rn(__fmul_rn(__ldcg(a.xg), __ldcg(a.wg)), 1152921504606846976.0f /* 2^60 */);
   const int row0 = tile * TR + warp * 32 * R;
   if (first == last) {
 #pragma unroll
@@ -484,6 +485,8 @@ int env_int(const char* name, int dflt) {
 nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
 bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
+cudaError_t nvfp4_internal_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
+                                        unsigned int* records, cudaStream_t stream);
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
                                    unsigned int* records, int grid_cap, int max_ctas_per_sm, cudaStream_t stream);
@@ -612,4 +615,29 @@ extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_
   return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
       xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
       env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
+}
+
+// BF16 GEMV on the tensor-core kernel: it needs only the records region of a
+// GEMV workspace (counters and records are at fixed places, so one workspace
+// serves both kinds of call).
+extern "C" size_t nvfp4_bf16_gemv_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < 64 || (K % 64) != 0) return 0;
+  return ws_layout(M, N, kChunk).xrec;
+}
+
+extern "C" nvfp4_status nvfp4_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
+                                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !w || !y || !workspace) return NVFP4_ERR_NULL;
+  if (M < 1 || M > kMaxM) return NVFP4_ERR_RANGE;
+  if (N < 1 || N > kMaxN || K < 64 || (K % 64) != 0) return NVFP4_ERR_SHAPE;
+  if (!nvfp4_internal_aligned(x, 16) || !nvfp4_internal_aligned(w, 16) || !nvfp4_internal_aligned(y, 16) ||
+      !nvfp4_internal_aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  const WsLayout wl = ws_layout(M, N, kChunk);
+  if (workspace_bytes < wl.xrec) return NVFP4_ERR_SHAPE;
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  return nvfp4_internal_cuda_status(
+      nvfp4_internal_bf16_gemv_tc(x, M, w, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec), stream));
 }

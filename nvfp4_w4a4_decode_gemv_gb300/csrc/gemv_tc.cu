@@ -70,6 +70,13 @@ constexpr uint32_t kColSF = 48;             // stage s: A scales at 48+32s+[0,16
 // Instruction descriptor: E2M1 x E2M1 (format 1), UE4M3 scales, K-major A and B,
 // N = 16 (bits 17-22: N >> 3), M = 128 (bits 24-28: M >> 4), dense.
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
+// BF16 operands (the lm_head variant, kind::f16): FP32 accumulator (bits 4-5 =
+// 1), A and B both BF16 (bits 7-9 and 10-12 = 1), K-major, same N and M.
+// A unit is [128 rows x 64 K] of BF16: 128 bytes per row, the same byte
+// layout as an E2M1 unit, and the same 32-byte step per MMA (K = 16).
+constexpr uint32_t kIdescBF16 =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
+constexpr uint32_t kStageTxBF16 = kCodeBytes + kActCodeBytes;
 
 struct TcArgs {
   const uint8_t* wpacked;        // packed weights, or null: weights through the two tensor maps
@@ -89,6 +96,14 @@ NVFP4_DEVINL uint64_t smem_desc_sw128(uint32_t saddr) {
 
 NVFP4_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 NVFP4_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+NVFP4_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(da), "l"(db), "r"(kIdescBF16), "r"(acc)
+      : "memory");
+}
 
 NVFP4_DEVINL void mma_mxf4nvf4(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
@@ -149,9 +164,10 @@ NVFP4_DEVINL Split split_of(const TcArgs& a, int tile, long long G) {
   return sp;
 }
 
-template <int M>
+template <int M, bool BF>
 NVFP4_DEVINL void store_y(const TcArgs& a, int tile, int row, const float (&v)[kNT]) {
-  const float yscale = __fmul_rn(__ldg(a.xg), __ldg(a.wg));
+  // L2-coherent loads: xg comes from the preceding kernel (see prefetch_l2).
+  const float yscale = BF ? 1.0f : __fmul_rn(__ldcg(a.xg), __ldcg(a.wg));
   const int n = tile * kTR + row;
   if (n < a.N) {
 #pragma unroll
@@ -229,7 +245,7 @@ NVFP4_DEVINL void read_acc(uint32_t tmem, int quad, int d, uint64_t* acc_empty_d
   for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
 }
 
-template <int M, int S>
+template <int M, int S, bool BF>
 __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                               const __grid_constant__ CUtensorMap tm_scales,
                                                               const __grid_constant__ CUtensorMap tm_xcodes,
@@ -280,12 +296,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0 && nunits > 0) {
+      constexpr uint32_t tx = BF ? kStageTxBF16 : kStageTx;
       if (!a.wpacked) {
         prefetch_tmap(&tm_codes);
-        prefetch_tmap(&tm_scales);
+        if (!BF) prefetch_tmap(&tm_scales);
       }
       prefetch_tmap(&tm_xcodes);
-      prefetch_tmap(&tm_xscales);
+      if (!BF) prefetch_tmap(&tm_xscales);
       const int pre = nunits < S ? nunits : S;
       const uint8_t* wp = a.wpacked ? a.wpacked + (size_t)u0 * kPackedBlock : nullptr;
       // Weight tiles do not depend on the preceding kernel: issue the first
@@ -294,12 +311,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         int tile = tile0, c = chunk0;
         for (int k = 0; k < pre; ++k) {
           uint8_t* slot = smem + k * kSlot;
-          mbar_arrive_expect_tx(&full[k], kStageTx);
+          mbar_arrive_expect_tx(&full[k], tx);
           if (wp) {
             bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[k]);
           } else {
             tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[k]);
-            tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
+            if (!BF) tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[k]);
           }
           if (++c == C) { c = 0; ++tile; }
         }
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       for (int k = 0; k < pre; ++k) {
         uint8_t* slot = smem + k * kSlot;
         tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[k]);      // rows >= M arrive as zeros
-        tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
+        if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
         if (++c == C) { c = 0; ++tile; }
       }
       int issued = pre;
@@ -318,15 +335,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       for (int k = pre; k < nunits; ++k) {
         if (!mbar_wait(&empty[s], phase ^ 1u)) break;   // the slot's previous use has been consumed
         uint8_t* slot = smem + s * kSlot;
-        mbar_arrive_expect_tx(&full[s], kStageTx);
+        mbar_arrive_expect_tx(&full[s], tx);
         if (wp) {
           bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[s]);
         } else {
           tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[s]);
-          tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
+          if (!BF) tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
         }
         tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[s]);
-        tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
+        if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
         issued = k + 1;
         if (++c == C) { c = 0; ++tile; }
         if (++s == S) { s = 0; phase ^= 1u; }
@@ -364,15 +381,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         }
         // The scale writers arrive on sf_ready only after they have seen the
         // slot full, so sf_ready also orders the slot's data before the MMAs.
-        if (!mbar_wait(&sf_ready[s], phase)) break;
+        // BF16 has no scales: the MMA waits for the slot itself.
+        if (!mbar_wait(BF ? &full[s] : &sf_ready[s], phase)) break;
         tc_fence_after();
         const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
         const uint32_t sfa = tmem + kColSF + 32u * s;
         const uint32_t sfb = sfa + 16u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, sfa + 4u * q, sfb + 4u * q,
-                       (first_of_tile && q == 0) ? 0u : 1u);
+          if (BF)
+            mma_bf16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, (first_of_tile && q == 0) ? 0u : 1u);
+          else
+            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, sfa + 4u * q, sfb + 4u * q,
+                         (first_of_tile && q == 0) ? 0u : 1u);
         }
         mma_commit(&empty[s]);
         issued = k + 1;
@@ -392,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     const uint32_t tb0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 16u;
     int s = 0;
     uint32_t phase = 0;
-    for (int k = 0; k < nunits; ++k) {
+    for (int k = 0; k < (BF ? 0 : nunits); ++k) {     // BF16 has no scales to place
       if (!mbar_wait_warp(&full[s], phase)) break;
       const uint8_t* slot = smem + s * kSlot;
       const uint4 sa = *reinterpret_cast<const uint4*>(slot + kOffSA + row * 16);
@@ -431,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         float acc[kNT];
         read_acc(tmem, quad, 2, nullptr, acc);
         if (sp.whole) {
-          store_y<M>(a, tile_last, row, acc);
+          store_y<M, BF>(a, tile_last, row, acc);
         } else if (fin) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -449,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
                 for (int m = 0; m < M; ++m) acc[m] += v[i][m];
               }
           }
-          store_y<M>(a, tile_last, row, acc);
+          store_y<M, BF>(a, tile_last, row, acc);
         } else {
           publish_record<M>(a, row, acc);
         }
@@ -472,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       if (tile == tile0 && u0 > (long long)tile0 * C) {
         publish_record<M>(a, quad * 32 + lane, acc);
       } else {
-        store_y<M>(a, tile, quad * 32 + lane, acc);
+        store_y<M, BF>(a, tile, quad * 32 + lane, acc);
       }
     }
   }
@@ -507,11 +528,11 @@ struct TcMaps {
   CUtensorMap w_codes, w_scales, x_codes, x_scales;
 };
 
-template <int M, int S>
+template <int M, int S, bool BF = false>
 static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm) {
   static int per_sm_fit = -1;
   constexpr size_t smem = tc_smem_bytes<S>();
-  auto kern = gemv_tc_kernel<M, S>;
+  auto kern = gemv_tc_kernel<M, S, BF>;
   if (per_sm_fit < 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -599,6 +620,40 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
     case 6: return launch_tc_m<6>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     case 7: return launch_tc_m<7>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     default: return launch_tc_m<8>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+  }
+}
+
+// BF16 y[M, N] = x[M, K] . w[N, K]^T on the same kernel (operands of kind::f16,
+// no scales, units of [128 rows x 64 K]); the caller has validated the
+// arguments (K a multiple of 64).
+cudaError_t nvfp4_internal_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t* w, int N, int K, float* y,
+                                        unsigned int* records, cudaStream_t stream) {
+  TcMaps mp;
+  memset(&mp, 0, sizeof(mp));   // no scale maps
+  if (!nvfp4_internal_encode_2d(&mp.w_codes, w, (uint64_t)K * 2, (uint64_t)N, 128, kTR, true) ||
+      !nvfp4_internal_encode_2d(&mp.x_codes, x, (uint64_t)K * 2, (uint64_t)M, 128, kNT, true))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.wpacked = nullptr;
+  a.xg = nullptr;
+  a.wg = nullptr;
+  a.y = y;
+  a.records = records;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.C = K / 64;
+  a.RT = (N + kTR - 1) / kTR;
+  a.U = (long long)a.RT * a.C;
+  switch (M) {
+    case 1: return launch_tc<1, 4, true>(mp, a, stream, 0, 2);
+    case 2: return launch_tc<2, 4, true>(mp, a, stream, 0, 2);
+    case 3: return launch_tc<3, 4, true>(mp, a, stream, 0, 2);
+    case 4: return launch_tc<4, 4, true>(mp, a, stream, 0, 2);
+    case 5: return launch_tc<5, 4, true>(mp, a, stream, 0, 2);
+    case 6: return launch_tc<6, 4, true>(mp, a, stream, 0, 2);
+    case 7: return launch_tc<7, 4, true>(mp, a, stream, 0, 2);
+    default: return launch_tc<8, 4, true>(mp, a, stream, 0, 2);
   }
 }
 

@@ -12,7 +12,7 @@ page "Core contribution"; reading note §6.1 setup):
     xd   = NVFP4(BF16(SiLU(gate) * up))    nvfp4_silu_mul_quantize
     h    = xd . Wdown^T                                               FP32 [M, 5120] -> next layer
 
-then logits = BF16(RMSNorm(h)) . Wlm^T (nvfp4_bf16_gemv) and the ReSET sampler
+then logits = BF16(RMSNorm(h)) . Wlm^T (nvfp4_bf16_gemv_tc) and the ReSET sampler
 (reset_sample).  Weights are random (N(0, 0.02) in BF16, quantized and packed
 once); the step is issued on one stream and can be captured as one CUDA graph.
 Every computation runs in the library's kernels; this module only orders the
@@ -107,7 +107,7 @@ class DecodeStep:
             self._layer(layer, h_in, stream, trace)
             h_in = self.h
         api.nvfp4_rms_norm_bf16(self.h, eps=self.eps, out=self.r, stream=stream)
-        api.nvfp4_bf16_gemv(self.r, self.lm_head, y=self.logits, stream=stream)
+        api.nvfp4_bf16_gemv_tc(self.r, self.lm_head, y=self.logits, workspace=self.ws, stream=stream)
         if trace is not None:
             trace.append({"h_final": self.h.clone(), "r_final": self.r.clone(), "logits": self.logits.clone()})
         return self.sampler(self.logits, self.step_start, self.u, stream=stream)

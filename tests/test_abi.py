@@ -123,3 +123,20 @@ def test_rms_norm_quantize_argument_errors(lib):
     assert nq(None, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 1
     assert nq(FAKE + 8, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, None, None) == 3      # x alignment
     assert nq(FAKE, 2, 32, 32, 1e-6, FAKE, FAKE, FAKE, FAKE + 8, None) == 3      # r_out alignment
+
+
+def test_bf16_gemv_tc_argument_errors(lib):
+    g = lib.nvfp4_bf16_gemv_tc
+    need = lib.nvfp4_bf16_gemv_workspace_bytes(8, 1000, 5120)
+    assert need > 0
+    assert lib.nvfp4_bf16_gemv_workspace_bytes(8, 1000, 100) == 0            # K % 64
+    assert lib.nvfp4_bf16_gemv_workspace_bytes(9, 1000, 128) == 0            # M > 8
+    assert need <= lib.nvfp4_gemv_workspace_bytes(8, 1000, 5120)             # a GEMV workspace serves
+    assert g(FAKE, 9, FAKE, 10, 64, FAKE, FAKE, need, None) == 4             # M > 8
+    assert g(FAKE, 1, FAKE, 10, 96, FAKE, FAKE, need, None) == 2             # K % 64
+    assert g(FAKE, 1, FAKE, 0, 64, FAKE, FAKE, need, None) == 2              # N < 1
+    assert g(FAKE, 1, FAKE, 10, 64, FAKE, FAKE, 16, None) == 2               # workspace too small
+    assert g(None, 1, FAKE, 10, 64, FAKE, FAKE, need, None) == 1
+    assert g(FAKE, 1, FAKE, 10, 64, FAKE, None, need, None) == 1
+    assert g(FAKE + 8, 1, FAKE, 10, 64, FAKE, FAKE, need, None) == 3         # x alignment
+    assert g(FAKE, 1, FAKE, 10, 64, FAKE, FAKE + 16, need, None) == 3        # workspace alignment

@@ -140,3 +140,57 @@ def test_rms_norm_quantize_zero_rows():
     x = torch.empty((0, 64), device="cuda")
     q = api.nvfp4_rms_norm_quantize(x)
     assert to_np(q.global_scale)[0] == 0.0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 512), (4, 4096, 5120), (8, 333, 6400), (3, 8, 64), (8, 129, 25600),
+                                   (2, 70000, 128), (5, 1, 8192)])
+def test_bf16_gemv_tc(M, N, K):
+    """The tensor-core BF16 GEMV against the FP64 oracle (several tiles, a
+    ragged last tile, K down to one chunk), bit-identical on repeat calls."""
+    x = synth.activations(M, K, seed=M + N + 1)
+    w = synth.weights(N, K, seed=K + 1)
+    xd, wd = x.cuda(), w.cuda()
+    ws = torch.zeros(api.nvfp4_bf16_gemv_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    y = api.nvfp4_bf16_gemv_tc(xd, wd, workspace=ws)
+    ref, scale = D.bf16_gemv(bits(x), bits(w))
+    assert_within(to_np(y), ref, scale, rel=1e-4)
+    y2 = api.nvfp4_bf16_gemv_tc(xd, wd, workspace=ws)
+    assert torch.equal(y, y2)
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_bf16_gemv_tc_lm_head_sampled_rows(M):
+    """The decode step's lm_head (5120 -> 151936): all logits on the GPU, 64
+    sampled vocabulary rows (and the last) checked by the oracle; the
+    CUDA-core path agrees within the same bound."""
+    K, V = 5120, synth.LM_HEAD_VOCAB
+    x = synth.activations(M, K, seed=15, outliers=False)
+    w = synth.weights(V, K, seed=16)
+    xd, wd = x.cuda(), w.cuda()
+    y = to_np(api.nvfp4_bf16_gemv_tc(xd, wd))
+    rows = np.concatenate([np.random.default_rng(2).choice(V, 64, replace=False), [V - 1]])
+    ref, scale = D.bf16_gemv(bits(x), bits(w[rows]))
+    assert_within(y[:, rows], ref, scale, rel=1e-4)
+    ycc = to_np(api.nvfp4_bf16_gemv(xd, wd))
+    full_scale = np.abs(to_np(xd.float())) @ np.abs(to_np(wd.float())).T
+    assert np.all(np.abs(y - ycc) <= 2e-4 * full_scale + 2e-6)
+
+
+def test_bf16_gemv_tc_shares_the_gemv_workspace():
+    """BF16 and NVFP4 GEMV calls of different shapes back to back on one
+    workspace: each still matches its own fresh-workspace result."""
+    shapes = [(8, 5120, 10240), (1, 5120, 2048)]
+    ws = torch.zeros(max(api.nvfp4_gemv_workspace_bytes(M, N, K) for M, K, N in shapes), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for M, K, N in shapes:
+        x = synth.activations(M, K, seed=N).cuda()
+        w = synth.weights(N, K, seed=K).cuda()
+        wq = api.nvfp4_quantize_act(w)
+        xq = api.nvfp4_quantize_act(x)
+        outs.append((api.nvfp4_bf16_gemv_tc(x, w, workspace=ws), api.nvfp4_gemv_smallm(xq, wq, workspace=ws),
+                     api.nvfp4_bf16_gemv_tc(x, w), api.nvfp4_gemv_smallm(xq, wq)))
+    for a, b, c, d in outs:
+        assert torch.equal(a, c) and torch.equal(b, d)
+    assert api.device_status() == 0
