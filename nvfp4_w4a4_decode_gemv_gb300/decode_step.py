@@ -106,10 +106,10 @@ class DecodeStep:
         for layer in range(self.layers):
             self._layer(layer, h_in, stream, trace)
             h_in = self.h
-        api.nvfp4_rms_norm_bf16(self.h, eps=self.eps, out=self.r, stream=stream)
+        api.nvfp4_rms_norm_bf16(h_in, eps=self.eps, out=self.r, stream=stream)   # the last layer's output
         api.nvfp4_bf16_gemv_tc(self.r, self.lm_head, y=self.logits, workspace=self.ws, stream=stream)
         if trace is not None:
-            trace.append({"h_final": self.h.clone(), "r_final": self.r.clone(), "logits": self.logits.clone()})
+            trace.append({"h_final": h_in.clone(), "r_final": self.r.clone(), "logits": self.logits.clone()})
         return self.sampler(self.logits, self.step_start, self.u, stream=stream)
 
     def capture(self):
