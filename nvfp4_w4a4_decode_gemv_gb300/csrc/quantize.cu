@@ -121,27 +121,34 @@ NVFP4_DEVINL uint32_t quant_block(const float v[16], float bm, float g, uint2& c
   // (IEEE reciprocal) unless an E2M1 decision point (0.25, 0.75, ..., 5) lies
   // within the few ulps that separate p from v: |p - v| < 1.5 * 2^-23 |v|.  So
   // when the codes of p (1 - 2^-20) and p (1 + 2^-20) agree, every value in
-  // between -- v among them -- has that code; otherwise divide.
-  const float r = (S > 0.0f) ? __frcp_rn(S) : 0.0f;
-  const bool fast = r > 0.0f && r < 1.0e38f;
+  // between -- v among them -- has that code; otherwise divide.  All eight
+  // pairs take the multiply path first, without branches, so that they
+  // overlap; the divisions run only for the pairs (if any) left undecided.
+  const float r = __frcp_rn(S);                 // +inf when S == 0 (codes are then sign-only)
+  const bool fast = S > 0.0f && r < 1.0e38f;
   constexpr float kLo = 1.0f - 0x1.0p-20f, kHi = 1.0f + 0x1.0p-20f;
+  uint32_t q[8];
+  uint32_t undecided = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float pl = __fmul_rn(v[2 * i], r), ph = __fmul_rn(v[2 * i + 1], r);
+    const uint32_t qa = f32x2_to_e2m1x2(__fmul_rn(ph, kLo), __fmul_rn(pl, kLo));
+    const uint32_t qb = f32x2_to_e2m1x2(__fmul_rn(ph, kHi), __fmul_rn(pl, kHi));
+    q[i] = qa;
+    undecided |= (qa != qb ? 1u : 0u) << i;
+  }
+  if (!fast) undecided = (S > 0.0f) ? 0xFFu : 0u;
+  if (undecided) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((undecided >> i) & 1u) q[i] = f32x2_to_e2m1x2(__fdiv_rn(v[2 * i + 1], S), __fdiv_rn(v[2 * i], S));
+  }
   uint32_t packed[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float lo = v[2 * i], hi = v[2 * i + 1];
-    const uint32_t sgn = ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
-    uint32_t byte = sgn;
-    if (S > 0.0f) {
-      uint32_t q = 0x100u;           // no code yet
-      if (fast) {
-        const float pl = __fmul_rn(lo, r), ph = __fmul_rn(hi, r);
-        const uint32_t qa = f32x2_to_e2m1x2(__fmul_rn(ph, kLo), __fmul_rn(pl, kLo));
-        const uint32_t qb = f32x2_to_e2m1x2(__fmul_rn(ph, kHi), __fmul_rn(pl, kHi));
-        if (qa == qb) q = qa;
-      }
-      if (q == 0x100u) q = f32x2_to_e2m1x2(__fdiv_rn(hi, S), __fdiv_rn(lo, S));
-      byte = (q & 0x77u) | sgn;       // magnitude from the conversion, sign from x
-    }
+    const uint32_t sgn = ((__float_as_uint(v[2 * i]) >> 31) << 3) | ((__float_as_uint(v[2 * i + 1]) >> 31) << 7);
+    // magnitude from the conversion, sign from x; S == 0: the sign alone
+    const uint32_t byte = (S > 0.0f) ? ((q[i] & 0x77u) | sgn) : sgn;
     packed[i >> 2] |= byte << (8 * (i & 3));
   }
   codes = make_uint2(packed[0], packed[1]);
