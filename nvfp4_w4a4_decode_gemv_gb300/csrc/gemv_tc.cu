@@ -164,10 +164,16 @@ NVFP4_DEVINL Split split_of(const TcArgs& a, int tile, long long G) {
   return sp;
 }
 
-template <int M, bool BF>
-NVFP4_DEVINL void store_y(const TcArgs& a, int tile, int row, const float (&v)[kNT]) {
-  // L2-coherent loads: xg comes from the preceding kernel (see prefetch_l2).
-  const float yscale = BF ? 1.0f : __fmul_rn(__ldcg(a.xg), __ldcg(a.wg));
+// The output scale xg * wg (1 for BF16).  Read once per thread right after the
+// dependency wait, off the critical path of the tile ends; L2-coherent loads,
+// as xg comes from the preceding kernel (see prefetch_l2).
+template <bool BF>
+NVFP4_DEVINL float output_scale(const TcArgs& a) {
+  return BF ? 1.0f : __fmul_rn(__ldcg(a.xg), __ldcg(a.wg));
+}
+
+template <int M>
+NVFP4_DEVINL void store_y(const TcArgs& a, float yscale, int tile, int row, const float (&v)[kNT]) {
   const int n = tile * kTR + row;
   if (n < a.N) {
 #pragma unroll
@@ -407,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     }
   } else if (warp < 6) {
     // ---------------- scale writers: rows 32*quad .. 32*quad + 31 ----------------
+    // Their first slot holds token scales of the preceding kernel anyway, so
+    // waiting on that kernel here costs nothing, and the output scale's load
+    // overlaps the whole stream.
+    griddep_wait();
+    const float yscale = output_scale<BF>(a);
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t ta0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + (uint32_t)quad;
@@ -440,7 +451,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     // The CTA's last tile is flushed here, by warps that are idle once the
     // scales are written, so it does not wait behind the earlier tiles' flushes.
     if (nunits > 0) {
-      griddep_wait();
       const int tile_last = (int)((u1 - 1) / C);
       const int row = quad * 32 + lane;
       const Split sp = split_of(a, tile_last, G);
@@ -452,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         float acc[kNT];
         read_acc(tmem, quad, 2, nullptr, acc);
         if (sp.whole) {
-          store_y<M, BF>(a, tile_last, row, acc);
+          store_y<M>(a, yscale, tile_last, row, acc);
         } else if (fin) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
                 for (int m = 0; m < M; ++m) acc[m] += v[i][m];
               }
           }
-          store_y<M, BF>(a, tile_last, row, acc);
+          store_y<M>(a, yscale, tile_last, row, acc);
         } else {
           publish_record<M>(a, row, acc);
         }
@@ -480,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
     griddep_wait();            // y and the records belong to the preceding kernel's era
+    const float yscale = output_scale<BF>(a);
     // Every tile but the CTA's last (that one is flushed by the scale writers).
     const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
     for (int tile = tile0, tile_idx = 0; tile < tile_last; ++tile, ++tile_idx) {
@@ -493,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       if (tile == tile0 && u0 > (long long)tile0 * C) {
         publish_record<M>(a, quad * 32 + lane, acc);
       } else {
-        store_y<M, BF>(a, tile, quad * 32 + lane, acc);
+        store_y<M>(a, yscale, tile, quad * 32 + lane, acc);
       }
     }
   }
