@@ -152,29 +152,40 @@ class ClockSampler:
 
 
 def dist_setup(args):
+    """One process per GPU (replicas: the path does not shard, so ranks share
+    nothing but the barrier and the max of their timings).  NCCL on GPUs; gloo
+    where there is no GPU (the host-side logic is tested that way)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    gpu = torch.cuda.is_available()
+    if gpu:
+        torch.cuda.set_device(local if world > 1 else 0)
     if world > 1:
-        torch.cuda.set_device(local)
-        torch.distributed.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
+        torch.distributed.init_process_group("nccl" if gpu else "gloo")
     return world, rank
 
 
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(world, v):
     if world == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbs(world, bytes_per_step, steps, ms_max):
+    """Whole-job throughput of `world` replicas that each moved bytes_per_step
+    per step, over the slowest rank's time."""
+    return world * bytes_per_step * steps / (ms_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -288,7 +299,7 @@ def run_ours(args, world, rank):
     per_call = cold_per_call(calls, weights, ws, reps=3)
 
     step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
-    value_gbs = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    value_gbs = aggregate_gbs(world, step_bytes, args.steps, ms_total)
     gemv_bytes_total = sum(c["gemv_bytes"] for c in calls)
     per_m = {f"M{M}": {"gemv_us_per_call": round(gemv_ms[M] * 1e3 / len(groups[M]), 2),
                        "gemv_gbs": round(sum(c["gemv_bytes"] for c in groups[M]) / (gemv_ms[M] * 1e-3) / 1e9, 1)}
