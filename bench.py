@@ -47,8 +47,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "cb40fb2d2d9b2cfb4252fb7115b72b225d2e9ccd522ef6055cfebbea8f935d7c",
-                  "workload": "qwen3-32b", "bytes_per_launch": 68993148}
+                  "sha256": "ff7ce167721dc2fd82f98249a3318f31c520e7e60c302f68a636a2c0787d0cc9",
+                  "workload": "qwen3-32b", "bytes_per_launch": 68984786}
 
 
 def recorded_traffic(workload):
