@@ -37,6 +37,11 @@
 //                   write y, or partial sums for the Stream-K fix-up
 // Work split as in gemv.cu (Stream-K over [tile x 256-K] units); a split tile
 // is finished by its first contributor (see the fix-up section below).
+//
+// The same kernel, instantiated with BF = true, is the BF16 GEMV of the
+// lm_head (nvfp4_bf16_gemv_tc): `tcgen05.mma ... kind::f16` on BF16 operands,
+// units of [128 rows x 64 K] (the same 128 bytes per row as an E2M1 unit, so
+// the same swizzle, descriptor steps and ring), no scales and no output scale.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>

@@ -8,12 +8,17 @@
 // __fmul_rn: no contraction, no approximate reciprocal), so codes and scales
 // are bit-identical to a plain FP32 evaluation of the recipe:
 //   g = amax / 2688;  s = E4M3(bm / (6 g));  code = E2M1(x / (dec(s) g)).
+// The element codes come from x times the IEEE reciprocal of the scale where
+// that provably gives the quotient's code (see quant_block), else from the
+// IEEE quotient itself.
 //
 // Two launch shapes:
-//  * activations (<= 16384 blocks of 16): ONE launch of a thread-block cluster;
-//    every CTA keeps its blocks in registers, the tensor amax is reduced across
-//    the cluster through distributed shared memory, then codes are written
-//    without a second read of x.
+//  * activations (up to 8 blocks of 16 per thread of one cluster of up to 16
+//    CTAs x 512 threads): ONE launch of a thread-block cluster; every CTA
+//    keeps its blocks in registers, the tensor amax is reduced across the
+//    cluster through distributed shared memory, then codes are written
+//    without a second read of x.  rms_norm_quant_kernel is the same pattern
+//    with the decode step's RMS normalization in front (one CTA per row).
 //  * larger tensors (offline weight quantization): amax kernel (atomicMax on
 //    the float bits, which order like the values for non-negative floats, into
 //    the global-scale slot), a grid-stride quantize kernel that reads that amax,
