@@ -413,6 +413,40 @@ def run_e2e(args, calls, weights, ws):
             "d2h_bytes_per_step": int(host_y.numel() * host_y.element_size())}
 
 
+def decode_stage_times(st, stream, reps=20):
+    """Per-launch time of the decode step's non-projection stages, each launched
+    `reps` times back to back (with programmatic dependent launch between
+    them, as in the step) between two events on the step's stream.  Inputs are
+    the step's own buffers, so these are L2-warm figures; the weight-streaming
+    projections are measured by the sweep."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    M = st.M
+    calls = {
+        "rms_norm_quantize": lambda: api.nvfp4_rms_norm_quantize(st.h, eps=st.eps, out=st.xq, stream=stream),
+        "quantize_f32_query_slice": lambda: api.nvfp4_quantize_f32(st.y_qkv, K=st.k_o, out=st.xq_o, stream=stream),
+        "silu_mul_quantize": lambda: api.nvfp4_silu_mul_quantize(st.y_gu, out=st.xq_d, stream=stream),
+        "rms_norm_bf16": lambda: api.nvfp4_rms_norm_bf16(st.h, eps=st.eps, out=st.r, stream=stream),
+        "lm_head_bf16_gemv_tc": lambda: api.nvfp4_bf16_gemv_tc(st.r, st.lm_head, y=st.logits, workspace=st.ws,
+                                                                stream=stream),
+        "reset_sample": lambda: st.sampler(st.logits, st.step_start, st.u, stream=stream),
+    }
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, fn in calls.items():
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            out[name] = round(a.elapsed_time(b) * 1e3 / reps, 2)
+    out["lm_head_gbs"] = round(st.lm_head.numel() * 2 / (out["lm_head_bf16_gemv_tc"] * 1e-6) / 1e9, 1)
+    out["note"] = f"M={M}; each stage {reps}x back to back, L2-warm inputs"
+    return out
+
+
 def run_decode(args, world, rank):
     """The synthetic decode step: `--layers` layers of the four projections,
     the lm_head and the sampler, captured as one CUDA graph and replayed
@@ -464,6 +498,7 @@ def run_decode(args, world, rank):
         e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+    stages = decode_stage_times(st, stream)
     weight_bytes = sum(w.packed.numel() for layer in st.weights for w in layer.values())
     step_bytes = weight_bytes + st.lm_head.numel() * 2 + st.logits.numel() * 4 * 2
     peak, peak_kind = measured_peaks()
@@ -482,6 +517,7 @@ def run_decode(args, world, rank):
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms/step", "h2d_bytes_per_step": host_h.numel() * 4 + M * 4,
                 "d2h_bytes_per_step": 3 * M * 4},
+        "stages_us": stages,
         "clocks": clk.summary(),
         "gpu_launches": (args.layers * 8 + 3) * args.steps,   # per layer: 2 norm+quantize, 2 quantizers, 4 GEMVs
     }
