@@ -47,8 +47,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "ff7ce167721dc2fd82f98249a3318f31c520e7e60c302f68a636a2c0787d0cc9",
-                  "workload": "qwen3-32b", "bytes_per_launch": 68984786}
+                  "sha256": "4f75984507cf6f1d640c9e92baa13187753c4806dd0ae9c4f66e260e626eda16",
+                  "workload": "qwen3-32b", "bytes_per_launch": 68992451}
 
 
 def recorded_traffic(workload):
