@@ -62,7 +62,8 @@ def recorded_traffic(workload):
         return None
     return TRAFFIC_RECORD["bytes_per_launch"]
 WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8]),
-             "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8])}
+             "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8]), "reset-sampler": (None, [8])}
+SAMPLER_METRIC = "ReSET sampler latency per decode step, FP32 logits [8, 151936] (entropy, state update, T, sample)"
 DECODE_METRIC = "Qwen3-32B-shaped decode step latency (64 NVFP4 layers + BF16 lm_head + ReSET sampler, one CUDA graph)"
 
 
@@ -523,6 +524,58 @@ def run_decode(args, world, rank):
     }
 
 
+def run_sampler(args, world, rank):
+    """The sampler workload: M = 8 rows over the 151936-token vocabulary, one
+    step per iteration.  Each step's logits are generated on the device from
+    the seeded generator (sigma per step from {1, 3, 8}), then L2 is flushed,
+    then the sampler call alone is timed with events (its first pass reads the
+    logits from HBM)."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    dev = torch.device("cuda")
+    M, V = 8, synth.LM_HEAD_VOCAB
+    total = args.warmup + args.steps
+    sig = synth.reset_sigmas(total)
+    starts = torch.from_numpy(synth.reset_boundaries(total, M)).to(dev)
+    us = torch.from_numpy(synth.reset_uniforms(total, M)).to(dev)
+    sampler = api.ResetSampler(M, V, 0.6, 0.3, 1.0, 8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(total)]
+    barrier(world)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(total):
+            logits.copy_(synth.reset_logits(i + 1000 * rank, M, V, float(sig[i]), device=dev))
+            flush.zero_()
+            ev[i][0].record()
+            sampler(logits, starts[i], us[i])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = np.array([a.elapsed_time(b) for a, b in ev[args.warmup:]])
+    ms_mean = max_over_ranks(world, float(ms.mean()))
+    first_pass = 4 * M * V
+    peak, peak_kind = measured_peaks()
+    gbs = first_pass / (ms_mean * 1e-3) / 1e9
+    return {
+        "metric": SAMPLER_METRIC, "value": round(ms_mean * 1e3, 2), "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_mean, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (entropy and sample), fp64 (merge, state)",
+        "data": "synthetic (seeded N(0, sigma) logits per step, sigma in {1,3,8}; geometric step boundaries; "
+                "PCG64 uniforms)",
+        "config": {"workload": f"reset sampler, M={M}, V={V}, w=8, tau0=0.6, T=0.3/1.0",
+                   "l2": "flushed before every timed call (256 MB write)", "parallelism": f"replicas x{world}"},
+        "p50_us": round(float(np.percentile(ms, 50)) * 1e3, 2), "p99_us": round(float(np.percentile(ms, 99)) * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "kernel": "reset_sample_kernel: first-pass logits bytes (4 M V) / call time; latency-bound",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(ms_mean * 1e3, 2), "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0, "note": "device-resident logits, as the lm_head leaves them"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+
+
 # ---------------------------------------------------------------------------
 def cpu_oracle_sample(args, seconds):
     """The oracle as it stands, on the host: per call, quantize the activation
@@ -580,8 +633,8 @@ def main():
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
-    if args.workload == "qwen3-32b-decode":
-        line = run_decode(args, world, rank)
+    if args.workload in ("qwen3-32b-decode", "reset-sampler"):
+        line = (run_decode if args.workload == "qwen3-32b-decode" else run_sampler)(args, world, rank)
         if rank == 0:
             print(json.dumps(line))
         if world > 1:

@@ -73,54 +73,53 @@ def step():
     return st
 
 
-def test_decode_step_stagewise(step):
-    trace = []
-    tok, H, T = step.run(trace=trace)
-    tok, H, T = to_np(tok), to_np(H), to_np(T)
-    rng = np.random.default_rng(7)
-    for layer in range(step.layers):
-        tr, wr = trace[layer], step.rowmajor[layer]
-        _check_norm(to_np(tr["h_in"]), tr["r"])
-        r_bits = bits(tr["r"])
-        _check_quant(r_bits, tr["xq"])
-        _check_gemv(r_bits, wr["qkv"], tr["y_qkv"], rng)
-        q_bits = Q.f32_to_bf16_bits(to_np(tr["y_qkv"])[:, :step.k_o])
-        _check_quant(q_bits, tr["xq_o"])
-        _check_gemv(q_bits, wr["o"], tr["y_o"], rng)
-        _check_norm(to_np(tr["y_o"]), tr["r2"])
-        _check_quant(bits(tr["r2"]), tr["xq_gu"])
-        _check_gemv(bits(tr["r2"]), wr["gate_up"], tr["y_gu"], rng)
-        # SiLU(gate) * up -> NVFP4: exact on decisive blocks
-        gu = to_np(tr["y_gu"]).astype(np.float64)
-        a = D.silu_mul(gu)
-        mid = D.to_bf16_bits(a)
-        dec = (D.to_bf16_bits(a * (1 - 8 * 2.0 ** -24)) == D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24))) & \
-              (D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24)) == mid)
-        rc, rs, rg = Q.quantize_bf16(mid)
-        codes, scales, g = (to_np(t) for t in tr["xq_d"])
-        amax_idx = np.unravel_index(np.argmax(np.abs(Q.bf16_bits_to_f32(mid))), mid.shape)
-        if dec[amax_idx]:
-            assert g[0] == rg
-            blk = dec.reshape(step.M, -1, 16).all(axis=2)
-            assert blk.mean() > 0.9
-            assert np.array_equal(scales[blk], rs[blk])
-            el = np.repeat(blk, 16, axis=1)
-            assert np.array_equal(Q.unpack_codes(codes)[el], Q.unpack_codes(rc)[el])
-        # down: the oracle multiplies the GPU's own codes (checked above)
-        N = step.hidden
-        rows = np.unique(np.concatenate([rng.choice(N, ROWS, replace=False), [0, N - 1]]))
-        wd = wr["down"]
-        y_ref, bound = Q.gemv(codes, scales, g[0], to_np(wd.codes)[rows], to_np(wd.scales)[rows],
-                              to_np(wd.global_scale)[0])
-        assert_within(to_np(tr["h_out"])[:, rows], y_ref, bound)
-    fin = trace[-1]
+def _check_layer(step, tr, wr, rng):
+    """Every stage of one traced layer against the oracle, each from the GPU's
+    own input to that stage."""
+    _check_norm(to_np(tr["h_in"]), tr["r"])
+    r_bits = bits(tr["r"])
+    _check_quant(r_bits, tr["xq"])
+    _check_gemv(r_bits, wr["qkv"], tr["y_qkv"], rng)
+    q_bits = Q.f32_to_bf16_bits(to_np(tr["y_qkv"])[:, :step.k_o])
+    _check_quant(q_bits, tr["xq_o"])
+    _check_gemv(q_bits, wr["o"], tr["y_o"], rng)
+    _check_norm(to_np(tr["y_o"]), tr["r2"])
+    _check_quant(bits(tr["r2"]), tr["xq_gu"])
+    _check_gemv(bits(tr["r2"]), wr["gate_up"], tr["y_gu"], rng)
+    # SiLU(gate) * up -> NVFP4: exact on decisive blocks
+    gu = to_np(tr["y_gu"]).astype(np.float64)
+    a = D.silu_mul(gu)
+    mid = D.to_bf16_bits(a)
+    dec = (D.to_bf16_bits(a * (1 - 8 * 2.0 ** -24)) == D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24))) & \
+          (D.to_bf16_bits(a * (1 + 8 * 2.0 ** -24)) == mid)
+    rc, rs, rg = Q.quantize_bf16(mid)
+    codes, scales, g = (to_np(t) for t in tr["xq_d"])
+    amax_idx = np.unravel_index(np.argmax(np.abs(Q.bf16_bits_to_f32(mid))), mid.shape)
+    if dec[amax_idx]:
+        assert g[0] == rg
+        blk = dec.reshape(step.M, -1, 16).all(axis=2)
+        assert blk.mean() > 0.9
+        assert np.array_equal(scales[blk], rs[blk])
+        el = np.repeat(blk, 16, axis=1)
+        assert np.array_equal(Q.unpack_codes(codes)[el], Q.unpack_codes(rc)[el])
+    # down: the oracle multiplies the GPU's own codes (checked above)
+    N = step.hidden
+    rows = np.unique(np.concatenate([rng.choice(N, ROWS, replace=False), [0, N - 1]]))
+    wd = wr["down"]
+    y_ref, bound = Q.gemv(codes, scales, g[0], to_np(wd.codes)[rows], to_np(wd.scales)[rows],
+                          to_np(wd.global_scale)[0])
+    assert_within(to_np(tr["h_out"])[:, rows], y_ref, bound)
+
+
+def _check_head(step, fin, tok, H, T, rng):
+    """Final norm, lm_head (64 sampled vocabulary rows) and the sampler at the
+    first position of a step, on the GPU's logits."""
     _check_norm(to_np(fin["h_final"]), fin["r_final"])
     V = step.vocab
     rows = rng.choice(V, 64, replace=False)
     ref, scale = D.bf16_gemv(bits(fin["r_final"]), bits(step.lm_head[rows]))
     logits = to_np(fin["logits"])
     assert_within(logits[:, rows], ref, scale, rel=1e-4)
-    # sampler: the first position of every row (a new step), on the GPU's logits
     p = R.ResetParams(tau0=float(np.float32(0.6)), t_low=float(np.float32(0.3)), t_high=1.0, w=8)
     u = to_np(step.u)
     for r in range(step.M):
@@ -133,7 +132,36 @@ def test_decode_step_stagewise(step):
         lo, hi = R.acceptable_tokens(ln, float(T[r]), float(u[r]), 4e-6)
         assert lo <= tok[r] <= hi
     assert np.all(np.isfinite(logits))
+
+
+def test_decode_step_stagewise(step):
+    trace = []
+    tok, H, T = step.run(trace=trace)
+    tok, H, T = to_np(tok), to_np(H), to_np(T)
+    rng = np.random.default_rng(7)
+    for layer in range(step.layers):
+        _check_layer(step, trace[layer], step.rowmajor[layer], rng)
+    _check_head(step, trace[-1], tok, H, T, rng)
     assert api.device_status() == 0
+
+
+def test_decode_step_full_depth_sampled():
+    """The full 64-layer step (distinct random weights per layer, M = 1) at
+    step 0: layers 0, 31 and 63 checked stage by stage, then the head."""
+    st = DecodeStep(M=1, layers=64, keep_rowmajor=True, seed=3)
+    st.h_in.copy_(synth.activations(1, st.hidden, seed=13).float().cuda())
+    st.step_start.fill_(1)
+    st.u.fill_(0.37)
+    trace = []
+    tok, H, T = st.run(trace=trace)
+    tok, H, T = to_np(tok), to_np(H), to_np(T)
+    rng = np.random.default_rng(8)
+    for layer in (0, 31, 63):
+        _check_layer(st, trace[layer], st.rowmajor[layer], rng)
+    _check_head(st, trace[-1], tok, H, T, rng)
+    assert api.device_status() == 0
+    del st, trace
+    torch.cuda.empty_cache()
 
 
 def _buffers(st):
