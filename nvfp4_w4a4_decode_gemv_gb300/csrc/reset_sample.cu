@@ -180,7 +180,13 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
     Z = warp_sum_d(Z);
     A = warp_sum_d(A);
     if (lane == 0) {
-      const double H = log(Z) - A / Z;
+      // The logarithm and the mean in FP32: FP64 is a narrow pipe on this part
+      // and this chain is serial.  Z >= 1 (the maximum contributes e^0), and
+      // Z - 1 is formed in FP64 so that log1p keeps its relative precision
+      // when the distribution is nearly one-hot (H -> 0); the two terms have
+      // the same sign, so H keeps ~1e-7 relative error against a 1e-4
+      // tolerance.
+      const double H = (double)(log1pf((float)(Z - 1.0)) - (float)A / (float)Z);
       // ---- ReSET state update (FP64 sums) ----
       RowState* st = reinterpret_cast<RowState*>(state + (size_t)row * stride);
       double* ring = reinterpret_cast<double*>(st + 1);
@@ -240,24 +246,43 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
     s_zt[q] = (double)expf((p0.x - gmax) * invT) * (double)(use_low ? p0.w : p1.x);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // first chunk whose cumulative Z_T passes the target; if rounding leaves
-    // the target at or past the total, the last chunk
-    double total = 0.0;
-    for (int q = 0; q < NC; ++q) total += s_zt[q];
-    s_target *= total;
-    double before = 0.0;
-    int cstar = NC - 1;
-    for (int q = 0; q < NC; ++q) {
-      if (before + s_zt[q] > s_target || q == NC - 1) {
-        cstar = q;
-        break;
-      }
-      before += s_zt[q];
+  if (warp == 0) {
+    // The first chunk whose cumulative Z_T passes the target (the last chunk
+    // if rounding leaves the target at or past the total).  Lane L owns the
+    // consecutive chunks [L per, (L+1) per): per-lane sums, an inclusive scan
+    // across the warp, and the first lane whose running sum passes the target
+    // walks its own chunks (a serial loop over all chunks cost 6 us in FP64).
+    const int per = (NC + 31) / 32;
+    const int q0 = lane * per, q1 = min(NC, q0 + per);
+    double mine = 0.0;
+    for (int q = q0; q < q1; ++q) mine += s_zt[q];
+    double incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
     }
-    s_chunk = cstar;
-    s_target = s_target - before;
-    s_tok = 0x7fffffff;
+    const double total = __shfl_sync(0xffffffffu, incl, 31);
+    const double target = s_target * total;     // s_target holds u until here
+    const unsigned hit = __ballot_sync(0xffffffffu, q0 < q1 && incl > target);
+    const int owner = hit ? __ffs(hit) - 1 : (NC - 1) / per;
+    if (lane == owner) {
+      // The owner's last chunk is the fallback: the walk re-adds in its own
+      // order, so it may stop short of a target that `incl` passed by a
+      // rounding; for the last lane this is the "last chunk" case.
+      double before = incl - mine;
+      int cstar = q1 - 1;
+      for (int q = q0; q < q1 - 1; ++q) {
+        if (before + s_zt[q] > target) {
+          cstar = q;
+          break;
+        }
+        before += s_zt[q];
+      }
+      s_chunk = cstar;
+      s_target = target - before;
+      s_tok = 0x7fffffff;
+    }
   }
   __syncthreads();
   // ---- scan the chosen chunk: thread t owns 8 consecutive logits ----
