@@ -165,18 +165,34 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
 
   // ---- last CTA of the row: merge chunk partials in chunk order (FP64) ----
   if (warp == 0) {
+    // Each lane's first kCached chunk partials are loaded together and kept in
+    // registers for both passes (one round of L2 latency instead of one per
+    // chunk and pass); chunks beyond 32 * kCached (V > 262144) are reloaded.
+    constexpr int kCached = 4;
+    const float4* prow = reinterpret_cast<const float4*>(parts + (size_t)row * NC);
+    float4 c0[kCached], c1[kCached];
+#pragma unroll
+    for (int i = 0; i < kCached; ++i) {
+      const int q = lane + 32 * i;
+      c0[i] = q < NC ? __ldcg(prow + 2 * q) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      c1[i] = q < NC ? __ldcg(prow + 2 * q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float gmax = -INFINITY;
-    for (int q = lane; q < NC; q += 32) gmax = fmaxf(gmax, __ldcg(&parts[(size_t)row * NC + q].mx));
+#pragma unroll
+    for (int i = 0; i < kCached; ++i) gmax = fmaxf(gmax, c0[i].x);
+    for (int q = lane + 32 * kCached; q < NC; q += 32) gmax = fmaxf(gmax, __ldcg(&parts[(size_t)row * NC + q].mx));
     gmax = warp_max(gmax);
     double Z = 0.0, A = 0.0;
-    for (int q = lane; q < NC; q += 32) {
-      const float4 p0 = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)row * NC + q));
-      const float4 p1 = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)row * NC + q) + 1);
+    auto add = [&](const float4& p0, const float4& p1) {
       const float d = p0.x - gmax;                      // <= 0
       const double r1 = (double)expf(d);
       Z += r1 * ((double)p1.y + (double)p0.y);
       A += r1 * ((double)p0.z + (double)d * ((double)p0.y + (double)p1.y));
-    }
+    };
+#pragma unroll
+    for (int i = 0; i < kCached; ++i)
+      if (lane + 32 * i < NC) add(c0[i], c1[i]);
+    for (int q = lane + 32 * kCached; q < NC; q += 32) add(__ldcg(prow + 2 * q), __ldcg(prow + 2 * q + 1));
     Z = warp_sum_d(Z);
     A = warp_sum_d(A);
     if (lane == 0) {
@@ -288,15 +304,32 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
   // ---- scan the chosen chunk: thread t owns 8 consecutive logits ----
   const int clo = s_chunk * kChunk;
   const int chi = min(V, clo + kChunk);
-  double pre[kPerThread];
-  double tsum = 0.0;
+  // The thread's 8 running sums in FP32 (relative error <= 8 roundings of the
+  // thread's sum, far inside the 4e-6 Z tolerance of the sample); the scan
+  // across threads and the comparisons in FP64.
+  float pre[kPerThread];
+  float fsum = 0.0f;
+  {
+    const int i0 = clo + threadIdx.x * kPerThread;
+    float lv[kPerThread];
+    // 16-byte loads only where the row start is 16-byte aligned (V a multiple
+    // of 4; logits itself is checked 16-byte aligned) and all 8 are in range.
+    if ((V & 3) == 0 && i0 + kPerThread <= chi) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(base + i0));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(base + i0) + 1);
+      lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
+      lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
+    } else {
 #pragma unroll
-  for (int k = 0; k < kPerThread; ++k) {
-    const int i = clo + threadIdx.x * kPerThread + k;
-    const double e = (i < chi) ? (double)expf((__ldg(base + i) - gmax) * invT) : 0.0;
-    tsum += e;
-    pre[k] = tsum;
+      for (int k = 0; k < kPerThread; ++k) lv[k] = (i0 + k < chi) ? __ldg(base + i0 + k) : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      fsum += (i0 + k < chi) ? expf((lv[k] - gmax) * invT) : 0.0f;
+      pre[k] = fsum;
+    }
   }
+  const double tsum = (double)fsum;
   // exclusive scan of thread totals across the CTA
   double incl = tsum;
 #pragma unroll
@@ -314,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
 #pragma unroll
   for (int k = kPerThread - 1; k >= 0; --k) {
     const int i = clo + threadIdx.x * kPerThread + k;
-    if (i < chi && excl + pre[k] > target) cand = i;
+    if (i < chi && excl + (double)pre[k] > target) cand = i;
   }
   if (cand != 0x7fffffff) atomicMin(&s_tok, cand);
   __syncthreads();
