@@ -38,16 +38,6 @@ enum : unsigned int {
   NVFP4_DEVERR_FLAG_TIMEOUT = 4,   // a wait for another CTA's partial sum exceeded its iteration limit
 };
 
-// Release store / acquire load of a flag word at GPU scope.
-NVFP4_DEVINL void st_release_gpu(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-NVFP4_DEVINL unsigned int ld_acquire_gpu(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Relaxed GPU-scope word store / load: single-copy atomic, no ordering.
 NVFP4_DEVINL void st_relaxed_gpu(unsigned int* p, unsigned int v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -72,10 +62,6 @@ NVFP4_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
 
 NVFP4_DEVINL void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-NVFP4_DEVINL void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 NVFP4_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -132,15 +118,6 @@ NVFP4_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32
 // __threadfence).
 NVFP4_DEVINL void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-// GPU-scope atomic add with acquire-release semantics: the calling thread's
-// earlier writes (and those ordered before them) are visible before the add,
-// and writes visible to the add are visible to the thread after it.
-NVFP4_DEVINL unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
-  unsigned int old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 // Programmatic dependent launch: wait for the preceding grid's completion and
 // memory, and let the next grid start launching.
 NVFP4_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -170,10 +147,6 @@ NVFP4_DEVINL void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The two halves of cluster_sync, for work placed between them.
-NVFP4_DEVINL void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-NVFP4_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
 // Address of the same shared variable in CTA `rank` of this cluster.
 NVFP4_DEVINL uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t out;
@@ -183,12 +156,6 @@ NVFP4_DEVINL uint32_t dsmem_addr(const void* local, uint32_t rank) {
 
 NVFP4_DEVINL void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-NVFP4_DEVINL float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 // ---- number formats --------------------------------------------------------
