@@ -62,6 +62,7 @@ def recorded_traffic(workload):
         return None
     return TRAFFIC_RECORD["bytes_per_launch"]
 WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8]),
+             "qwen3-14b": (synth.QWEN3_14B, [1, 2, 4, 8]),
              "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8]), "reset-sampler": (None, [8])}
 SAMPLER_METRIC = "ReSET sampler latency per decode step, FP32 logits [8, 151936] (entropy, state update, T, sample)"
 DECODE_METRIC = "Qwen3-32B-shaped decode step latency (64 NVFP4 layers + BF16 lm_head + ReSET sampler, one CUDA graph)"
@@ -614,9 +615,50 @@ def cpu_oracle_sample(args, seconds):
     return done_bytes / dt / 1e9, sample, threads, dt
 
 
+def cpu_sampler_sample(args, seconds):
+    """The oracle sampler as it stands, on the host: per step, for the 8 rows,
+    the FP64 entropy, the ReSET update and the FP64 inverse-CDF sample, over
+    the same seeded logits as the GPU workload, until about `seconds`."""
+    from oracle import reset as R
+    M, V = 8, synth.LM_HEAD_VOCAB
+    p = R.ResetParams(tau0=0.6, t_low=0.3, t_high=1.0, w=8)
+    total = max(1, args.warmup + args.steps)
+    sig = synth.reset_sigmas(total)
+    starts = synth.reset_boundaries(total, M)
+    us = synth.reset_uniforms(total, M)
+    states = [R.RowState(w=8) for _ in range(M)]
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < seconds:
+        t = done % total
+        ln = synth.reset_logits(t, M, V, float(sig[t])).numpy().astype(np.float64)
+        for r in range(M):
+            res = R.reset_update(states[r], R.token_entropy(ln[r]), bool(starts[t, r]), p)
+            R.sample_inverse_cdf(ln[r], res.T, float(us[t, r]))
+        done += 1
+    dt = time.perf_counter() - t0
+    return dt / done * 1e6, f"{done} steps of the reset-sampler workload (M={M}, V={V}); {dt:.1f} s"
+
+
 def main():
     args = parse()
     world, rank = dist_setup(args)
+    if args.impl == "reference" and args.workload == "reset-sampler":
+        if rank != 0:
+            return
+        us_step, sample = cpu_sampler_sample(args, seconds=max(5.0, min(60.0, args.cpu_seconds)))
+        threads = torch.get_num_threads()
+        line = {"metric": SAMPLER_METRIC, "value": round(us_step, 1), "unit": "us/step", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_step / 1e3, 4),
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64 (oracle entropy and inverse-CDF sample)", "data": "synthetic", "impl": "reference",
+                "config": {"workload": f"reset sampler, M=8, V={synth.LM_HEAD_VOCAB}, w=8, tau0=0.6, T=0.3/1.0"},
+                "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -635,6 +677,10 @@ def main():
         return
     if args.workload in ("qwen3-32b-decode", "reset-sampler"):
         line = (run_decode if args.workload == "qwen3-32b-decode" else run_sampler)(args, world, rank)
+        if rank == 0 and args.workload == "reset-sampler" and not args.no_cpu_baseline:
+            us_step, sample = cpu_sampler_sample(args, seconds=args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(us_step, 1), "unit": "us/step", "cores": torch.get_num_threads(),
+                                    "kind": "oracle", "sample": sample}
         if rank == 0:
             print(json.dumps(line))
         if world > 1:

@@ -79,7 +79,7 @@ def test_deterministic_and_repeatable():
     assert np.array_equal(y1, y2) and np.array_equal(y2, y3)
 
 
-@pytest.mark.parametrize("name,K,N", synth.QWEN3_32B + synth.QWEN3_8B)
+@pytest.mark.parametrize("name,K,N", synth.QWEN3_32B + synth.QWEN3_8B + synth.QWEN3_14B)
 def test_full_size_sampled_rows(name, K, N):
     """The benchmark's projection shapes at full size: the GPU quantizes and
     multiplies the whole matrix; the oracle checks 96 sampled output rows (and
