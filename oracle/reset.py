@@ -12,7 +12,12 @@ Sources (the ReSET pages):
     the mean of the last w token entropies (crossing the step boundary), after
     that the running in-step mean (reading note §4.2);
   * T_t = T_low if H_t < tau_t else T_high (project page formula; reading note
-    Eq. (1) in §3.1 and §4.3), then sample from softmax(logits / T_t).
+    Eq. (1) in §3.1 and §4.3), then sample from softmax(logits / T_t);
+  * the two threshold policies ReSET is compared against (reading note §3.1
+    Eq. (1) and §6.3, Table 2): a fixed threshold tau_t = tau0, and a
+    sliding-window threshold;
+  * nucleus (top-p) truncation, which the pages' evaluation applies on top of
+    the temperature (reading note §6.1 "top-p=0.95", §6.3 Table 5).
 
 Readings where the pages leave a step open (each pinned by a test):
   * entropy is in nats, at temperature 1, of the raw logits;
@@ -25,7 +30,17 @@ Readings where the pages leave a step open (each pinned by a test):
   * H_bar_t is the mean of H_0..H_t (including t);
   * the sample is inverse-CDF: token = min{ i : C_i > u * Z } with
     C_i = sum_{k<=i} exp(s_k / T), Z = C_{V-1}, s = logits - max, u in [0, 1)
-    supplied by the caller.  No top-p.
+    supplied by the caller;
+  * the sliding-window threshold is tau_t = the mean of the last w token
+    entropies including H_t, over the whole sequence (step boundaries play no
+    part; truncated at the sequence start) -- the pages name the policy but do
+    not write it out, and this is the window half of HSE used as the threshold
+    at every position;
+  * top-p keeps the smallest set of most probable tokens whose probability
+    (at temperature T_t) reaches p, and keeps every token tied with the least
+    probable one kept: token i stays iff the mass of the tokens with a
+    strictly larger logit is below p * Z.  The kept tokens are renormalised and
+    sampled inverse-CDF in vocabulary order, as above.  top_p = 1 keeps all.
 
 Test infrastructure only (see the package docstring).
 """
@@ -35,12 +50,17 @@ from dataclasses import dataclass, field
 import numpy as np
 
 
+THRESHOLDS = ("reset", "fixed", "window")
+
+
 @dataclass
 class ResetParams:
     tau0: float = 0.6
     t_low: float = 0.3
     t_high: float = 1.0
     w: int = 8
+    threshold: str = "reset"        # one of THRESHOLDS
+    top_p: float = 1.0              # in (0, 1]; 1 = no truncation
 
 
 def token_entropy(logits: np.ndarray) -> float:
@@ -52,25 +72,72 @@ def token_entropy(logits: np.ndarray) -> float:
     return float(np.log(Z) - np.sum(e * s) / Z)
 
 
-def sample_inverse_cdf(logits: np.ndarray, T: float, u: float) -> int:
-    """min{ i : C_i > u Z } for p_i proportional to exp((l_i - max l) / T)."""
+def nucleus_mask(logits: np.ndarray, T: float, top_p: float) -> np.ndarray:
+    """Boolean [V]: the tokens top-p keeps at temperature T.  Token i stays iff
+    sum of exp((l_j - max l) / T) over the tokens with l_j > l_i is below
+    top_p * Z (so ties with the least probable kept token all stay)."""
     l = np.asarray(logits, dtype=np.float64)
+    if top_p >= 1.0:
+        return np.ones(l.shape, dtype=bool)
     e = np.exp((l - np.max(l)) / T)
+    Z = float(np.sum(e))
+    vals, inv = np.unique(l, return_inverse=True)       # ascending distinct logits
+    group_mass = np.bincount(inv, weights=e, minlength=len(vals))
+    # mass of the strictly larger logits, per distinct value
+    above = np.concatenate([np.cumsum(group_mass[::-1])[::-1][1:], [0.0]])
+    return (above < top_p * Z)[inv]
+
+
+def sample_inverse_cdf(logits: np.ndarray, T: float, u: float, top_p: float = 1.0) -> int:
+    """min{ i : C_i > u Z } for p_i proportional to exp((l_i - max l) / T),
+    restricted to the nucleus_mask tokens (all of them when top_p = 1)."""
+    l = np.asarray(logits, dtype=np.float64)
+    e = np.exp((l - np.max(l)) / T) * nucleus_mask(l, T, top_p)
     C = np.cumsum(e)
     return int(np.argmax(C > u * C[-1]))
 
 
-def acceptable_tokens(logits: np.ndarray, T: float, u: float, rel: float) -> tuple[int, int]:
+def acceptable_tokens(logits: np.ndarray, T: float, u: float, rel: float, keep=None) -> tuple[int, int]:
     """Range [lo, hi] of tokens that a sampler whose partial sums are accurate
-    to rel * Z may return: lo samples at u - rel, hi at u + rel."""
+    to rel * Z may return: lo samples at u - rel, hi at u + rel.  `keep`
+    restricts the sample to a nucleus (boolean mask)."""
     l = np.asarray(logits, dtype=np.float64)
     e = np.exp((l - np.max(l)) / T)
+    if keep is not None:
+        e = e * keep
     C = np.cumsum(e)
     Z = C[-1]
     lo = int(np.argmax(C > max(u - rel, 0.0) * Z))
     hi_mask = C > min(u + rel, 1.0) * Z
     hi = int(np.argmax(hi_mask)) if hi_mask.any() else len(C) - 1
     return lo, hi
+
+
+def nucleus_candidates(logits: np.ndarray, T: float, top_p: float, rel: float) -> list:
+    """The nuclei a sampler whose masses are accurate to rel * Z may keep: the
+    exact nucleus_mask, plus the one with its least probable logit group
+    dropped when that group's `above` sum lies within rel * Z of top_p * Z, and
+    the one with the next group added when that group's `above` sum does."""
+    l = np.asarray(logits, dtype=np.float64)
+    if top_p >= 1.0:
+        return [np.ones(l.shape, dtype=bool)]
+    e = np.exp((l - np.max(l)) / T)
+    Z = float(np.sum(e))
+    vals, inv = np.unique(l, return_inverse=True)
+    group_mass = np.bincount(inv, weights=e, minlength=len(vals))
+    above = np.concatenate([np.cumsum(group_mass[::-1])[::-1][1:], [0.0]])
+    kept = above < top_p * Z                      # a suffix of the ascending groups
+    out = [kept[inv]]
+    g_last = int(np.argmax(kept))                 # least probable kept group
+    if g_last + 1 < len(vals) and abs(above[g_last] - top_p * Z) <= rel * Z:
+        k2 = kept.copy()
+        k2[g_last] = False
+        out.append(k2[inv])
+    if g_last >= 1 and abs(above[g_last - 1] - top_p * Z) <= rel * Z:
+        k3 = kept.copy()
+        k3[g_last - 1] = True
+        out.append(k3[inv])
+    return out
 
 
 @dataclass
@@ -93,6 +160,7 @@ class StepResult:
     tau: float
     T: float
     j: int
+    H_win: float = 0.0
 
 
 def reset_update(st: RowState, H: float, step_start: bool, p: ResetParams) -> StepResult:
@@ -101,17 +169,25 @@ def reset_update(st: RowState, H: float, step_start: bool, p: ResetParams) -> St
         st.j = 0
     st.hist.append(float(H))
     j = st.j
+    win = st.hist[-p.w:]                          # last <= w entropies, may cross the step start
+    H_win = math.fsum(win) / len(win)
     if j < p.w:
-        win = st.hist[-p.w:]                      # last <= w entropies, may cross the step start
-        H_step = math.fsum(win) / len(win)
+        H_step = H_win
     else:
         H_step = math.fsum(st.hist[-(j + 1):]) / (j + 1)   # positions 0..j of this step
     H_bar = math.fsum(st.hist) / (st.t + 1)
-    tau = p.tau0 if H_step <= H_bar else H_step
+    if p.threshold == "fixed":                    # Eq. (1): one global threshold
+        tau = p.tau0
+    elif p.threshold == "window":                 # sliding-window threshold
+        tau = H_win
+    elif p.threshold == "reset":                  # SAT over the HSE estimate
+        tau = p.tau0 if H_step <= H_bar else H_step
+    else:
+        raise ValueError(f"unknown threshold policy {p.threshold!r}")
     T = p.t_low if H < tau else p.t_high
     st.t += 1
     st.j += 1
-    return StepResult(H=H, H_step=H_step, H_bar=H_bar, tau=tau, T=T, j=j)
+    return StepResult(H=H, H_step=H_step, H_bar=H_bar, tau=tau, T=T, j=j, H_win=H_win)
 
 
 def run_sequence(logits: np.ndarray, step_start: np.ndarray, u: np.ndarray, p: ResetParams):
@@ -127,7 +203,7 @@ def run_sequence(logits: np.ndarray, step_start: np.ndarray, u: np.ndarray, p: R
         for r in range(M):
             H = token_entropy(logits[t, r])
             res = reset_update(states[r], H, bool(step_start[t, r]), p)
-            tokens[t, r] = sample_inverse_cdf(logits[t, r], res.T, float(u[t, r]))
+            tokens[t, r] = sample_inverse_cdf(logits[t, r], res.T, float(u[t, r]), p.top_p)
             row_res.append(res)
         results.append(row_res)
     return results, tokens
@@ -140,7 +216,7 @@ def temperature_is_ambiguous(res: StepResult, p: ResetParams, rel: float = 1e-4)
         return p.t_low if res.H < tau else p.t_high
     cands = {res.T}
     taus = [res.tau]
-    if abs(res.H_step - res.H_bar) <= rel * max(1.0, abs(res.H_bar)):
+    if p.threshold == "reset" and abs(res.H_step - res.H_bar) <= rel * max(1.0, abs(res.H_bar)):
         taus = [p.tau0, res.H_step]
         cands.update(pick_T(tau) for tau in taus)
     for tau in taus:

@@ -145,3 +145,115 @@ def test_ambiguity_detector():
     assert R.temperature_is_ambiguous(near_tau, p)
     near_bar = R.StepResult(H=0.7, H_step=0.90001, H_bar=0.9, tau=0.90001, T=0.3, j=0)
     assert R.temperature_is_ambiguous(near_bar, p)
+
+
+# ---- the two other threshold policies (reading note §3.1 Eq. (1), §6.3 Table 2) ----
+# Same 11-position script.  Fixed: T_low exactly where H < tau0 = 0.6.
+SCRIPT_T_FIXED = [1.0, 0.3, 0.3, 1.0, 0.3, 0.3, 1.0, 0.3, 1.0, 1.0, 1.0]
+# Sliding window, w = 3: tau = mean of the last 3 entropies including H (the
+# step boundary at t = 6 plays no part), worked by hand.
+SCRIPT_TAU_WINDOW = [1.0, 0.625, 1.75 / 3, 2.75 / 3, 1.0, 2.75 / 3, 0.75, 0.625, 0.875, 2.875 / 3, 3.625 / 3]
+SCRIPT_T_WINDOW = [1.0, 0.3, 0.3, 1.0, 0.3, 0.3, 1.0, 0.3, 1.0, 1.0, 0.3]
+
+
+@pytest.mark.parametrize("policy", ["fixed", "window"])
+def test_threshold_policies_hand_script(policy):
+    p = R.ResetParams(tau0=0.6, t_low=0.3, t_high=1.0, w=3, threshold=policy)
+    st = R.RowState(w=3)
+    for t, (H, s) in enumerate(zip(SCRIPT_H, SCRIPT_START)):
+        res = R.reset_update(st, H, bool(s), p)
+        # the HSE estimate and the running mean are tracked whatever the policy
+        hs, hb, _, _, j = SCRIPT_WANT[t]
+        assert res.j == j and res.H_step == pytest.approx(hs, abs=1e-15) and res.H_bar == pytest.approx(hb, abs=1e-15)
+        if policy == "fixed":
+            assert res.tau == 0.6 and res.T == SCRIPT_T_FIXED[t], t
+        else:
+            assert res.tau == pytest.approx(SCRIPT_TAU_WINDOW[t], abs=1e-15), t
+            assert res.T == SCRIPT_T_WINDOW[t], t
+
+
+def test_unknown_policy_is_an_error():
+    with pytest.raises(ValueError):
+        R.reset_update(R.RowState(w=2), 0.5, False, R.ResetParams(threshold="ema"))
+
+
+def test_policy_ambiguity_ignores_step_comparison_outside_reset():
+    # H_step == H_bar is a guard-band case for ReSET only (tau0 = 0.6 gives
+    # T_high at H = 0.7, tau = H_step = 0.9 gives T_low)
+    res = R.StepResult(H=0.7, H_step=0.9, H_bar=0.9, tau=0.6, T=1.0, j=0)
+    assert R.temperature_is_ambiguous(res, R.ResetParams(tau0=0.6, t_low=0.3))
+    assert not R.temperature_is_ambiguous(res, R.ResetParams(tau0=0.6, t_low=0.3, threshold="fixed"))
+
+
+# ---- top-p (reading note §6.1, §6.3 Table 5) ------------------------------------
+@pytest.mark.parametrize("top_p,keep", [
+    (0.49, [1]), (0.51, [1, 2]), (0.79, [1, 2]), (0.81, [0, 1, 2]), (1.0, [0, 1, 2]),
+])
+def test_nucleus_hand_worked(top_p, keep):
+    # probabilities 0.2, 0.5, 0.3 in vocabulary order
+    l = np.log(np.array([0.2, 0.5, 0.3]))
+    assert np.flatnonzero(R.nucleus_mask(l, 1.0, top_p)).tolist() == keep
+
+
+def test_nucleus_keeps_whole_tie_group():
+    l = np.log(np.array([0.3, 0.4, 0.3]))
+    assert R.nucleus_mask(l, 1.0, 0.5).tolist() == [True, True, True]     # 0.4 + one 0.3 reaches 0.5: both 0.3 stay
+    assert R.nucleus_mask(l, 1.0, 0.39).tolist() == [False, True, False]
+    assert R.nucleus_mask(np.zeros(10), 1.0, 0.01).all()                   # uniform: one group
+
+
+def test_nucleus_temperature_applies_first():
+    # p = [1, 2, 3, 4] / 10 at T = 1; at T = 0.5 they become [1, 4, 9, 16] / 30
+    l = np.log(np.array([1.0, 2.0, 3.0, 4.0]))
+    assert np.flatnonzero(R.nucleus_mask(l, 1.0, 0.5)).tolist() == [2, 3]   # 0.4 < 0.5 <= 0.7
+    assert np.flatnonzero(R.nucleus_mask(l, 0.5, 0.5)).tolist() == [3]      # 16/30 >= 0.5
+    assert np.flatnonzero(R.nucleus_mask(l, 0.5, 0.6)).tolist() == [2, 3]   # 16/30 < 0.6 <= 25/30
+
+
+def _brute_nucleus(prob, top_p):
+    """Smallest subset reaching top_p, by enumeration (distinct probabilities:
+    the most massive subset of the smallest size that reaches top_p)."""
+    import itertools
+    V = len(prob)
+    tot = prob.sum()
+    for k in range(1, V + 1):
+        best = max(itertools.combinations(range(V), k), key=lambda c: prob[list(c)].sum())
+        if prob[list(best)].sum() >= top_p * tot:
+            return sorted(best)
+    return list(range(V))
+
+
+def test_nucleus_brute_force_and_sample():
+    rng = np.random.default_rng(7)
+    n = 0
+    for _ in range(300):
+        V = int(rng.integers(1, 8))
+        l = rng.standard_normal(V) * 2
+        T = float(rng.choice([0.3, 1.0]))
+        top_p = float(rng.uniform(0.05, 1.0))
+        prob = np.exp((l - l.max()) / T)
+        keep = _brute_nucleus(prob, top_p)
+        if any(abs(prob[keep[:i]].sum() - top_p * prob.sum()) < 1e-9 for i in range(len(keep) + 1)):
+            continue                                  # too close to a boundary for an exact comparison
+        assert np.flatnonzero(R.nucleus_mask(l, T, top_p)).tolist() == keep
+        # inverse CDF over the kept tokens only, renormalised
+        u = float(rng.uniform())
+        c, want = 0.0, keep[-1]
+        for i in keep:
+            c += prob[i]
+            if c > u * prob[keep].sum():
+                want = i
+                break
+        assert R.sample_inverse_cdf(l, T, u, top_p) == want
+        n += 1
+    assert n > 250
+
+
+def test_nucleus_candidates_cover_boundary_groups():
+    l = np.log(np.array([0.2, 0.5, 0.3]))
+    # top_p * Z at exactly the kept mass 0.8: within rel of the group at 0.2
+    c = R.nucleus_candidates(l, 1.0, 0.8 + 1e-9, 1e-6)
+    masks = sorted(tuple(m.tolist()) for m in c)
+    assert (True, True, True) in masks and (False, True, True) in masks
+    assert len(R.nucleus_candidates(l, 1.0, 0.7, 1e-6)) == 1
+    assert R.nucleus_candidates(l, 1.0, 1.0, 1e-6)[0].all()
