@@ -80,6 +80,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
     ap.add_argument("--m", type=int, default=None, help="decode workload: the number of tokens M (1, 4 or 8)")
+    ap.add_argument("--top-p", type=float, default=1.0,
+                    help="sampler workload: nucleus mass (1 = no truncation; the pages' evaluation uses 0.95)")
+    ap.add_argument("--threshold", default="reset", choices=["reset", "fixed", "window"],
+                    help="sampler workload: the entropy-threshold policy")
     ap.add_argument("--layers", type=int, default=64, help="decode workload: decoder layers")
     ap.add_argument("--weights", default="packed", choices=["packed", "rowmajor"],
                     help="weight layout: packed (nvfp4_pack_weights, offline) or row-major codes/scales")
@@ -525,6 +529,15 @@ def run_decode(args, world, rank):
     }
 
 
+def sampler_workload(args) -> str:
+    text = f"reset sampler, M=8, V={synth.LM_HEAD_VOCAB}, w=8, tau0=0.6, T=0.3/1.0"
+    if args.threshold != "reset":
+        text += f", {args.threshold} threshold"
+    if args.top_p < 1.0:
+        text += f", top-p {args.top_p:g}"
+    return text
+
+
 def run_sampler(args, world, rank):
     """The sampler workload: M = 8 rows over the 151936-token vocabulary, one
     step per iteration.  Each step's logits are generated on the device from
@@ -538,7 +551,7 @@ def run_sampler(args, world, rank):
     sig = synth.reset_sigmas(total)
     starts = torch.from_numpy(synth.reset_boundaries(total, M)).to(dev)
     us = torch.from_numpy(synth.reset_uniforms(total, M)).to(dev)
-    sampler = api.ResetSampler(M, V, 0.6, 0.3, 1.0, 8, device=dev)
+    sampler = api.ResetSampler(M, V, 0.6, 0.3, 1.0, 8, device=dev, threshold=args.threshold, top_p=args.top_p)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     logits = torch.empty((M, V), dtype=torch.float32, device=dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(total)]
@@ -563,17 +576,18 @@ def run_sampler(args, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (entropy and sample), fp64 (merge, state)",
         "data": "synthetic (seeded N(0, sigma) logits per step, sigma in {1,3,8}; geometric step boundaries; "
                 "PCG64 uniforms)",
-        "config": {"workload": f"reset sampler, M={M}, V={V}, w=8, tau0=0.6, T=0.3/1.0",
+        "config": {"workload": sampler_workload(args),
                    "l2": "flushed before every timed call (256 MB write)", "parallelism": f"replicas x{world}"},
         "p50_us": round(float(np.percentile(ms, 50)) * 1e3, 2), "p99_us": round(float(np.percentile(ms, 99)) * 1e3, 2),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "traffic": None,
-                     "kernel": "reset_sample_kernel: first-pass logits bytes (4 M V) / call time; latency-bound",
+                     "kernel": "reset_sample_kernel" + (" + 4 top-p launches" if args.top_p < 1.0 else "") +
+                               ": first-pass logits bytes (4 M V) / call time; latency-bound",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(ms_mean * 1e3, 2), "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0, "note": "device-resident logits, as the lm_head leaves them"},
         "clocks": clk.summary(),
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (5 if args.top_p < 1.0 else 1),
     }
 
 
@@ -621,7 +635,8 @@ def cpu_sampler_sample(args, seconds):
     the same seeded logits as the GPU workload, until about `seconds`."""
     from oracle import reset as R
     M, V = 8, synth.LM_HEAD_VOCAB
-    p = R.ResetParams(tau0=0.6, t_low=0.3, t_high=1.0, w=8)
+    p = R.ResetParams(tau0=0.6, t_low=0.3, t_high=1.0, w=8, threshold=args.threshold,
+                      top_p=float(np.float32(args.top_p)))
     total = max(1, args.warmup + args.steps)
     sig = synth.reset_sigmas(total)
     starts = synth.reset_boundaries(total, M)
@@ -634,7 +649,7 @@ def cpu_sampler_sample(args, seconds):
         ln = synth.reset_logits(t, M, V, float(sig[t])).numpy().astype(np.float64)
         for r in range(M):
             res = R.reset_update(states[r], R.token_entropy(ln[r]), bool(starts[t, r]), p)
-            R.sample_inverse_cdf(ln[r], res.T, float(us[t, r]))
+            R.sample_inverse_cdf(ln[r], res.T, float(us[t, r]), p.top_p)
         done += 1
     dt = time.perf_counter() - t0
     return dt / done * 1e6, f"{done} steps of the reset-sampler workload (M={M}, V={V}); {dt:.1f} s"
@@ -652,7 +667,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_step / 1e3, 4),
                 "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64 (oracle entropy and inverse-CDF sample)", "data": "synthetic", "impl": "reference",
-                "config": {"workload": f"reset sampler, M=8, V={synth.LM_HEAD_VOCAB}, w=8, tau0=0.6, T=0.3/1.0"},
+                "config": {"workload": sampler_workload(args)},
                 "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0,

@@ -260,11 +260,25 @@ nvfp4_status nvfp4_f32_to_bf16(const float* x, size_t n, uint16_t* y, cudaStream
 /* ------------------------------------------------------------------------ */
 /* ReSET sampler                                                              */
 /* ------------------------------------------------------------------------ */
+/* Threshold policies (reset_params.threshold).  ReSET's own is the default;
+ * the other two are the policies the ReSET reading note compares it with
+ * (§3.1 Eq. (1) and §6.3 Table 2).  The sliding-window threshold is read as
+ * the mean of the last w token entropies including H, across step boundaries
+ * (the pages name the policy without writing it out). */
+enum {
+  RESET_THRESHOLD_RESET = 0,   /* tau = tau0 if H_step <= H_bar else H_step (SAT over HSE) */
+  RESET_THRESHOLD_FIXED = 1,   /* tau = tau0 at every position (Eq. (1))                   */
+  RESET_THRESHOLD_WINDOW = 2   /* tau = mean of the last w entropies, including H          */
+};
+
+/* A zero-initialised tail (threshold 0, top_p 0) gives ReSET without top-p. */
 typedef struct reset_params {
   float tau0;    /* global entropy threshold (nats), used in confident steps        */
   float t_low;   /* temperature below the threshold, > 0                            */
   float t_high;  /* temperature at or above the threshold, > 0                      */
   int w;         /* HSE window: positions 0..w-1 of a step use the last-w mean, 1..256 */
+  int threshold; /* RESET_THRESHOLD_*                                                */
+  float top_p;   /* nucleus mass in (0, 1); 0 or 1: no truncation                   */
 } reset_params;
 
 /* Bytes of the per-row sampler state for M rows and window w. */
@@ -285,16 +299,25 @@ size_t reset_workspace_bytes(int M, int V);
  *   H_step = mean of the last w entropies (including H) while the in-step
  *            position j < w, else the mean of the step's entropies so far;
  *   H_bar  = mean of all entropies of the row so far (including H);
- *   tau    = tau0 if H_step <= H_bar else H_step;
+ *   tau    = tau0 if H_step <= H_bar else H_step   (p->threshold RESET_THRESHOLD_RESET;
+ *            tau0 for _FIXED, the mean of the last w entropies for _WINDOW);
  *   T      = t_low if H < tau else t_high;
  *   token  = min{ i : sum_{k<=i} exp((l_k - max l)/T) > u[r] * sum_k exp((l_k - max l)/T) }.
+ * With 0 < p->top_p < 1 (reading note §6.1: the evaluation samples with
+ * top-p 0.95), the sums run over the nucleus only: token i stays iff the sum
+ * of exp((l_k - max l)/T) over the logits l_k > l_i is below top_p times the
+ * full sum -- the smallest set of most probable tokens that reaches top_p,
+ * with every logit tied to its least probable member.  The top-p path adds
+ * four launches and computes in integer masses, exp((l - max l)/T) scaled by
+ * 2^(62 - ceil(log2 V)) and rounded: deterministic, accurate to ~1e-7 of Z.
  *
  *   logits     device, [M, V] FP32, 16-byte aligned, finite
  *   M          1..64;  V 1 .. 2^24
  *   step_start device, [M] uint8 (may be NULL: no step boundaries)
  *   u          device, [M] FP32 uniforms in [0, 1)
  *   state      device, reset_state_bytes(M, p->w) bytes from reset_state_init (updated)
- *   p          HOST pointer to the parameters (copied at the call)
+ *   p          HOST pointer to the parameters (copied at the call); threshold
+ *              one of RESET_THRESHOLD_*, top_p in [0, 1] (else NVFP4_ERR_RANGE)
  *   token      device, [M] int32 (written)
  *   H_out      device, [M] FP32 entropies (written; may be NULL)
  *   T_out      device, [M] FP32 chosen temperatures (written; may be NULL)
@@ -315,9 +338,9 @@ nvfp4_status reset_sample(const float* logits, int M, int V, const uint8_t* step
  * pool and only hands out fixed input/output buffers, or a latency-critical
  * decode loop that must not call cudaMalloc because it synchronizes the device.
  *
- * The scratch (per-row counters and per-chunk partial sums) lives in a
- * 131,328-byte array that the library reserves statically on every GPU that
- * loads it, until the process exits.  Nothing is allocated: no cudaMalloc,
+ * The scratch (per-row counters, per-chunk partial sums, the top-p records
+ * and histograms) lives in a 1,217,280-byte array that the library reserves
+ * statically on every GPU that loads it, until the process exits.  Nothing is allocated: no cudaMalloc,
  * cudaFree or allocating library routine.
  *   Limit: M * ceil(V / 2048) <= 4096 (M = 8 allows V up to 1,048,576);
  *          larger calls return NVFP4_ERR_SHAPE without launching anything.

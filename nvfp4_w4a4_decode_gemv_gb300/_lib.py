@@ -23,8 +23,14 @@ _c_i = ctypes.c_int
 _c_sz = ctypes.c_size_t
 
 
+# reset_params.threshold values (RESET_THRESHOLD_* in nvfp4.h)
+THRESHOLD_RESET, THRESHOLD_FIXED, THRESHOLD_WINDOW = 0, 1, 2
+
+
 class ResetParams(ctypes.Structure):
-    _fields_ = [("tau0", ctypes.c_float), ("t_low", ctypes.c_float), ("t_high", ctypes.c_float), ("w", ctypes.c_int)]
+    """reset_params; fields left out default to 0 (ReSET threshold, no top-p)."""
+    _fields_ = [("tau0", ctypes.c_float), ("t_low", ctypes.c_float), ("t_high", ctypes.c_float), ("w", ctypes.c_int),
+                ("threshold", ctypes.c_int), ("top_p", ctypes.c_float)]
 
 
 # name -> (restype, argtypes); mirrors include/nvfp4.h

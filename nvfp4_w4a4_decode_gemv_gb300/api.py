@@ -7,7 +7,7 @@ import ctypes
 
 import torch
 
-from ._lib import ResetParams, check, lib, ptr, stream_handle
+from ._lib import THRESHOLD_FIXED, THRESHOLD_RESET, THRESHOLD_WINDOW, ResetParams, check, lib, ptr, stream_handle
 
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
@@ -266,9 +266,12 @@ def reset_sample_noalloc(logits, step_start, u, state, params: ResetParams, toke
 class ResetSampler:
     """Owns the per-row state, the workspace and the outputs of reset_sample for M rows x V logits."""
 
-    def __init__(self, M: int, V: int, tau0=0.6, t_low=0.3, t_high=1.0, w=8, device="cuda"):
+    THRESHOLDS = {"reset": THRESHOLD_RESET, "fixed": THRESHOLD_FIXED, "window": THRESHOLD_WINDOW}
+
+    def __init__(self, M: int, V: int, tau0=0.6, t_low=0.3, t_high=1.0, w=8, device="cuda", threshold="reset",
+                 top_p=1.0):
         self.M, self.V = M, V
-        self.params = ResetParams(tau0, t_low, t_high, w)
+        self.params = ResetParams(tau0, t_low, t_high, w, self.THRESHOLDS[threshold], top_p)
         self.state = torch.zeros(reset_state_bytes(M, w), dtype=torch.uint8, device=device)
         self.workspace = torch.zeros(reset_workspace_bytes(M, V), dtype=torch.uint8, device=device)
         self.token = torch.zeros(M, dtype=torch.int32, device=device)

@@ -7,8 +7,12 @@
 //            else the running mean of the step's entropies
 //   H_bar  = running mean of all entropies of the sequence
 //   tau    = tau0 if H_step <= H_bar (confident step) else H_step
+//            (or, for the two policies ReSET is compared against -- reading
+//            note §3.1 Eq. (1) and §6.3 Table 2 -- tau0 always, or the mean
+//            of the last w entropies)
 //   T      = T_low if H < tau else T_high
 //   token  = min{ i : sum_{k<=i} p_k > u * sum_k p_k },  p_k = exp((l_k - max l) / T)
+//            over the top-p nucleus when top_p is set (reading note §6.1)
 //
 // One launch: grid = M rows x NC chunks of kChunk logits.  Each CTA reduces its
 // chunk to (max m, the number of logits equal to m, sum of e^(l-m) over the
@@ -19,6 +23,15 @@
 // FP64 -- deterministic whichever CTA is last -- updates the row's state,
 // picks T, finds the chunk that holds u * Z_T and scans that one chunk with an
 // FP64 prefix sum.  It resets the row counter for the next call.
+//
+// With top-p, the last CTA stops after choosing T and four more launches of
+// M x NC CTAs follow: three levels of a radix select over the logits' order
+// keys (11, 11 and 10 bits) that find the least probable kept logit, and one
+// that sums each chunk's kept mass and samples.  Masses there are integers
+// (exp((l - max) / T) scaled by 2^(62 - ceil(log2 V)) and rounded), so every
+// level, the chunk sums and the final scan see the same numbers and the sums
+// are exact in any order: the result is deterministic, and the per-row
+// histograms can be accumulated with atomics.
 #include <math.h>
 
 #include <mutex>
@@ -47,7 +60,36 @@ struct RowState {           // per-row state, followed by `w` doubles (the entro
 struct Params {
   float tau0, t_low, t_high;
   int w;
+  int threshold;            // RESET_THRESHOLD_*
+  float top_p;              // in (0, 1) when the nucleus launches follow, else ignored
 };
+
+constexpr int kHistBins = 2048;   // per-row histogram of one radix level
+
+// Per-row record of the top-p launches.
+struct NucRow {
+  float gmax, T;                   // row maximum and chosen temperature (first launch)
+  unsigned int prefix;             // key bits chosen so far; the boundary key after level 2
+  unsigned int pad;
+  unsigned long long below;        // kept mass of the keys before the current prefix's range
+  unsigned long long target;       // ceil(top_p * Z), Z the row's total integer mass
+  unsigned long long zk;           // the nucleus's integer mass
+  unsigned long long pad2[3];
+};
+
+// Order key of a logit: ascending as the logit falls, equal for equal logits
+// (-0 and +0 included).
+__device__ __forceinline__ uint32_t nucleus_key(float l) {
+  uint32_t b = __float_as_uint(l);
+  if (b == 0x80000000u) b = 0u;
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);   // ascending with l
+  return ~ord;
+}
+
+// Integer mass of a logit at temperature 1/invT, relative to the row maximum.
+__device__ __forceinline__ unsigned long long nucleus_mass(float l, float gmax, float invT, float mscale) {
+  return __float2ull_rn(expf((l - gmax) * invT) * mscale);
+}
 
 size_t state_stride(int w) { return (sizeof(RowState) + (size_t)w * sizeof(double) + 15) & ~size_t(15); }
 
@@ -76,7 +118,8 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
                                                                const uint8_t* __restrict__ step_start,
                                                                const float* __restrict__ u, uint8_t* state,
                                                                int stride, Params p, int32_t* token, float* H_out,
-                                                               float* T_out, Part* parts, unsigned int* counters) {
+                                                               float* T_out, Part* parts, unsigned int* counters,
+                                                               NucRow* nrows, unsigned long long* hist) {
   __shared__ float s_red[5][kThreads / 32];
   __shared__ int s_last;
   __shared__ double s_scan[kThreads / 32];
@@ -212,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
       const int w = p.w;
       const bool state_ok = (st->w == w);
       if (!state_ok) atomicExch(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
-      double Hs = 0.0, Hbar = 0.0;
+      double Hs = 0.0, Hbar = 0.0, Hwin = 0.0;
       int t1 = 0, j = 0;
       if (state_ok) {
         if (st->t == 0 || (step_start && step_start[row])) {
@@ -224,20 +267,20 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
         ring[st->t % w] = H;
         t1 = st->t + 1;
         j = st->j;
-        if (j < w) {
-          if (t1 <= w) {
-            Hs = st->glob_sum / t1;             // the window is the whole history
-          } else {
-            double ws = 0.0;
-            for (int i = 0; i < w; ++i) ws += ring[i];
-            Hs = ws / w;
-          }
+        if (t1 <= w) {
+          Hwin = st->glob_sum / t1;             // the window is the whole history
         } else {
-          Hs = st->step_sum / (j + 1);
+          double ws = 0.0;
+          for (int i = 0; i < w; ++i) ws += ring[i];
+          Hwin = ws / w;
         }
+        Hs = (j < w) ? Hwin : st->step_sum / (j + 1);
         Hbar = st->glob_sum / t1;
       }
-      const double tau = (Hs <= Hbar) ? (double)p.tau0 : Hs;
+      const double tau = (p.threshold == RESET_THRESHOLD_FIXED)    ? (double)p.tau0
+                         : (p.threshold == RESET_THRESHOLD_WINDOW) ? Hwin
+                         : (Hs <= Hbar)                            ? (double)p.tau0
+                                                                   : Hs;
       const bool low = state_ok && H < tau;
       const float T = low ? p.t_low : p.t_high;
       if (state_ok) {
@@ -253,6 +296,19 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
   }
   __syncthreads();
   const float T = s_T, gmax = s_rowmax;
+  if (nrows) {
+    // top-p: hand the row over to the nucleus launches; clear its histogram.
+    unsigned long long* h = hist + (size_t)row * kHistBins;
+    for (int b = threadIdx.x; b < kHistBins; b += kThreads) h[b] = 0ull;
+    if (threadIdx.x == 0) {
+      NucRow nr = {};
+      nr.gmax = gmax;
+      nr.T = T;
+      nrows[row] = nr;
+      counters[row] = 0u;
+    }
+    return;
+  }
   const float invT = 1.0f / T;
   const bool use_low = (T == p.t_low);
   // per-chunk Z_T rescaled to the row max, then the chunk that holds the target
@@ -359,6 +415,273 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
   }
 }
 
+// ---- top-p launches ---------------------------------------------------------------
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Exclusive scan of one value per thread across the CTA; *total gets the sum.
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* s_w,
+                                                                  unsigned long long* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0ull, all = 0ull;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) base += s_w[w];
+    all += s_w[w];
+  }
+  __syncthreads();
+  *total = all;
+  return base + incl - v;
+}
+
+// One radix level of the nucleus boundary search.  The boundary key is the
+// smallest key whose inclusive mass (over keys <= it) reaches ceil(top_p * Z):
+// every logit at or above it is kept.  Level 0 bins the whole row by key bits
+// 31..21; level 1 the logits whose bits 31..21 equal the chosen digit, by bits
+// 20..10; level 2 those matching bits 31..10, by bits 9..0.  Each CTA bins its
+// chunk in shared memory and adds the non-zero bins to the row's histogram;
+// the last CTA of the row picks the digit, records it and clears the histogram.
+template <int level>
+__global__ void __launch_bounds__(kThreads) nucleus_level_kernel(const float* __restrict__ logits, int V, int NC,
+                                                                float top_p, float mscale, NucRow* nrows,
+                                                                unsigned long long* hist, unsigned int* counters) {
+  __shared__ unsigned long long s_h[kHistBins];
+  __shared__ unsigned long long s_w[kThreads / 32];
+  __shared__ int s_last, s_b;
+  const int row = blockIdx.x / NC, c = blockIdx.x % NC;
+  const float* base = logits + (size_t)row * V;
+  const int lo = c * kChunk, hi = min(V, lo + kChunk);
+  NucRow* nr = nrows + row;
+  const float gmax = __ldcg(&nr->gmax), T = __ldcg(&nr->T);
+  const float invT = 1.0f / T;
+  const unsigned int prefix = __ldcg(&nr->prefix);
+  constexpr int nb = (level == 2) ? 1024 : kHistBins;
+  for (int b = threadIdx.x; b < nb; b += kThreads) s_h[b] = 0ull;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int i = lo + threadIdx.x + k * kThreads;
+    if (i < hi) {
+      const float l = __ldcg(base + i);
+      const uint32_t key = nucleus_key(l);
+      bool match;
+      uint32_t d;
+      if constexpr (level == 0) {
+        match = true;
+        d = key >> 21;
+      } else if constexpr (level == 1) {
+        match = (key >> 21) == prefix;
+        d = (key >> 10) & 0x7FFu;
+      } else {
+        match = (key >> 10) == prefix;
+        d = key & 0x3FFu;
+      }
+      if (match) {
+        const unsigned long long m = nucleus_mass(l, gmax, invT, mscale);
+        if (m) atomicAdd(&s_h[d], m);
+      }
+    }
+  }
+  __syncthreads();
+  unsigned long long* h = hist + (size_t)row * kHistBins;
+  for (int b = threadIdx.x; b < nb; b += kThreads)
+    if (s_h[b]) atomicAdd(h + b, s_h[b]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counters + row, 1u) == (unsigned int)(NC - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- last CTA of the row: thread t owns bins [t per, (t+1) per) ----
+  constexpr int per = nb / kThreads;   // 8 or 4
+  unsigned long long hv[per];
+  unsigned long long tsum = 0ull;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    hv[j] = __ldcg(h + threadIdx.x * per + j);
+    tsum += hv[j];
+  }
+  unsigned long long total;
+  const unsigned long long excl = block_excl_scan_u64(tsum, s_w, &total);
+  unsigned long long below, target;
+  if constexpr (level == 0) {
+    // total >= 1: the maximum's mass is mscale.
+    const double t = ceil((double)top_p * (double)total);
+    target = (unsigned long long)t;
+    if (target < 1ull) target = 1ull;
+    if (target > total) target = total;
+    below = 0ull;
+  } else {
+    below = __ldcg(&nr->below);
+    target = __ldcg(&nr->target);
+  }
+  if (threadIdx.x == 0) s_b = 0x7fffffff;
+  __syncthreads();
+  {
+    unsigned long long run = below + excl;
+    int first = -1;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      if (first < 0 && run + hv[j] >= target) first = j;
+      run += hv[j];
+    }
+    if (first >= 0) atomicMin(&s_b, threadIdx.x * per + first);
+  }
+  __syncthreads();
+  int b = s_b;
+  // The masses of every level are the same integers, so the range chosen at
+  // the level before always reaches the target; the fallback is unreachable.
+  if (b == 0x7fffffff) b = nb - 1;
+  if (threadIdx.x == b / per) {
+    unsigned long long nb_below = below + excl;
+#pragma unroll
+    for (int j = 0; j < per; ++j)
+      if (j < b % per) nb_below += hv[j];
+    nr->below = nb_below;
+    if constexpr (level == 0) {
+      nr->target = target;
+      nr->prefix = (unsigned int)b;
+    } else if constexpr (level == 1) {
+      nr->prefix = (prefix << 11) | (unsigned int)b;
+    } else {
+      nr->prefix = (prefix << 10) | (unsigned int)b;
+      unsigned long long hb = 0ull;
+#pragma unroll
+      for (int j = 0; j < per; ++j)
+        if (j == b % per) hb = hv[j];
+      nr->zk = nb_below + hb;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < per; ++j) h[threadIdx.x * per + j] = 0ull;   // ready for the next level or call
+  if (threadIdx.x == 0) counters[row] = 0u;
+}
+
+// Kept mass of each chunk, then (last CTA of the row) the inverse-CDF sample
+// over the kept logits: the first chunk whose running sum passes u * Zk, and a
+// prefix scan of that one chunk -- all in exact integers.
+__global__ void __launch_bounds__(kThreads) nucleus_sample_kernel(const float* __restrict__ logits, int V, int NC,
+                                                                 const float* __restrict__ u, float mscale,
+                                                                 const NucRow* nrows, unsigned long long* csum,
+                                                                 unsigned int* counters, int32_t* token) {
+  __shared__ unsigned long long s_w[kThreads / 32];
+  __shared__ unsigned long long s_target;
+  __shared__ int s_last, s_chunk, s_tok;
+  const int row = blockIdx.x / NC, c = blockIdx.x % NC;
+  const float* base = logits + (size_t)row * V;
+  const int lo = c * kChunk, hi = min(V, lo + kChunk);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const NucRow* nr = nrows + row;
+  const float gmax = __ldcg(&nr->gmax), T = __ldcg(&nr->T);
+  const float invT = 1.0f / T;
+  const unsigned int kstar = __ldcg(&nr->prefix);
+
+  unsigned long long ms = 0ull;
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int i = lo + threadIdx.x + k * kThreads;
+    if (i < hi) {
+      const float l = __ldcg(base + i);
+      if (nucleus_key(l) <= kstar) ms += nucleus_mass(l, gmax, invT, mscale);
+    }
+  }
+  ms = warp_sum_u64(ms);
+  if (lane == 0) s_w[warp] = ms;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0ull;
+    for (int w = 0; w < kThreads / 32; ++w) t += s_w[w];
+    __stcg(csum + (size_t)row * NC + c, t);
+    __threadfence();
+    s_last = (atomicAdd(counters + row, 1u) == (unsigned int)(NC - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  const unsigned long long* crow = csum + (size_t)row * NC;
+  if (warp == 0) {
+    const int per = (NC + 31) / 32;
+    const int q0 = lane * per, q1 = min(NC, q0 + per);
+    unsigned long long mine = 0ull;
+    for (int q = q0; q < q1; ++q) mine += __ldcg(crow + q);
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+    // token = min{ i : P_i > u * Zk } with integer prefix sums P: P > u Zk <=> P > floor(u Zk)
+    unsigned long long tgt = (unsigned long long)floor((double)__ldg(u + row) * (double)total);
+    if (tgt >= total) tgt = total - 1ull;
+    const unsigned hit = __ballot_sync(0xffffffffu, q0 < q1 && incl > tgt);
+    const int owner = hit ? __ffs(hit) - 1 : (NC - 1) / per;
+    if (lane == owner) {
+      unsigned long long before = incl - mine;
+      int cstar = q1 - 1;
+      for (int q = q0; q < q1; ++q) {
+        const unsigned long long v = __ldcg(crow + q);
+        if (before + v > tgt) {
+          cstar = q;
+          break;
+        }
+        before += v;
+      }
+      s_chunk = cstar;
+      s_target = tgt - before;
+      s_tok = 0x7fffffff;
+    }
+  }
+  __syncthreads();
+  const int clo = s_chunk * kChunk;
+  const int chi = min(V, clo + kChunk);
+  const int i0 = clo + threadIdx.x * kPerThread;
+  float lv[kPerThread];
+  if ((V & 3) == 0 && i0 + kPerThread <= chi) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(base + i0));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(base + i0) + 1);
+    lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
+    lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) lv[k] = (i0 + k < chi) ? __ldcg(base + i0 + k) : 0.0f;
+  }
+  unsigned long long pre[kPerThread];
+  unsigned long long run = 0ull;
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    if (i0 + k < chi && nucleus_key(lv[k]) <= kstar) run += nucleus_mass(lv[k], gmax, invT, mscale);
+    pre[k] = run;
+  }
+  unsigned long long total;
+  const unsigned long long excl = block_excl_scan_u64(run, s_w, &total);
+  const unsigned long long target = s_target;
+  int cand = 0x7fffffff;
+#pragma unroll
+  for (int k = kPerThread - 1; k >= 0; --k) {
+    if (i0 + k < chi && excl + pre[k] > target) cand = i0 + k;
+  }
+  if (cand != 0x7fffffff) atomicMin(&s_tok, cand);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Exact sums always find the token; the fallback is unreachable.
+    token[row] = (s_tok != 0x7fffffff) ? s_tok : (chi - 1);
+    counters[row] = 0u;
+  }
+}
+
 __global__ void reset_state_init_kernel(uint8_t* state, int M, int w, int stride) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= M) return;
@@ -374,14 +697,79 @@ __global__ void reset_state_init_kernel(uint8_t* state, int M, int w, int stride
 }
 
 // Row counters first, at a fixed place for every M, so one zeroed workspace
-// serves calls of any shape.
+// serves calls of any shape.  Nothing else in the scratch needs to start
+// zeroed: the first launch clears a row's histogram before the top-p launches
+// add to it.
 constexpr size_t kCounterBytes = 256;   // kMaxRows counters
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct SampleLayout {
+  size_t parts, nrows, hist, csum, total;
+};
+
+SampleLayout sample_layout(int M, int NC) {
+  SampleLayout L;
+  L.parts = kCounterBytes;
+  L.nrows = align256(L.parts + (size_t)M * NC * sizeof(Part));
+  L.hist = align256(L.nrows + (size_t)M * sizeof(NucRow));
+  L.csum = L.hist + (size_t)M * kHistBins * sizeof(unsigned long long);
+  L.total = L.csum + (size_t)M * NC * sizeof(unsigned long long);
+  return L;
+}
+
+// 2^(62 - ceil(log2 V)): V masses of at most this value sum below 2^63.
+float mass_scale(int V) {
+  int lg = 0;
+  while ((1ll << lg) < (long long)V) ++lg;
+  return ldexpf(1.0f, 62 - lg);
+}
 
 }  // namespace
 
 nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
 bool nvfp4_internal_aligned(const void* p, size_t a);
 nvfp4_status nvfp4_internal_check_device();
+
+namespace {
+
+nvfp4_status check_params(const reset_params* p) {
+  if (!(p->t_low > 0.0f) || !(p->t_high > 0.0f) || p->w < 1 || p->w > kMaxW || !(p->tau0 == p->tau0))
+    return NVFP4_ERR_RANGE;
+  if (p->t_low == p->t_high) return NVFP4_ERR_RANGE;   // the two branches must be distinguishable
+  if (p->threshold < RESET_THRESHOLD_RESET || p->threshold > RESET_THRESHOLD_WINDOW) return NVFP4_ERR_RANGE;
+  if (!(p->top_p >= 0.0f && p->top_p <= 1.0f)) return NVFP4_ERR_RANGE;   // NaN fails too
+  return NVFP4_OK;
+}
+
+// The sampler's launches for M rows in `scratch` (laid out by sample_layout).
+nvfp4_status launch_sample(const float* logits, int M, int V, int NC, const uint8_t* step_start, const float* u,
+                           void* state, const reset_params* p, int32_t* token, float* H_out, float* T_out,
+                           uint8_t* scratch, cudaStream_t stream) {
+  const SampleLayout L = sample_layout(M, NC);
+  unsigned int* counters = reinterpret_cast<unsigned int*>(scratch);
+  Part* parts = reinterpret_cast<Part*>(scratch + L.parts);
+  NucRow* nrows = reinterpret_cast<NucRow*>(scratch + L.nrows);
+  unsigned long long* hist = reinterpret_cast<unsigned long long*>(scratch + L.hist);
+  unsigned long long* csum = reinterpret_cast<unsigned long long*>(scratch + L.csum);
+  const bool nucleus = p->top_p > 0.0f && p->top_p < 1.0f;
+  Params prm{p->tau0, p->t_low, p->t_high, p->w, p->threshold, p->top_p};
+  reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
+                                                        (int)state_stride(p->w), prm, token, H_out, T_out, parts,
+                                                        counters, nucleus ? nrows : nullptr, hist);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !nucleus) return nvfp4_internal_cuda_status(e);
+  const float mscale = mass_scale(V);
+  nucleus_level_kernel<0><<<M * NC, kThreads, 0, stream>>>(logits, V, NC, p->top_p, mscale, nrows, hist, counters);
+  nucleus_level_kernel<1><<<M * NC, kThreads, 0, stream>>>(logits, V, NC, p->top_p, mscale, nrows, hist, counters);
+  nucleus_level_kernel<2><<<M * NC, kThreads, 0, stream>>>(logits, V, NC, p->top_p, mscale, nrows, hist, counters);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
+  nucleus_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, V, NC, u, mscale, nrows, csum, counters, token);
+  return nvfp4_internal_cuda_status(cudaGetLastError());
+}
+
+}  // namespace
 
 extern "C" size_t reset_state_bytes(int M, int w) {
   if (M < 1 || M > kMaxRows || w < 1 || w > kMaxW) return 0;
@@ -399,7 +787,7 @@ extern "C" nvfp4_status reset_state_init(void* state, int M, int w, cudaStream_t
 extern "C" size_t reset_workspace_bytes(int M, int V) {
   if (M < 1 || M > kMaxRows || V < 1 || V > (1 << 24)) return 0;
   const int NC = (V + kChunk - 1) / kChunk;
-  return kCounterBytes + (size_t)M * NC * sizeof(Part);
+  return sample_layout(M, NC).total;
 }
 
 extern "C" nvfp4_status reset_sample(const float* logits, int M, int V, const uint8_t* step_start, const float* u,
@@ -408,9 +796,8 @@ extern "C" nvfp4_status reset_sample(const float* logits, int M, int V, const ui
   if (!logits || !u || !state || !p || !token || !workspace) return NVFP4_ERR_NULL;
   if (M < 1 || M > kMaxRows) return NVFP4_ERR_RANGE;
   if (V < 1 || V > (1 << 24)) return NVFP4_ERR_SHAPE;
-  if (!(p->t_low > 0.0f) || !(p->t_high > 0.0f) || p->w < 1 || p->w > kMaxW || !(p->tau0 == p->tau0))
-    return NVFP4_ERR_RANGE;
-  if (p->t_low == p->t_high) return NVFP4_ERR_RANGE;   // the two branches must be distinguishable
+  nvfp4_status ps = check_params(p);
+  if (ps != NVFP4_OK) return ps;
   if (!nvfp4_internal_aligned(logits, 16) || !nvfp4_internal_aligned(state, 16) ||
       !nvfp4_internal_aligned(workspace, 256) || !nvfp4_internal_aligned(u, 4) || !nvfp4_internal_aligned(token, 4))
     return NVFP4_ERR_ALIGN;
@@ -419,24 +806,21 @@ extern "C" nvfp4_status reset_sample(const float* logits, int M, int V, const ui
   if (workspace_bytes < reset_workspace_bytes(M, V)) return NVFP4_ERR_SHAPE;
   nvfp4_status ds = nvfp4_internal_check_device();
   if (ds != NVFP4_OK) return ds;
-  Params prm{p->tau0, p->t_low, p->t_high, p->w};
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  unsigned int* counters = reinterpret_cast<unsigned int*>(wsb);
-  Part* parts = reinterpret_cast<Part*>(wsb + kCounterBytes);
-  reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
-                                                        (int)state_stride(p->w), prm, token, H_out, T_out, parts,
-                                                        counters);
-  return nvfp4_internal_cuda_status(cudaGetLastError());
+  return launch_sample(logits, M, V, NC, step_start, u, state, p, token, H_out, T_out,
+                       static_cast<uint8_t*>(workspace), stream);
 }
 
 // ---- allocation-free variant ------------------------------------------------------
-// Same kernel, with its scratch (row counters, then per-chunk partials) in a
-// file-scope device array instead of a caller workspace, for callers that may
-// not allocate device memory.  The array is reserved on every GPU that loads
-// the library, until the process exits.
+// Same launches, with their scratch (row counters, per-chunk partials, the
+// top-p records and histograms) in a file-scope device array instead of a
+// caller workspace, for callers that may not allocate device memory.  The
+// array is reserved on every GPU that loads the library, until the process
+// exits.
 namespace {
 constexpr int kNoAllocMaxChunks = 4096;   // limit on M * ceil(V / 2048)
-constexpr size_t kNoAllocScratchBytes = kCounterBytes + (size_t)kNoAllocMaxChunks * sizeof(Part);   // 131,328
+constexpr size_t kNoAllocScratchBytes =
+    kCounterBytes + (size_t)kNoAllocMaxChunks * (sizeof(Part) + sizeof(unsigned long long)) +
+    (size_t)kMaxRows * (sizeof(NucRow) + kHistBins * sizeof(unsigned long long)) + 512;   // 1,217,280
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 uint8_t* g_noalloc_scratch_dev[kNoAllocMaxDevices] = {};
@@ -468,14 +852,14 @@ extern "C" nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, 
   if (!logits || !u || !state || !p || !token) return NVFP4_ERR_NULL;
   if (M < 1 || M > kMaxRows) return NVFP4_ERR_RANGE;
   if (V < 1 || V > (1 << 24)) return NVFP4_ERR_SHAPE;
-  if (!(p->t_low > 0.0f) || !(p->t_high > 0.0f) || p->w < 1 || p->w > kMaxW || !(p->tau0 == p->tau0))
-    return NVFP4_ERR_RANGE;
-  if (p->t_low == p->t_high) return NVFP4_ERR_RANGE;
+  nvfp4_status ps = check_params(p);
+  if (ps != NVFP4_OK) return ps;
   if (!nvfp4_internal_aligned(logits, 16) || !nvfp4_internal_aligned(state, 16) || !nvfp4_internal_aligned(u, 4) ||
       !nvfp4_internal_aligned(token, 4))
     return NVFP4_ERR_ALIGN;
   const int NC = (V + kChunk - 1) / kChunk;
   if (NC > 1024 || (long long)M * NC > kNoAllocMaxChunks) return NVFP4_ERR_SHAPE;   // beyond the static scratch
+  if (sample_layout(M, NC).total > kNoAllocScratchBytes) return NVFP4_ERR_SHAPE;
   nvfp4_status ds = nvfp4_internal_check_device();
   if (ds != NVFP4_OK) return ds;
   uint8_t* scratch = nullptr;
@@ -484,10 +868,5 @@ extern "C" nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, 
   // The array keeps the previous call's contents: clear the row counters.
   e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
   if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
-  Params prm{p->tau0, p->t_low, p->t_high, p->w};
-  reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
-                                                        (int)state_stride(p->w), prm, token, H_out, T_out,
-                                                        reinterpret_cast<Part*>(scratch + kCounterBytes),
-                                                        reinterpret_cast<unsigned int*>(scratch));
-  return nvfp4_internal_cuda_status(cudaGetLastError());
+  return launch_sample(logits, M, V, NC, step_start, u, state, p, token, H_out, T_out, scratch, stream);
 }

@@ -68,6 +68,7 @@ class DecodeStep:
         self.ws = torch.zeros(need, dtype=torch.uint8, device=dev)
         rp = reset or ResetParams(0.6, 0.3, 1.0, 8)
         self.sampler = api.ResetSampler(M, vocab, rp.tau0, rp.t_low, rp.t_high, rp.w, device=dev)
+        self.sampler.params = rp                     # threshold policy and top-p as given
         self.step_start = torch.zeros(M, dtype=torch.uint8, device=dev)
         self.u = torch.zeros(M, dtype=torch.float32, device=dev)
         self.graph = None

@@ -98,6 +98,16 @@ def test_reset_argument_errors(lib):
     assert call(8, 0, p) == 2
     assert call(8, 100, ResetParams(0.6, 0.0, 1.0, 8)) == 4           # T_low must be > 0
     assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 0)) == 4           # w >= 1
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 8, 3, 0.0)) == 4   # unknown threshold policy
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 8, -1, 0.0)) == 4
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 8, 0, 1.5)) == 4   # top_p in [0, 1]
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 8, 0, -0.1)) == 4
+    assert call(8, 100, ResetParams(0.6, 0.3, 1.0, 8, 0, float("nan"))) == 4
+    noalloc = lambda prm: lib.reset_sample_noalloc(FAKE, 8, 100, None, FAKE, FAKE, ctypes.byref(prm), FAKE, None,
+                                                   None, None)
+    assert noalloc(ResetParams(0.6, 0.3, 1.0, 8, 2, 2.0)) == 4
+    # the top-p scratch: per-row records and 2048-bin histograms, per-chunk kept sums
+    assert lib.reset_workspace_bytes(8, 151936) >= 256 + 8 * 75 * 32 + 8 * (64 + 2048 * 8) + 8 * 75 * 8
     assert lib.reset_state_bytes(8, 8) > 0 and lib.reset_state_bytes(8, 0) == 0
     assert lib.reset_workspace_bytes(8, 151936) > 0
     assert lib.nvfp4_bf16_gemv(FAKE, 9, FAKE, 10, 64, FAKE, None) == 4

@@ -5,7 +5,10 @@ comparison is inside its 1e-4 guard band (then either T is accepted); the
 token equal to the oracle's inverse-CDF sample at the GPU's T, up to the
 tokens whose cumulative sum lies within 4e-6 * Z of u * Z (the GPU sums exp
 values of FP32 accuracy -- 2 ulp per exp, FP32 chunk sums of <= 2048 terms --
-so its partial sums carry a relative error below that bound).
+so its partial sums carry a relative error below that bound).  The same for
+the fixed and sliding-window threshold policies and for top-p, where the
+token must also lie in the oracle's nucleus (or, when the nucleus boundary is
+within 1e-6 * Z, in the nucleus with the boundary group on the other side).
 """
 import numpy as np
 import pytest
@@ -18,16 +21,33 @@ from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams
 pytestmark = pytest.mark.gpu
 
 TOKEN_REL = 4e-6
+# top-p: the kernels' integer masses carry the FP32 exp's error (a few ulp) and
+# one rounding to 2^-(62 - ceil(log2 V)) of the maximum's mass each, so a
+# boundary logit group within 1e-6 * Z of top_p * Z may fall either way.
+NUCLEUS_REL = 1e-6
 
 
 def _f32(v):
     return float(np.float32(v))
 
 
-def _run(M, V, steps, sigmas, starts, us, tau0=0.6, t_low=0.3, t_high=1.0, w=8, seed0=4, pass_starts=True):
-    p_gpu = dict(tau0=tau0, t_low=t_low, t_high=t_high, w=w)
+def _token_ok(ln, T, u, tok, top_p):
+    """The token is the oracle's inverse-CDF sample at T up to TOKEN_REL * Z,
+    over one of the nuclei the oracle's guard band allows (all tokens when
+    top_p = 1), and is a member of that nucleus."""
+    for keep in R.nucleus_candidates(ln, T, top_p, NUCLEUS_REL):
+        lo, hi = R.acceptable_tokens(ln, T, u, TOKEN_REL, keep=keep)
+        if lo <= tok <= hi and keep[tok]:
+            return True
+    return False
+
+
+def _run(M, V, steps, sigmas, starts, us, tau0=0.6, t_low=0.3, t_high=1.0, w=8, seed0=4, pass_starts=True,
+         threshold="reset", top_p=1.0):
+    p_gpu = dict(tau0=tau0, t_low=t_low, t_high=t_high, w=w, threshold=threshold, top_p=top_p)
     sampler = api.ResetSampler(M, V, **p_gpu)
-    p = R.ResetParams(tau0=_f32(tau0), t_low=_f32(t_low), t_high=_f32(t_high), w=w)
+    p = R.ResetParams(tau0=_f32(tau0), t_low=_f32(t_low), t_high=_f32(t_high), w=w, threshold=threshold,
+                      top_p=_f32(top_p))
     states = [R.RowState(w=w) for _ in range(M)]
     n_amb = 0
     for t in range(steps):
@@ -47,8 +67,7 @@ def _run(M, V, steps, sigmas, starts, us, tau0=0.6, t_low=0.3, t_high=1.0, w=8, 
                 assert T[r] in (np.float32(t_low), np.float32(t_high))
             else:
                 assert T[r] == np.float32(res.T), (t, r, T[r], res)
-            lo, hi = R.acceptable_tokens(ln[r], float(T[r]), float(us[t, r]), TOKEN_REL)
-            assert lo <= tok[r] <= hi, (t, r, tok[r], lo, hi)
+            assert _token_ok(ln[r], float(T[r]), float(us[t, r]), int(tok[r]), p.top_p), (t, r, tok[r])
     assert api.device_status() == 0
     return n_amb
 
@@ -125,4 +144,88 @@ def test_window_mismatch_is_reported_without_fault():
     sampler(torch.zeros((M, V)).cuda(), None, torch.zeros(M).cuda())
     torch.cuda.synchronize()
     assert api.device_status() == 2
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("threshold", ["fixed", "window"])
+def test_threshold_policies_sequence(threshold):
+    M, V, steps = 8, 5000, 40
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=2), synth.reset_boundaries(steps, M, p=0.15, seed=2),
+         synth.reset_uniforms(steps, M, seed=2), w=3, threshold=threshold)
+
+
+def test_top_p_full_size_prefix():
+    """Top-p 0.95 (the pages' evaluation setting) on M = 8 rows x V = 151936
+    logits, sigma from {1, 3, 8}: nuclei from one token to most of the
+    vocabulary."""
+    M, V, steps = 8, synth.LM_HEAD_VOCAB, 10
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=3), synth.reset_boundaries(steps, M, p=1 / 4, seed=3),
+         synth.reset_uniforms(steps, M, seed=3), top_p=0.95)
+
+
+@pytest.mark.parametrize("top_p,threshold", [(0.5, "reset"), (0.9, "window"), (0.05, "fixed")])
+@pytest.mark.parametrize("V", [1, 3, 2047, 2049, 6001])
+def test_top_p_ragged_vocab(V, top_p, threshold):
+    M, steps = 3, 6
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=V), synth.reset_boundaries(steps, M, p=0.3, seed=V),
+         synth.reset_uniforms(steps, M, seed=V), top_p=top_p, threshold=threshold)
+
+
+def _tie_logits(M, V, seed):
+    """Integer logits in [-3, 1] (large tie groups), one -0.0 per row."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(-3, 2, (M, V), generator=g).float()
+    x[:, 7] = -0.0
+    return x
+
+
+@pytest.mark.parametrize("top_p", [0.3, 0.7, 0.95])
+def test_top_p_keeps_whole_tie_groups(top_p):
+    M, V = 4, 9000
+    sampler = api.ResetSampler(M, V, top_p=top_p)
+    p = R.ResetParams(top_p=_f32(top_p))
+    us = synth.reset_uniforms(8, M, seed=11)
+    for t in range(8):
+        logits = _tie_logits(M, V, seed=100 + t)
+        tok, H, T = sampler(logits.cuda(), None, torch.from_numpy(us[t]).cuda())
+        torch.cuda.synchronize()
+        ln = logits.numpy().astype(np.float64)
+        for r in range(M):
+            assert _token_ok(ln[r], float(T.cpu()[r]), float(us[t, r]), int(tok.cpu()[r]), p.top_p)
+    assert api.device_status() == 0
+
+
+def test_top_p_single_token_nucleus_and_u_extremes():
+    """One dominant logit: at top_p <= its probability only it is kept, for
+    every u, including u = 0 and the largest float below 1."""
+    M, V = 3, 4096
+    logits = torch.zeros((M, V))
+    logits[:, 1234] = 12.0
+    for u0 in (0.0, float(np.nextafter(np.float32(1.0), np.float32(0.0)))):
+        sampler = api.ResetSampler(M, V, top_p=0.5)
+        tok, _, _ = sampler(logits.cuda(), None, torch.full((M,), u0).cuda())
+        torch.cuda.synchronize()
+        assert tok.tolist() == [1234] * M
+
+
+def test_top_p_repeatable_and_noalloc_identical():
+    """The top-p path is deterministic (integer masses), and the allocation-free
+    entry point gives the same tokens."""
+    M, V, steps = 8, 20000, 6
+    sig, us = synth.reset_sigmas(steps, seed=5), synth.reset_uniforms(steps, M, seed=5)
+    runs = []
+    for noalloc in (False, False, True):
+        sampler = api.ResetSampler(M, V, top_p=0.95, threshold="window")
+        toks = []
+        for t in range(steps):
+            logits = synth.reset_logits(t, M, V, float(sig[t])).cuda()
+            u = torch.from_numpy(us[t]).cuda()
+            if noalloc:
+                api.reset_sample_noalloc(logits, None, u, sampler.state, sampler.params, sampler.token, sampler.H,
+                                         sampler.T)
+            else:
+                sampler(logits, None, u)
+            toks.append(sampler.token.cpu().numpy().copy())
+        runs.append(np.stack(toks))
+    assert np.array_equal(runs[0], runs[1]) and np.array_equal(runs[0], runs[2])
     assert api.device_status() == 0
