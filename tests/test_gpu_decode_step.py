@@ -187,3 +187,38 @@ def test_decode_step_graph_replay_matches_eager():
         g.replay()
         assert all(torch.equal(a, b) for a, b in zip(first, _buffers(st)))
     assert api.device_status() == 0
+
+
+def test_decode_step_top_p_in_graph():
+    """The decode step with the sliding-window threshold and top-p 0.95: the
+    four top-p launches are captured with the rest of the step, a replay gives
+    the eager tokens, and the tokens lie in the oracle's nucleus of the GPU's
+    logits (lm_head only: no decoder layers)."""
+    from nvfp4_w4a4_decode_gemv_gb300._lib import THRESHOLD_WINDOW, ResetParams
+    rp = ResetParams(0.6, 0.3, 1.0, 8, THRESHOLD_WINDOW, 0.95)
+    st = DecodeStep(M=8, layers=0, seed=4, reset=rp)
+    st.h_in.copy_(synth.activations(8, st.hidden, seed=14).float().cuda())
+    st.u.copy_(torch.from_numpy(synth.reset_uniforms(1, 8, seed=9)[0]).cuda())
+    st.run()
+    tok, H, T = (to_np(t).copy() for t in st.run())
+    g = st.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    # every call sees the same logits, so the window holds copies of one H and
+    # its mean is H (sums of up to 8 copies of an FP32 value are exact in FP64):
+    # H < tau fails and T = T_high at every call, eager or replayed
+    assert np.all(T == np.float32(1.0)) and np.all(to_np(st.sampler.T) == np.float32(1.0))
+    assert np.array_equal(to_np(st.sampler.token), tok)
+    logits = to_np(st.logits)
+    u = to_np(st.u)
+    for r in range(8):
+        ln = logits[r].astype(np.float64)
+        assert abs(H[r] - R.token_entropy(ln)) <= 1e-4 * abs(R.token_entropy(ln))
+        ok = False
+        for keep in R.nucleus_candidates(ln, 1.0, float(np.float32(0.95)), 1e-6):
+            lo, hi = R.acceptable_tokens(ln, 1.0, float(u[r]), 4e-6, keep=keep)
+            ok |= bool(lo <= tok[r] <= hi and keep[tok[r]])
+        assert ok, r
+    assert api.device_status() == 0
+    del st, g
+    torch.cuda.empty_cache()
