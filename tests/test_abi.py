@@ -150,3 +150,32 @@ def test_bf16_gemv_tc_argument_errors(lib):
     assert g(FAKE, 1, FAKE, 10, 64, FAKE, None, need, None) == 1
     assert g(FAKE + 8, 1, FAKE, 10, 64, FAKE, FAKE, need, None) == 3         # x alignment
     assert g(FAKE, 1, FAKE, 10, 64, FAKE, FAKE + 16, need, None) == 3        # workspace alignment
+
+
+def test_reset_params_layout_matches_header(tmp_path):
+    """The ctypes mirror of reset_params has the C struct's size, field offsets
+    and RESET_THRESHOLD_* values (compiled against include/nvfp4.h by gcc)."""
+    import shutil
+    import subprocess
+    from nvfp4_w4a4_decode_gemv_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = next((d for d in ("/usr/local/cuda/include", os.path.join(os.environ.get("CUDA_HOME", ""), "include"))
+                     if os.path.exists(os.path.join(d, "cuda_runtime_api.h"))), None)
+    if not cc or not cuda_inc:
+        pytest.skip("needs a C compiler and the CUDA headers")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "nvfp4.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu %zu %zu %zu %d %d %d\\n", sizeof(reset_params),\n'
+        "         offsetof(reset_params, tau0), offsetof(reset_params, t_low), offsetof(reset_params, t_high),\n"
+        "         offsetof(reset_params, w), offsetof(reset_params, threshold), offsetof(reset_params, top_p),\n"
+        "         RESET_THRESHOLD_RESET, RESET_THRESHOLD_FIXED, RESET_THRESHOLD_WINDOW);\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = _lib.ResetParams
+    want = [ctypes.sizeof(P)] + [getattr(P, f).offset for f in ("tau0", "t_low", "t_high", "w", "threshold", "top_p")]
+    want += [_lib.THRESHOLD_RESET, _lib.THRESHOLD_FIXED, _lib.THRESHOLD_WINDOW]
+    assert got == want
