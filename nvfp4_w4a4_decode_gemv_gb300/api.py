@@ -264,7 +264,11 @@ def reset_sample_noalloc(logits, step_start, u, state, params: ResetParams, toke
 
 
 class ResetSampler:
-    """Owns the per-row state, the workspace and the outputs of reset_sample for M rows x V logits."""
+    """Owns the per-row state, the workspace and the outputs of reset_sample for M rows x V logits.
+
+    threshold: "reset" (ReSET's step-aware threshold), "fixed" (tau0 at every
+    position) or "window" (the mean of the last w entropies); top_p in (0, 1)
+    samples from the nucleus only (1 keeps every token)."""
 
     THRESHOLDS = {"reset": THRESHOLD_RESET, "fixed": THRESHOLD_FIXED, "window": THRESHOLD_WINDOW}
 
