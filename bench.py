@@ -311,7 +311,7 @@ def run_ours(args, world, rank):
                        "gemv_gbs": round(sum(c["gemv_bytes"] for c in groups[M]) / (gemv_ms[M] * 1e-3) / 1e9, 1)}
              for M in order}
     peak, peak_kind = measured_peaks()
-    cuda_cores = args.weights == "rowmajor" and os.environ.get("NVFP4_GEMV_PATH", "tc").startswith("c")
+    cuda_cores = False                # the CUDA-core kernel is a test cross-check, not a bench path
     # per call: the quantizer and the GEMV (+ the activation-record kernel on the CUDA-core path)
     launches_per_call = 3 if cuda_cores else 2
     gemv_name = ("nvfp4_gemv_smallm_packed (tensor-core GEMV kernel)" if args.weights == "packed" else

@@ -62,11 +62,17 @@ const char* nvfp4_last_cuda_error(void);
 int nvfp4_version(void);
 
 /*
- * Reads and clears the device error word of the current device.  A kernel sets
- * it (non-zero) when one of its bounded waits gave up: bit 0, a wait on an
- * mbarrier; bit 2, a GEMV CTA's wait for another CTA's partial sum.  The
- * kernel then returned early and its outputs are incomplete.  Synchronous
- * (it copies 4 bytes from the device); not for use inside stream capture.
+ * Reads and clears the device error bits of the current device (the OR of
+ * every error any kernel recorded since the last read).  A kernel sets a bit
+ * when one of its bounded waits gave up, then returns early with incomplete
+ * outputs:
+ *   bit 0 (1)  a wait on an mbarrier (a TMA copy or an MMA that never completed);
+ *   bit 1 (2)  reset_sample called with a state built for a smaller window;
+ *   bit 2 (4)  a GEMV CTA's wait for another CTA's partial sum.  After this
+ *              error the GEMV workspace may hold a partial sum published after
+ *              the wait gave up: zero the workspace again before its next use.
+ * Synchronous (it copies a few bytes from the device); not for use inside
+ * stream capture.
  */
 nvfp4_status nvfp4_device_status(unsigned int* code);
 
@@ -138,9 +144,17 @@ nvfp4_status nvfp4_silu_mul_quantize(const float* gate_up, int rows, int I, uint
  *   workspace    device scratch of at least nvfp4_gemv_workspace_bytes(M, N, K)
  *                bytes, 256-byte aligned, ZEROED ONCE before its first use
  *                (cudaMemset); every call leaves it ready for the next one,
- *                whatever the shape of the next call.
+ *                whatever the shape of the next call -- unless the call
+ *                recorded device error bit 2 (nvfp4_device_status): zero it
+ *                again then.
  *                Calls that overlap in time on the GPU must use different
  *                workspaces.
+ * Co-residency: the kernel's CTAs (two per SM, one grid of up to 2 x the SM
+ * count) exchange partial sums and wait for one another, so all of them must
+ * be resident at once.  That holds when the call has the GPU to itself or
+ * shares it with other kernels that finish; under MPS limits or green contexts
+ * that cap the SMs a context may use, or beside a kernel that never ends, a
+ * CTA's wait can run out: the call then records bit 2 and its y is wrong.
  * Alignment: xq, wq, xs, ws 16-byte aligned; y 16-byte aligned.
  */
 size_t nvfp4_gemv_workspace_bytes(int M, int N, int K);
@@ -149,6 +163,34 @@ nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float
                                const uint8_t* wq, const uint8_t* ws, const float* wg, int N, int K,
                                float* y, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+
+/*
+ * nvfp4_gemv_smallm computed by a second, independent kernel on the CUDA cores:
+ * the pages' own design (ReSET project page, "Core contribution -- the nvfp4r
+ * CUDA-core kernel": each weight tile streamed once for all M tokens (C1),
+ * several FP32 accumulator chains per thread (C2), dequantization in
+ * registers (C3)), with each 16-element block summed exactly in integers.
+ * Same arguments, result tolerance, workspace and errors as
+ * nvfp4_gemv_smallm; not the fast path (the tensor-core kernel is), kept so
+ * that two implementations can be checked against each other.
+ */
+nvfp4_status nvfp4_gemv_smallm_cudacore(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                                        const uint8_t* wq, const uint8_t* ws, const float* wg, int N, int K,
+                                        float* y, void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/*
+ * Test hook for the tensor-core GEMV's bounded wait (no counterpart in the
+ * pages).  For every later tensor-core GEMV launch in the process:
+ * flag_spin_limit = how many times a CTA polls another CTA's partial sum
+ * before giving up (0 = the default, about 2^24 polls), and drop_records != 0
+ * makes every CTA skip publishing its partial sums, so that the CTA finishing
+ * a split tile waits until the limit, records device error bit 2 and writes a
+ * wrong y.  Lets a test make the wait run out without any fault or hang.
+ * Call nvfp4_test_gemv_fault(0, 0) to return to normal operation; not
+ * thread-safe against concurrent GEMV calls.
+ */
+void nvfp4_test_gemv_fault(unsigned int flag_spin_limit, int drop_records);
 
 /*
  * Packed weights.  The pages quantize the weights offline, from the BF16

@@ -44,6 +44,9 @@ SIGNATURES = {
     "nvfp4_silu_mul_quantize": (_c_i, [_c_p, _c_i, _c_i, _c_p, _c_p, _c_p, _c_p]),
     "nvfp4_gemv_workspace_bytes": (_c_sz, [_c_i, _c_i, _c_i]),
     "nvfp4_gemv_smallm": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
+    "nvfp4_gemv_smallm_cudacore": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz,
+                                          _c_p]),
+    "nvfp4_test_gemv_fault": (None, [ctypes.c_uint, _c_i]),
     "nvfp4_packed_weight_bytes": (_c_sz, [_c_i, _c_i]),
     "nvfp4_pack_weights": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_sz, _c_p]),
     "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),

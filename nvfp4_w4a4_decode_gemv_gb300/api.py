@@ -4,6 +4,7 @@ workspaces with torch, then one call into libnvfp4_gb300.so on the current
 stream.  Every computation runs in the library's CUDA kernels.
 """
 import ctypes
+import weakref
 
 import torch
 
@@ -11,6 +12,7 @@ from ._lib import THRESHOLD_FIXED, THRESHOLD_RESET, THRESHOLD_WINDOW, ResetParam
 
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
+    "nvfp4_gemv_smallm_cudacore", "DEVERR_FLAG_TIMEOUT",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
     "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
     "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
@@ -88,12 +90,21 @@ def nvfp4_gemv_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(lib().nvfp4_gemv_workspace_bytes(M, N, K))
 
 
+# Device error bit of a GEMV CTA whose wait for another CTA's partial sum gave up
+# (nvfp4_device_status); the GEMV workspaces must be zeroed again after it.
+DEVERR_FLAG_TIMEOUT = 4
+
+_live_workspaces = weakref.WeakSet()
+
+
 class GemvWorkspace:
-    """A zero-initialised GEMV workspace that grows on demand (re-zeroed when it grows)."""
+    """A zero-initialised GEMV workspace that grows on demand (re-zeroed when it
+    grows, and by device_status() after a GEMV wait gave up)."""
 
     def __init__(self, device="cuda"):
         self.device = device
         self.buf = torch.zeros(0, dtype=torch.uint8, device=device)
+        _live_workspaces.add(self)
 
     def get(self, M, N, K) -> torch.Tensor:
         need = nvfp4_gemv_workspace_bytes(M, N, K)
@@ -102,6 +113,9 @@ class GemvWorkspace:
         if self.buf.numel() < need:
             self.buf = torch.zeros(need + 4096, dtype=torch.uint8, device=self.device)
         return self.buf
+
+    def rezero(self) -> None:
+        self.buf.zero_()
 
 
 _default_ws: dict = {}
@@ -125,6 +139,20 @@ def nvfp4_gemv_smallm(x: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor | None = N
     check(lib().nvfp4_gemv_smallm(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.codes), ptr(w.scales),
                                   ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(), stream_handle(stream)),
           "nvfp4_gemv_smallm")
+    return y
+
+
+def nvfp4_gemv_smallm_cudacore(x: NVFP4Tensor, w: NVFP4Tensor, y: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """nvfp4_gemv_smallm on the library's second, CUDA-core kernel (a cross-check, not the fast path)."""
+    M, N, K = x.rows, w.rows, x.K
+    if w.K != K:
+        raise ValueError("x and w disagree on K")
+    y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.codes.device)
+    ws = workspace if workspace is not None else _ws_for(x.codes.device).get(M, N, K)
+    check(lib().nvfp4_gemv_smallm_cudacore(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.codes),
+                                           ptr(w.scales), ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(),
+                                           stream_handle(stream)), "nvfp4_gemv_smallm_cudacore")
     return y
 
 
@@ -290,7 +318,15 @@ class ResetSampler:
 
 
 def device_status() -> int:
-    """Reads and clears the library's device error words (synchronous)."""
+    """Reads and clears the library's device error bits (synchronous).  After a
+    GEMV wait gave up (DEVERR_FLAG_TIMEOUT), a late partial sum may sit in a
+    workspace: every GemvWorkspace of this process is zeroed again; a caller's
+    own workspace tensors must be zeroed by the caller."""
     code = ctypes.c_uint(0)
     check(lib().nvfp4_device_status(ctypes.byref(code)), "nvfp4_device_status")
+    if code.value & DEVERR_FLAG_TIMEOUT:
+        torch.cuda.synchronize()
+        for ws in list(_live_workspaces):
+            ws.rezero()
+        torch.cuda.synchronize()
     return int(code.value)

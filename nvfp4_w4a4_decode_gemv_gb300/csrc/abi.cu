@@ -4,6 +4,7 @@
 #include "common.cuh"
 
 cudaError_t nvfp4_internal_read_error_gemv(unsigned int* out);
+cudaError_t nvfp4_internal_read_error_gemv_tc(unsigned int* out);
 cudaError_t nvfp4_internal_read_error_reset(unsigned int* out);
 
 namespace {
@@ -58,6 +59,7 @@ extern "C" nvfp4_status nvfp4_device_status(unsigned int* code) {
   if (!code) return NVFP4_ERR_NULL;
   *code = 0;
   cudaError_t e = nvfp4_internal_read_error_gemv(code);
+  if (e == cudaSuccess) e = nvfp4_internal_read_error_gemv_tc(code);
   if (e == cudaSuccess) e = nvfp4_internal_read_error_reset(code);
   return nvfp4_internal_cuda_status(e);
 }

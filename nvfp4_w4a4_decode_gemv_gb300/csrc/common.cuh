@@ -11,13 +11,17 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/nvfp4.h"
 
 #define NVFP4_DEVINL __device__ __forceinline__
 
 // Device-side error word, one per translation unit (internal linkage, so no
-// relocatable device code is needed).  Non-zero after a kernel of that unit
-// gave up on a bounded wait; nvfp4_device_status() reads and clears them all.
+// relocatable device code is needed).  A bit set: kernels OR their error bits
+// into it, so one error never erases another.  Every unit whose kernels set it
+// defines a reader (NVFP4_DEFINE_ERROR_READER), and nvfp4_device_status()
+// reads and clears them all.
 static __device__ unsigned int g_nvfp4_device_error;
 
 // Defines a host function that ORs this unit's error word into *out and
@@ -30,6 +34,30 @@ static __device__ unsigned int g_nvfp4_device_error;
     *out |= v;                                                                         \
     return e;                                                                          \
   }
+
+// Host: one positive int per device, computed by `compute(dev)` on the first
+// call made with that device current.  Thread-safe: racing first calls compute
+// the same value (and `compute` only sets attributes that are idempotent).
+// A failed computation returns its error through *err and caches nothing.
+struct PerDeviceInt {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<int> v[kMaxDevices] = {};
+  template <class F>
+  int get(F compute, cudaError_t* err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
+    if (e != cudaSuccess) {
+      *err = e;
+      return 0;
+    }
+    int x = v[dev].load(std::memory_order_acquire);
+    if (x > 0) return x;
+    x = compute(dev, err);
+    if (x > 0) v[dev].store(x, std::memory_order_release);
+    return x;
+  }
+};
 
 enum : unsigned int {
   NVFP4_DEVERR_NONE = 0,
@@ -91,7 +119,7 @@ NVFP4_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kMbarSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
-  atomicExch(&g_nvfp4_device_error, NVFP4_DEVERR_MBAR_TIMEOUT);
+  atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_MBAR_TIMEOUT);
   return false;
 }
 

@@ -427,18 +427,23 @@ WsLayout ws_layout(int M, int N, int K) {
 
 template <int M, int TR, int R, int S>
 cudaError_t launch_variant(const void* wq, const void* wsc, GemvArgs a, cudaStream_t stream, int grid_cap) {
-  static int occ = -1;
+  static PerDeviceInt occ_cache;
   constexpr int WC = TR / (32 * R);
   constexpr size_t smem = gemv_smem_bytes<M, TR, R, S>();
   auto kern = gemv_kernel<M, TR, R, S>;
-  if (occ < 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  cudaError_t err = cudaSuccess;
+  const int occ = occ_cache.get([](int, cudaError_t* e_out) -> int {
+    auto k = gemv_kernel<M, TR, R, S>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 32 * (WC + 1), smem);
-    if (e != cudaSuccess) return e;
-    occ = o < 1 ? 1 : (o > kMaxCtasPerSm ? kMaxCtasPerSm : o);
-  }
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, 32 * (WC + 1), smem);
+    if (e != cudaSuccess) {
+      *e_out = e;
+      return 0;
+    }
+    return o < 1 ? 1 : (o > kMaxCtasPerSm ? kMaxCtasPerSm : o);
+  }, &err);
+  if (occ == 0) return err;
   CUtensorMap tc, ts;
   if (!encode_2d(&tc, wq, (uint64_t)a.K / 2, (uint64_t)a.N, 128, TR, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&ts, wsc, (uint64_t)a.K / 16, (uint64_t)a.N, 16, TR, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -480,6 +485,18 @@ int env_int(const char* name, int dflt) {
   return v ? atoi(v) : dflt;
 }
 
+// Tuning knobs, read once per process: a grid cap for either GEMV kernel
+// (NVFP4_GEMV_GRID, 0 = none) and the CUDA-core kernel's tile variant
+// (NVFP4_GEMV_VARIANT).
+int gemv_grid_cap() {
+  static const int v = env_int("NVFP4_GEMV_GRID", 0);
+  return v;
+}
+int gemv_variant() {
+  static const int v = env_int("NVFP4_GEMV_VARIANT", 0);
+  return v;
+}
+
 }  // namespace
 
 nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
@@ -502,24 +519,18 @@ bool nvfp4_internal_encode_2d(CUtensorMap* map, const void* base, uint64_t inner
 
 int nvfp4_internal_device_sms() { return device_sms(); }
 
-namespace {
-// GEMV path: "tc" = tensor cores (gemv_tc.cu), "cc" = CUDA cores (this file).
-bool use_tensor_cores(int M) {
-  (void)M;
-  const char* v = getenv("NVFP4_GEMV_PATH");
-  if (v && v[0] == 'c') return false;
-  return true;
-}
-}  // namespace
+void nvfp4_internal_test_gemv_fault(unsigned int flag_spin_limit, int drop_records);
 
 extern "C" size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
   return ws_layout(M, N, K).total;
 }
 
-extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
-                                          const uint8_t* wq, const uint8_t* ws, const float* wg, int N, int K,
-                                          float* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+namespace {
+// Checks shared by the two row-major entry points.
+nvfp4_status check_gemv_args(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
+                             const uint8_t* ws, const float* wg, int N, int K, float* y, void* workspace,
+                             size_t workspace_bytes) {
   if (!xq || !xs || !xg || !wq || !ws || !wg || !y || !workspace) return NVFP4_ERR_NULL;
   if (M < 1 || M > kMaxM) return NVFP4_ERR_RANGE;
   if (N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return NVFP4_ERR_SHAPE;
@@ -527,17 +538,32 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
       !nvfp4_internal_aligned(ws, 16) || !nvfp4_internal_aligned(y, 16) || !nvfp4_internal_aligned(xg, 4) ||
       !nvfp4_internal_aligned(wg, 4) || !nvfp4_internal_aligned(workspace, 256))
     return NVFP4_ERR_ALIGN;
-  const WsLayout wl = ws_layout(M, N, K);
-  if (workspace_bytes < wl.total) return NVFP4_ERR_SHAPE;
-  nvfp4_status ds = nvfp4_internal_check_device();
-  if (ds != NVFP4_OK) return ds;
+  if (workspace_bytes < ws_layout(M, N, K).total) return NVFP4_ERR_SHAPE;
+  return nvfp4_internal_check_device();
+}
+}  // namespace
 
+extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                                          const uint8_t* wq, const uint8_t* ws, const float* wg, int N, int K,
+                                          float* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const nvfp4_status st = check_gemv_args(xq, xs, xg, M, wq, ws, wg, N, K, y, workspace, workspace_bytes);
+  if (st != NVFP4_OK) return st;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  if (use_tensor_cores(M)) {
-    return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
-        xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
-        env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
-  }
+  return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
+      xq, xs, xg, M, wq, ws, nullptr, wg, N, K, y,
+      reinterpret_cast<unsigned int*>(wsb + ws_layout(M, N, K).tcrec), gemv_grid_cap(), kMaxCtasPerSm, stream));
+}
+
+// The CUDA-core kernel of this file: the pages' own design point, kept as an
+// independent second implementation that the tests compare against.
+extern "C" nvfp4_status nvfp4_gemv_smallm_cudacore(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                                                   const uint8_t* wq, const uint8_t* ws, const float* wg, int N,
+                                                   int K, float* y, void* workspace, size_t workspace_bytes,
+                                                   cudaStream_t stream) {
+  const nvfp4_status st = check_gemv_args(xq, xs, xg, M, wq, ws, wg, N, K, y, workspace, workspace_bytes);
+  if (st != NVFP4_OK) return st;
+  const WsLayout wl = ws_layout(M, N, K);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
   GemvArgs a;
   a.xrec = wsb + wl.xrec;
   a.xg = xg;
@@ -565,8 +591,8 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
   cudaError_t e = cudaLaunchKernelEx(&pcfg, xrec_kernel, xq, xs, M, K, reinterpret_cast<uint4*>(wsb + wl.xrec));
   if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
 
-  const int variant = env_int("NVFP4_GEMV_VARIANT", 0);
-  const int grid_cap = env_int("NVFP4_GEMV_GRID", 0);
+  const int variant = gemv_variant();
+  const int grid_cap = gemv_grid_cap();
   switch (M) {
     case 1: e = launch_m<1>(variant, wq, ws, a, stream, grid_cap); break;
     case 2: e = launch_m<2>(variant, wq, ws, a, stream, grid_cap); break;
@@ -578,6 +604,10 @@ extern "C" nvfp4_status nvfp4_gemv_smallm(const uint8_t* xq, const uint8_t* xs, 
     default: e = launch_m<8>(variant, wq, ws, a, stream, grid_cap); break;
   }
   return nvfp4_internal_cuda_status(e);
+}
+
+extern "C" void nvfp4_test_gemv_fault(unsigned int flag_spin_limit, int drop_records) {
+  nvfp4_internal_test_gemv_fault(flag_spin_limit, drop_records);
 }
 
 extern "C" size_t nvfp4_packed_weight_bytes(int N, int K) {
@@ -614,7 +644,7 @@ extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
       xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
-      env_int("NVFP4_GEMV_GRID", 0), kMaxCtasPerSm, stream));
+      gemv_grid_cap(), kMaxCtasPerSm, stream));
 }
 
 // BF16 GEMV on the tensor-core kernel: it needs only the records region of a

@@ -47,7 +47,11 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
+
+NVFP4_DEFINE_ERROR_READER(nvfp4_internal_read_error_gemv_tc)
 
 namespace {
 
@@ -91,6 +95,8 @@ struct TcArgs {
   unsigned int* records;         // [G][M][128] words: a CTA's partial sums of its first tile; zero between calls
   int M, N, K, C, RT;
   long long U;                   // units = RT * C, numbered tile-major
+  uint32_t flag_spins;           // polls of a record before the wait gives up (kFlagSpinLimit)
+  int drop_records;              // test hook: non-zero = publish no record (the first contributor's wait runs out)
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -194,13 +200,17 @@ NVFP4_DEVINL unsigned int* record(const TcArgs& a, long long q, int row) {
 // A contributor other than the first: its partial sums, encoded.
 template <int M>
 NVFP4_DEVINL void publish_record(const TcArgs& a, int row, const float (&acc)[kNT]) {
+  if (a.drop_records) return;
   unsigned int* rec = record<M>(a, blockIdx.x, row);
 #pragma unroll
   for (int m = 0; m < M; ++m) st_relaxed_gpu(rec + m * kTR, ~__float_as_uint(acc[m]));
 }
 
 // The records of contributors q0 .. q0+3 (those <= last), once every word is
-// written (bounded wait); each word read is reset to zero.
+// written (bounded wait); every live word is then reset to zero.  A wait that
+// gives up sets device error bit 2 and zeroes the words all the same, so a
+// record published late is the only thing it can leave behind (the caller
+// re-zeroes the workspace after that error).
 template <int M>
 NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, int row, float (&v)[4][M]) {
   unsigned int w[4][M];
@@ -222,7 +232,7 @@ NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, in
       }
     }
     if (ready) break;
-    if (++spins >= kFlagSpinLimit) {
+    if (++spins >= a.flag_spins) {
       atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
       break;
     }
@@ -526,6 +536,57 @@ constexpr size_t tc_smem_bytes() {
   return (size_t)S * kSlot + 1024 + (3 * S + 5) * sizeof(uint64_t) + 16;
 }
 
+struct TcMaps {
+  CUtensorMap w_codes, w_scales, x_codes, x_scales;
+};
+
+// Test hook (nvfp4_test_gemv_fault): the record wait's poll limit and whether
+// records are dropped, for every later launch in the process.
+std::atomic<uint32_t> g_test_flag_spins{0};     // 0: kFlagSpinLimit
+std::atomic<int> g_test_drop_records{0};
+
+// Ring depth, read once per process (tuning knob NVFP4_GEMV_TC_STAGES: 4, 5 or 6).
+int tc_stages() {
+  static const int stages = [] {
+    const char* st = getenv("NVFP4_GEMV_TC_STAGES");
+    const int v = st ? atoi(st) : 4;
+    return (v == 5 || v == 6) ? v : 4;
+  }();
+  return stages;
+}
+
+// CTAs of one instance that fit on an SM of the current device: shared memory
+// (plus the 1 KB the driver reserves per CTA), TMEM columns and registers
+// (allocated per warp in units of 256).  Sets the kernel's attributes on each
+// device the first time; 0 and *err on failure.
+template <int M, int S, bool BF>
+int tc_per_sm_fit(cudaError_t* err) {
+  static PerDeviceInt fit;
+  return fit.get([](int dev, cudaError_t* e_out) -> int {
+    constexpr size_t smem = tc_smem_bytes<S>();
+    auto kern = gemv_tc_kernel<M, S, BF>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) {
+      *e_out = e;
+      return 0;
+    }
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    const int by_smem = smem_sm > 0 ? (int)(smem_sm / (smem + 1024)) : 1;
+    const int by_tmem = 512 / (int)kTmemCols;
+    int by_regs = 2;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs > 0) {
+      const int per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+      by_regs = 65536 / (per_warp * kWarps);
+    }
+    int f = by_smem < by_tmem ? by_smem : by_tmem;
+    if (by_regs < f) f = by_regs;
+    return f < 1 ? 1 : f;
+  }, err);
+}
+
 }  // namespace
 
 // Defined in gemv.cu.
@@ -540,52 +601,35 @@ static int tc_grid_max() { return 2 * nvfp4_internal_device_sms(); }
 // must stay zero between calls of any shape).
 size_t nvfp4_internal_tc_record_bytes() { return (size_t)tc_grid_max() * kTR * 8 * sizeof(unsigned int); }
 
-struct TcMaps {
-  CUtensorMap w_codes, w_scales, x_codes, x_scales;
-};
+void nvfp4_internal_test_gemv_fault(unsigned int flag_spin_limit, int drop_records) {
+  g_test_flag_spins.store(flag_spin_limit, std::memory_order_relaxed);
+  g_test_drop_records.store(drop_records ? 1 : 0, std::memory_order_relaxed);
+}
 
 template <int M, int S, bool BF = false>
 static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm) {
-  static int per_sm_fit = -1;
-  constexpr size_t smem = tc_smem_bytes<S>();
-  auto kern = gemv_tc_kernel<M, S, BF>;
-  if (per_sm_fit < 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    int dev = 0, smem_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    // CTAs per SM: shared memory (plus the 1 KB the driver reserves per CTA),
-    // TMEM columns and registers (allocated per warp in units of 256).
-    int by_smem = smem_sm > 0 ? (int)(smem_sm / (smem + 1024)) : 1;
-    int by_tmem = 512 / (int)kTmemCols;
-    cudaFuncAttributes fa;
-    int by_regs = 2;
-    if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs > 0) {
-      const int per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-      by_regs = 65536 / (per_warp * kWarps);
-    }
-    per_sm_fit = by_smem < by_tmem ? by_smem : by_tmem;
-    if (by_regs < per_sm_fit) per_sm_fit = by_regs;
-    if (per_sm_fit < 1) per_sm_fit = 1;
-  }
-  int per_sm = per_sm_fit < max_ctas_per_sm ? per_sm_fit : max_ctas_per_sm;
+  cudaError_t e = cudaSuccess;
+  const int fit = tc_per_sm_fit<M, S, BF>(&e);
+  if (fit == 0) return e;
+  const int per_sm = fit < max_ctas_per_sm ? fit : max_ctas_per_sm;
   long long G = (long long)per_sm * nvfp4_internal_device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
   if (G > tc_grid_max()) G = tc_grid_max();  // records exist for that many CTAs
+  const uint32_t spins = g_test_flag_spins.load(std::memory_order_relaxed);
+  a.flag_spins = spins ? spins : kFlagSpinLimit;
+  a.drop_records = g_test_drop_records.load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = tc_smem_bytes<S>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mp.w_codes, mp.w_scales, mp.x_codes, mp.x_scales, a);
+  return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<M, S, BF>, mp.w_codes, mp.w_scales, mp.x_codes, mp.x_scales, a);
 }
 
 template <int M>
@@ -605,8 +649,7 @@ static cudaError_t launch_tc_m(int stages, const TcMaps& mp, const TcArgs& a, cu
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
                                    unsigned int* records, int grid_cap, int max_ctas_per_sm, cudaStream_t stream) {
-  const char* st = getenv("NVFP4_GEMV_TC_STAGES");   // tuning knob: 4 (default), 5 or 6
-  const int stages = st ? atoi(st) : 4;
+  const int stages = tc_stages();
   TcMaps mp;
   memset(&mp, 0, sizeof(mp));   // the weight maps stay unused (and are never prefetched) for packed weights
   if (!wpacked && (!nvfp4_internal_encode_2d(&mp.w_codes, wq, (uint64_t)K / 2, (uint64_t)N, 128, kTR, true) ||
@@ -616,6 +659,7 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
       !nvfp4_internal_encode_2d(&mp.x_scales, xs, (uint64_t)K / 16, (uint64_t)M, 16, kNT, false))
     return cudaErrorInvalidValue;
   TcArgs a;
+  memset(&a, 0, sizeof(a));
   a.wpacked = wpacked;
   a.xg = xg;
   a.wg = wg;
@@ -650,6 +694,7 @@ cudaError_t nvfp4_internal_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t
       !nvfp4_internal_encode_2d(&mp.x_codes, x, (uint64_t)K * 2, (uint64_t)M, 128, kNT, true))
     return cudaErrorInvalidValue;
   TcArgs a;
+  memset(&a, 0, sizeof(a));
   a.wpacked = nullptr;
   a.xg = nullptr;
   a.wg = nullptr;

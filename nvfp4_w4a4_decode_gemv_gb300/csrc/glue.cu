@@ -128,16 +128,22 @@ __global__ void __launch_bounds__(kNormThreads) rms_norm_bf16_kernel(const float
 
 template <int M>
 cudaError_t launch_bf16(const uint16_t* x, const uint16_t* w, int N, int K, float* y, cudaStream_t stream) {
-  static int sms = 0;
+  static PerDeviceInt sms_cache;   // SM count; the kernel's shared-memory attribute is set per device
   const size_t smem = (size_t)M * K * sizeof(float);
   auto kern = bf16_gemv_kernel<M>;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemFloats * 4);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t err = cudaSuccess;
+  const int sms = sms_cache.get([](int dev, cudaError_t* e_out) -> int {
+    int n = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bf16_gemv_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemFloats * 4);
+    if (e != cudaSuccess) {
+      *e_out = e;
+      return 0;
+    }
+    return n > 0 ? n : 1;
+  }, &err);
+  if (sms == 0) return err;
   kern<<<sms, kThreads, smem, stream>>>(x, w, N, K, y);
   return cudaGetLastError();
 }

@@ -370,12 +370,16 @@ __global__ void finalize_global_kernel(float* global) {
 
 __global__ void zero_global_kernel(float* global) { *global = 0.0f; }
 
+// Largest cluster of quant_cluster_kernel<Src, NB> the current device can
+// run (8, the portable size, or up to 16 with the non-portable opt-in, which
+// this sets on the device).  Cached per device.
 template <class Src, int NB>
 int max_cluster() {
-  static int cap = 0;
-  if (cap == 0) {
+  static PerDeviceInt cap_cache;
+  cudaError_t err = cudaSuccess;
+  const int cap = cap_cache.get([](int, cudaError_t*) -> int {
     auto kern = quant_cluster_kernel<Src, NB>;
-    cap = 8;                                    // portable size, always available
+    int cap = 8;                                  // portable size, always available
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kMaxCluster);
@@ -392,19 +396,17 @@ int max_cluster() {
       if (cap > kMaxCluster) cap = kMaxCluster;
     }
     cudaGetLastError();
-  }
-  return cap;
+    return cap;
+  }, &err);
+  return cap > 0 ? cap : 8;
 }
 
 template <class Src, int NB>
 cudaError_t launch_cluster(const Src& src, long nblocks, int csize, uint8_t* codes, uint8_t* scales,
                            float* global, cudaStream_t stream) {
-  static bool non_portable = false;   // per instantiation: clusters above 8 CTAs need the opt-in
-  if (csize > 8 && !non_portable) {
-    cudaError_t e = cudaFuncSetAttribute(quant_cluster_kernel<Src, NB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    non_portable = true;
-  }
+  // Clusters above 8 CTAs need the non-portable opt-in, which max_cluster
+  // sets on each device before it reports a cap above 8.
+  if (csize > 8 && max_cluster<Src, NB>() < csize) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize);
   cfg.blockDim = dim3(kCThreads);
@@ -424,8 +426,6 @@ cudaError_t launch_cluster(const Src& src, long nblocks, int csize, uint8_t* cod
   }();
   return cudaLaunchKernelEx(&cfg, quant_cluster_kernel<Src, NB>, src, nblocks, codes, scales, global, trigger_late);
 }
-
-int g_num_sms = 0;
 
 template <class Src>
 cudaError_t quantize_dispatch(const Src& src, long nblocks, uint8_t* codes, uint8_t* scales, float* global,
@@ -449,14 +449,12 @@ cudaError_t quantize_dispatch(const Src& src, long nblocks, uint8_t* codes, uint
     if (nb <= 4) return launch_cluster<Src, 4>(src, nblocks, (int)csize, codes, scales, global, stream);
     return launch_cluster<Src, 8>(src, nblocks, (int)csize, codes, scales, global, stream);
   }
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
+  int dev = 0, num_sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (num_sms <= 0) num_sms = 152;
   long grid = (nblocks + kThreads - 1) / kThreads;
-  if (grid > (long)g_num_sms * 8) grid = (long)g_num_sms * 8;
+  if (grid > (long)num_sms * 8) grid = (long)num_sms * 8;
   cudaError_t e = cudaMemsetAsync(global, 0, sizeof(float), stream);
   if (e != cudaSuccess) return e;
   amax_kernel<Src><<<(unsigned)grid, kThreads, 0, stream>>>(src, nblocks, reinterpret_cast<unsigned int*>(global));

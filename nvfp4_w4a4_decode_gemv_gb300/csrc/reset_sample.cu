@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
       // sampled at T_high without touching its state.
       const int w = p.w;
       const bool state_ok = (st->w == w);
-      if (!state_ok) atomicExch(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
+      if (!state_ok) atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
       double Hs = 0.0, Hbar = 0.0, Hwin = 0.0;
       int t1 = 0, j = 0;
       if (state_ok) {

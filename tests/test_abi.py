@@ -68,6 +68,11 @@ def test_gemv_argument_errors(lib):
     assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, x=None)) == 1
     assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, x=FAKE + 4)) == 3
     assert lib.nvfp4_gemv_smallm(*args(1, 256, 256, ws=FAKE + 16)) == 3
+    for fn in (lib.nvfp4_gemv_smallm, lib.nvfp4_gemv_smallm_cudacore):
+        assert fn(*args(9, 256, 256)) == 4
+        assert fn(*args(1, 256, 272)) == 2
+        assert fn(*args(1, 256, 256, x=None)) == 1
+        assert fn(*args(1, 256, 256, ws=FAKE + 16)) == 3
     assert lib.nvfp4_gemv_workspace_bytes(9, 256, 256) == 0
     assert lib.nvfp4_gemv_workspace_bytes(1, 256, 100) == 0
 

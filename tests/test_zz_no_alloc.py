@@ -67,3 +67,43 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     rc = L.reset_sample_noalloc(ptr(small), M, V, None, ptr(u), ptr(st), ctypes.byref(params), ptr(tok), None, None,
                                 stream_handle())
     assert rc == 2                                        # NVFP4_ERR_SHAPE
+
+
+def _status(L):
+    code = ctypes.c_uint(0)
+    assert L.nvfp4_device_status(ctypes.byref(code)) == 0
+    return code.value
+
+
+def test_noalloc_across_shapes_and_top_p():
+    """Calls of different shapes, with and without top-p, one after another on
+    the shared static array (its layout depends on M and V, and its counters
+    are cleared by each call): every call matches reset_sample on a fresh
+    workspace, and no device error is recorded."""
+    L = lib()
+    w = 8
+    _status(L)
+    seq = [(8, synth.LM_HEAD_VOCAB, 1.0), (3, 2049, 0.9), (64, 4096, 0.95), (1, 1, 1.0),
+           (8, synth.LM_HEAD_VOCAB, 0.95), (5, 70001, 1.0), (3, 2049, 0.9)]
+    for i, (M, V, top_p) in enumerate(seq):
+        params = ResetParams(0.6, 0.3, 1.0, w, 0, top_p)
+        st_ref, st_new = _state(L, M, w), _state(L, M, w)
+        ws = torch.zeros(L.reset_workspace_bytes(M, V), dtype=torch.uint8, device="cuda")
+        us = synth.reset_uniforms(2, M, seed=20 + i)
+        for call in range(2):
+            logits = synth.reset_logits(call + 10 * i, M, V, (1.0, 3.0, 8.0)[(i + call) % 3]).cuda()
+            u = torch.from_numpy(us[call]).cuda()
+            ref = [torch.zeros(M, dtype=torch.int32, device="cuda"), torch.zeros(M, device="cuda"),
+                   torch.zeros(M, device="cuda")]
+            new = [torch.zeros(M, dtype=torch.int32, device="cuda"), torch.zeros(M, device="cuda"),
+                   torch.zeros(M, device="cuda")]
+            assert L.reset_sample(ptr(logits), M, V, None, ptr(u), ptr(st_ref), ctypes.byref(params), ptr(ref[0]),
+                                  ptr(ref[1]), ptr(ref[2]), ptr(ws), ws.numel(), stream_handle()) == 0
+            assert L.reset_sample_noalloc(ptr(logits), M, V, None, ptr(u), ptr(st_new), ctypes.byref(params),
+                                          ptr(new[0]), ptr(new[1]), ptr(new[2]), stream_handle()) == 0
+            torch.cuda.synchronize()
+            assert np.array_equal(ref[0].cpu().numpy(), new[0].cpu().numpy()), (M, V, top_p, call)
+            assert np.array_equal(ref[2].cpu().numpy(), new[2].cpu().numpy()), (M, V, top_p, call)
+            h, h2 = ref[1].cpu().numpy().astype(np.float64), new[1].cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(h - h2) <= 1e-4 * np.maximum(np.abs(h), 1e-6)), (M, V, top_p, call)
+    assert _status(L) == 0
