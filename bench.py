@@ -76,6 +76,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3-32b", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline line only: skip per_proj, the cold per-call table, sampler and decode_step")
+    ap.add_argument("--decode-steps", type=int, default=1500, help="decode_step key: graph replays per M")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
@@ -88,6 +91,9 @@ def parse():
     ap.add_argument("--weights", default="packed", choices=["packed", "rowmajor"],
                     help="weight layout: packed (nvfp4_pack_weights, offline) or row-major codes/scales")
     return ap.parse_args()
+
+
+SPEC_HBM_GBS = 8000.0      # GB300 HBM3e nominal (~8 TB/s), the second denominator
 
 
 def measured_peaks():
@@ -302,7 +308,8 @@ def run_ours(args, world, rank):
     gemv_ms_total = float(np.mean([a.elapsed_time(b) for a, b in ev_gemv]))
     gemv_ms = {M: float(np.mean([ev_m[k][i][0].elapsed_time(ev_m[k][i][1]) for k in range(args.steps)]))
                for i, M in enumerate(order)}
-    per_call = cold_per_call(calls, weights, ws, reps=3)
+    per_call = None if args.no_extras else cold_per_call(calls, weights, ws)
+    proj = None if args.no_extras else per_projection(calls, weights, ws)
 
     step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
     value_gbs = aggregate_gbs(world, step_bytes, args.steps, ms_total)
@@ -332,6 +339,7 @@ def run_ours(args, world, rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
+                     "frac_spec": round(achieved / SPEC_HBM_GBS, 4), "peak_spec": SPEC_HBM_GBS,
                      "traffic": recorded_traffic(args.workload) if args.weights == "packed" and not cuda_cores else None,
                      "traffic_unit": "bytes per GEMV launch (ncu dram__bytes_read + dram__bytes_write, sweep mean)",
                      "algorithmic_bytes_per_launch": round(gemv_bytes_total / len(calls)),
@@ -341,34 +349,144 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "gpu_launches": len(calls) * launches_per_call * args.steps,
         "per_m": per_m,
-        "per_call_cold_l2": per_call,
     }
+    if proj is not None:
+        result["per_proj"] = proj
+    if per_call is not None:
+        result["per_call_cold_l2"] = per_call
     return result, calls, weights, ws
 
 
-def cold_per_call(calls, weights, ws, reps=3):
-    """us per call of the quantizer and the GEMV with L2 flushed before every
-    call (a 512 MB memset, during which the host enqueues the timed call)."""
+def _l2_bytes():
+    return int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 128 << 20))
+
+
+def _weight_clone(api, w):
+    if isinstance(w, api.NVFP4PackedWeight):
+        return api.NVFP4PackedWeight(w.packed.clone(), w.global_scale, w.N, w.K)
+    return api.NVFP4Tensor(w.codes.clone(), w.scales.clone(), w.global_scale)
+
+
+def _weight_bytes(w):
+    return w.packed.numel() if hasattr(w, "packed") else w.codes.numel() + w.scales.numel()
+
+
+def per_projection(calls, weights, ws, R=64, trials=5):
+    """Each (projection, M) alone: a CUDA graph of R chained GEMV calls of that
+    projection (programmatic dependent launches between them, as in a decode
+    chain), replayed after an L2 flush.  Call r reads weight copy r mod n, with
+    n chosen so that the other copies between two uses of one copy exceed
+    2x the L2 size: every call streams its weights from HBM.  A second graph
+    chains quantize -> GEMV pairs.  Median over `trials` replays."""
     from nvfp4_w4a4_decode_gemv_gb300 import api
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    peak, _ = measured_peaks()
+    l2 = _l2_bytes()
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    copies = {}
+    for name, w in weights.items():
+        n = 1 + -(-2 * l2 // _weight_bytes(w))
+        copies[name] = [w] + [_weight_clone(api, w) for _ in range(n - 1)]
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
     out = {}
     for c in calls:
-        q_us, g_us = [], []
-        for _ in range(reps):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            flush.zero_()
-            e[0].record()
-            api.nvfp4_quantize_act(c["x"], out=c["xq"])
-            e[1].record()
-            gemv_call(api, c, weights[c["name"]], ws)
-            e[2].record()
-            torch.cuda.synchronize()
-            q_us.append(e[0].elapsed_time(e[1]) * 1e3)
-            g_us.append(e[1].elapsed_time(e[2]) * 1e3)
-        g = float(np.median(g_us))
-        out[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(g, 2), "quant_us": round(float(np.median(q_us)), 2),
-                                         "gemv_gbs": round(c["gemv_bytes"] / (g * 1e-6) / 1e9, 1)}
-    del flush
+        cp = copies[c["name"]]
+        graphs = {}
+        with torch.cuda.stream(stream):
+            for with_q in (False, True):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for r in range(R):
+                        if with_q:
+                            api.nvfp4_quantize_act(c["x"], out=c["xq"])
+                        gemv_call(api, c, cp[r % len(cp)], ws)
+                graphs[with_q] = g
+        t = {False: [], True: []}
+        with torch.cuda.stream(stream):
+            for _ in range(trials):
+                for with_q in (False, True):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    flush.zero_()
+                    e0.record()
+                    graphs[with_q].replay()
+                    e1.record()
+                    e1.synchronize()
+                    t[with_q].append(e0.elapsed_time(e1) * 1e3 / R)
+        g_us, q_us = float(np.median(t[False])), float(np.median(t[True]))
+        gbs = c["gemv_bytes"] / (g_us * 1e-6) / 1e9
+        qgbs = (c["gemv_bytes"] + c["q_bytes"]) / (q_us * 1e-6) / 1e9
+        out[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(g_us, 3), "gemv_gbs": round(gbs, 1),
+                                         "frac": round(gbs / peak, 4), "frac_spec": round(gbs / SPEC_HBM_GBS, 4),
+                                         "quant_gemv_us": round(q_us, 3), "quant_gemv_gbs": round(qgbs, 1)}
+        del graphs
+    del flush, copies
+    torch.cuda.synchronize()
+    fr = [v["frac"] for v in out.values()]
+    out["summary"] = {"min_frac": round(min(fr), 4), "mean_frac": round(float(np.mean(fr)), 4),
+                      "min_frac_by_proj": {n: round(min(v["frac"] for k, v in out.items() if k.startswith(n + "_M")), 4)
+                                           for n in weights},
+                      "method": f"graph of {R} chained calls of one projection, weight copies rotated so that "
+                                f">= 2x L2 of other weights lies between two uses of one copy; L2 flushed before "
+                                f"each replay; median of {trials} replays; frac against the measured copy peak, "
+                                f"frac_spec against {SPEC_HBM_GBS:.0f} GB/s"}
+    return out
+
+
+def cold_per_call(calls, weights, ws, R=200, trials=7):
+    """us per call with L2 flushed before every call (a write of 2x the L2
+    size): graphs of R x [flush + quantize + GEMV], R x [flush + quantize],
+    R x [flush + GEMV] and R x [flush]; the call's time is the difference over
+    R, per replay; p50 and max over `trials` replays (event clock resolution
+    divided by R)."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    flush = torch.empty(2 * _l2_bytes(), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(R):
+                    flush.zero_()
+                    body()
+        return g
+
+    def time_graph(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            g.replay()
+            e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3
+
+    g_flush = capture(lambda: None)
+    out = {}
+    for c in calls:
+        w = weights[c["name"]]
+        q = lambda: api.nvfp4_quantize_act(c["x"], out=c["xq"])
+        gv = lambda: gemv_call(api, c, w, ws)
+        gs = {"flush": g_flush, "q": capture(q), "qg": capture(lambda: (q(), gv())), "g": capture(gv)}
+        tt = {k: [] for k in gs}
+        for _ in range(trials):
+            for k, g in gs.items():
+                tt[k].append(time_graph(g))
+        f = np.array(tt["flush"])
+        quant = (np.array(tt["q"]) - f) / R
+        gemv_chain = (np.array(tt["qg"]) - np.array(tt["q"])) / R
+        gemv_alone = (np.array(tt["g"]) - f) / R
+        ga = float(np.median(gemv_alone))
+        out[f"{c['name']}_M{c['M']}"] = {
+            "gemv_us": round(ga, 3), "gemv_us_max": round(float(gemv_alone.max()), 3),
+            "gemv_gbs": round(c["gemv_bytes"] / (ga * 1e-6) / 1e9, 1),
+            "quant_us": round(float(np.median(quant)), 3), "quant_us_max": round(float(quant.max()), 3),
+            "gemv_after_quant_us": round(float(np.median(gemv_chain)), 3)}
+        del gs
+    del g_flush, flush
+    torch.cuda.synchronize()
+    out["method"] = (f"graphs of {R} x [L2 flush (2x L2 write) + call] minus {R} x [flush]; median (p50) and max "
+                     f"over {trials} replays; gemv_us = a lone GEMV, gemv_after_quant_us = the GEMV behind its "
+                     f"quantizer (programmatic dependent launch)")
     return out
 
 
@@ -591,6 +709,117 @@ def run_sampler(args, world, rank):
     }
 
 
+def sampler_summary(top_p, n=200, trials=3):
+    """The sampler workload (M = 8 rows x 151936 logits, sigma per step from
+    {1, 3, 8}, geometric step boundaries, PCG64 uniforms), n calls each on its
+    own logits (all resident, 0.97 GB), L2 flushed (2x L2 write) before every
+    call.  Mean: a graph of n x [flush + call] minus n x [flush], median of
+    `trials` replays.  p50 / p99: n eager calls, each between its own two events
+    (resolution of the event clock, ~2 us)."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    dev = torch.device("cuda")
+    M, V = 8, synth.LM_HEAD_VOCAB
+    sig = synth.reset_sigmas(n)
+    logits = torch.empty((n, M, V), dtype=torch.float32, device=dev)
+    for i in range(n):
+        logits[i].copy_(synth.reset_logits(i, M, V, float(sig[i]), device=dev))
+    starts = torch.from_numpy(synth.reset_boundaries(n, M)).to(dev)
+    us = torch.from_numpy(synth.reset_uniforms(n, M)).to(dev)
+    sampler = api.ResetSampler(M, V, 0.6, 0.3, 1.0, 8, device=dev, top_p=top_p)
+    flush = torch.empty(2 * _l2_bytes(), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            sampler(logits[i], starts[i], us[i])
+        g_s, g_f = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_s, stream=stream):
+            for i in range(n):
+                flush.zero_()
+                sampler(logits[i], starts[i], us[i])
+        with torch.cuda.graph(g_f, stream=stream):
+            for i in range(n):
+                flush.zero_()
+    torch.cuda.synchronize()
+    ts, tf = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(trials):
+            for g, acc in ((g_s, ts), (g_f, tf)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                e1.synchronize()
+                acc.append(e0.elapsed_time(e1) * 1e3)
+    mean_us = float(np.median((np.array(ts) - np.array(tf)) / n))
+    single = []
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            e0.record()
+            sampler(logits[i], starts[i], us[i])
+            e1.record()
+            e1.synchronize()
+            single.append(e0.elapsed_time(e1) * 1e3)
+    del logits, flush, g_s, g_f
+    torch.cuda.synchronize()
+    peak, _ = measured_peaks()
+    gbs = 4 * M * V / (mean_us * 1e-6) / 1e9
+    return {"workload": f"M={M}, V={V}, w=8, tau0=0.6, T=0.3/1.0" + (f", top-p {top_p:g}" if top_p < 1 else ""),
+            "us_mean": round(mean_us, 2), "us_p50": round(float(np.percentile(single, 50)), 2),
+            "us_p99": round(float(np.percentile(single, 99)), 2), "calls": n,
+            "launches_per_call": 5 if top_p < 1 else 1,
+            "first_pass_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "method": f"mean: graph of {n} x [L2 flush + call] minus {n} x [flush], median of {trials}; "
+                      f"p50/p99: {n} single calls between events (~2 us event-clock resolution)"}
+
+
+def decode_summary(args, Ms=(1, 4, 8), warmup=20):
+    """The synthetic Qwen3-32B-shaped decode step (64 layers of the four NVFP4
+    projections with their quantizers, BF16 lm_head, ReSET sampler) as one CUDA
+    graph per M, replayed args.decode_steps times, each replay between two
+    events; one model's weights serve every M."""
+    from nvfp4_w4a4_decode_gemv_gb300.decode_step import DecodeStep
+    peak, _ = measured_peaks()
+    base, out = None, {}
+    steps = args.decode_steps
+    for M in Ms:
+        st = DecodeStep(M=M, layers=args.layers, share_weights=base)
+        base = base or st
+        st.h_in.copy_(synth.activations(M, st.hidden, seed=100 + M).float().cuda())
+        us = torch.from_numpy(synth.reset_uniforms(steps + warmup, M)).cuda()
+        st.u.copy_(us[0])
+        st.run()
+        torch.cuda.synchronize()
+        g = st.capture()
+        stream = torch.cuda.Stream()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                st.u.copy_(us[i], non_blocking=True)
+                g.replay()
+            for i in range(steps):
+                st.u.copy_(us[warmup + i], non_blocking=True)
+                evs[i][0].record()
+                g.replay()
+                evs[i][1].record()
+        torch.cuda.synchronize()
+        ms = np.array([a.elapsed_time(b) for a, b in evs])
+        weight_bytes = sum(w.packed.numel() for layer in st.weights for w in layer.values())
+        step_bytes = weight_bytes + st.lm_head.numel() * 2 + st.logits.numel() * 4 * 2
+        gbs = step_bytes / (ms.mean() * 1e-3) / 1e9
+        out[f"M{M}"] = {"ms_mean": round(float(ms.mean()), 4), "ms_p50": round(float(np.percentile(ms, 50)), 4),
+                        "ms_p99": round(float(np.percentile(ms, 99)), 4), "tokens_per_s": round(M * 1e3 / ms.mean(), 1),
+                        "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        del g, st.graph
+    out["method"] = (f"{args.layers} layers + lm_head 5120->151936 + ReSET sampler as one CUDA graph; {steps} replays "
+                     f"per M after {warmup} warm-up replays, each between two events; frac = (NVFP4 weight + BF16 "
+                     f"lm_head + 2 x logits bytes) / mean step time / measured copy peak")
+    del base
+    torch.cuda.synchronize()
+    return out
+
+
 # ---------------------------------------------------------------------------
 def cpu_oracle_sample(args, seconds):
     """The oracle as it stands, on the host: per call, quantize the activation
@@ -704,6 +933,11 @@ def main():
     result, calls, weights, ws = run_ours(args, world, rank)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, calls, weights, ws)
+    if not args.no_extras and args.workload == "qwen3-32b":
+        del calls, weights, ws
+        torch.cuda.synchronize()
+        result["sampler"] = {"plain": sampler_summary(1.0), "top_p_0.95": sampler_summary(0.95)}
+        result["decode_step"] = decode_summary(args)
     if rank == 0:
         if not args.no_cpu_baseline:
             gbs, sample, threads, _ = cpu_oracle_sample(args, seconds=args.cpu_seconds)

@@ -27,7 +27,7 @@ from ._lib import ResetParams
 class DecodeStep:
     def __init__(self, M: int, layers: int, shapes=synth.QWEN3_32B, vocab: int = synth.LM_HEAD_VOCAB,
                  seed: int = 0, eps: float = 1e-6, reset: ResetParams | None = None, keep_rowmajor: bool = False,
-                 device="cuda"):
+                 device="cuda", share_weights: "DecodeStep | None" = None):
         (_, hidden, n_qkv), (_, k_o, _), (_, _, n_gu), (_, k_d, _) = shapes
         self.M, self.layers, self.hidden, self.vocab, self.eps = M, layers, hidden, vocab, eps
         self.n_qkv, self.k_o, self.n_gu, self.k_d = n_qkv, k_o, n_gu, k_d
@@ -35,7 +35,10 @@ class DecodeStep:
         self.device = dev
         self.weights = []          # per layer: {name: NVFP4PackedWeight}
         self.rowmajor = []         # per layer (keep_rowmajor): {name: NVFP4Tensor}
-        for layer in range(layers):
+        if share_weights is not None:  # another step's weights and lm_head (steps of other M on one model)
+            assert share_weights.layers == layers and share_weights.hidden == hidden
+            self.weights, self.rowmajor = share_weights.weights, share_weights.rowmajor
+        for layer in range(0 if share_weights is not None else layers):
             packed, rm = {}, {}
             for i, (name, K, N) in enumerate(shapes):
                 g = torch.Generator(device=dev)
@@ -48,9 +51,12 @@ class DecodeStep:
                     rm[name] = wq
             self.weights.append(packed)
             self.rowmajor.append(rm)
-        g = torch.Generator(device=dev)
-        g.manual_seed(seed * 100003 + 99991)
-        self.lm_head = (torch.randn((vocab, hidden), generator=g, device=dev) * synth.W_STD).to(torch.bfloat16)
+        if share_weights is not None:
+            self.lm_head = share_weights.lm_head
+        else:
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed * 100003 + 99991)
+            self.lm_head = (torch.randn((vocab, hidden), generator=g, device=dev) * synth.W_STD).to(torch.bfloat16)
         # activations and intermediates (reused by every layer)
         f32 = dict(dtype=torch.float32, device=dev)
         self.h_in = torch.zeros((M, hidden), **f32)          # the step's input hidden state
