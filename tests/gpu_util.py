@@ -30,3 +30,23 @@ def assert_within(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, rel=1
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{bad.sum()} elements out of tolerance; first at {tuple(i)}: "
                              f"gpu={y_gpu[tuple(i)]!r} ref={y_ref[tuple(i)]!r} tol={tol[tuple(i)]!r}")
+
+
+GUARD = 4096
+PATTERN = 0xA5
+
+
+class Guarded:
+    """A device tensor of `shape`/`dtype` with GUARD pattern bytes on both sides."""
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        self.nbytes = n
+        self.buf = torch.full((2 * GUARD + n,), PATTERN, dtype=torch.uint8, device="cuda")
+        self.t = self.buf[GUARD:GUARD + n].view(dtype).view(shape)
+
+    def check(self, what):
+        b = to_np(self.buf)
+        head, tail = b[:GUARD], b[GUARD + self.nbytes:]
+        assert (head == PATTERN).all(), f"{what}: {np.count_nonzero(head != PATTERN)} bytes written before the output"
+        assert (tail == PATTERN).all(), f"{what}: {np.count_nonzero(tail != PATTERN)} bytes written after the output"

@@ -21,29 +21,9 @@ from oracle import nvfp4 as Q
 from oracle import reset as R
 from nvfp4_w4a4_decode_gemv_gb300 import api, synth
 from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams, lib
-from tests.gpu_util import assert_within, bits, to_np
+from tests.gpu_util import Guarded, assert_within, bits, to_np
 
 pytestmark = pytest.mark.gpu
-
-GUARD = 4096
-PATTERN = 0xA5
-
-
-class Guarded:
-    """A device tensor of `shape`/`dtype` with GUARD pattern bytes on both sides."""
-
-    def __init__(self, shape, dtype):
-        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
-        self.nbytes = n
-        self.buf = torch.full((2 * GUARD + n,), PATTERN, dtype=torch.uint8, device="cuda")
-        self.t = self.buf[GUARD:GUARD + n].view(dtype).view(shape)
-
-    def check(self, what):
-        b = to_np(self.buf)
-        head, tail = b[:GUARD], b[GUARD + self.nbytes:]
-        assert (head == PATTERN).all(), f"{what}: {np.count_nonzero(head != PATTERN)} bytes written before the output"
-        assert (tail == PATTERN).all(), f"{what}: {np.count_nonzero(tail != PATTERN)} bytes written after the output"
-
 
 def _guarded_nvfp4(rows, K):
     c, s, g = Guarded((rows, K // 2), torch.uint8), Guarded((rows, K // 16), torch.uint8), Guarded((1,), torch.float32)
