@@ -226,6 +226,36 @@ nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, cons
                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Prefill-sized NVFP4 GEMM (M up to 128)                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * y[m, n] = xg * wg * sum_k e2m1(xq[m,k]) e4m3(xs[m,k/16]) e2m1(w[n,k]) e4m3(sw[n,k/16])
+ * for m < M <= 128 and packed weights: the same product as
+ * nvfp4_gemv_smallm_packed for a prefill-sized batch of tokens (the pages'
+ * own tensor-core GEMM at M = 128: ReSET reading note §7.3, Table 16).  One
+ * tcgen05 MMA covers 128 weight rows x 128 tokens x 64 K; each weight block is
+ * read from HBM once per call.  FP32 accumulation: within
+ * 1e-3 * sum_k |x_k w_k| + 1e-6 of the exact product.
+ *   xq, xs, xg   activations, NVFP4 layout [M, K/2], [M, K/16] (16-byte
+ *                aligned), one float
+ *   M            1..128 (else NVFP4_ERR_RANGE)
+ *   wpacked, wg  the weight in the nvfp4_pack_weights layout, one float
+ *   N, K         N 1 .. 2^20, K a positive multiple of 256
+ *   y            [M, N] FP32, 16-byte aligned (written)
+ *   workspace    device scratch of at least nvfp4_gemm_workspace_bytes(M, N, K)
+ *                bytes (a fixed size per device: 64 KB per SM), 256-byte
+ *                aligned, ZEROED ONCE before its first use and left ready for
+ *                the next call of any shape; zero it again after device error
+ *                bit 2.  Calls that overlap on the GPU need different workspaces.
+ * Co-residency and errors as nvfp4_gemv_smallm.  One CTA per SM.
+ */
+size_t nvfp4_gemm_workspace_bytes(int M, int N, int K);
+
+nvfp4_status nvfp4_gemm_packed(const uint8_t* xq, const uint8_t* xs, const float* xg, int M,
+                               const uint8_t* wpacked, const float* wg, int N, int K, float* y,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* BF16 GEMV (the decode step's lm_head)                                       */
 /* ------------------------------------------------------------------------ */
 /*

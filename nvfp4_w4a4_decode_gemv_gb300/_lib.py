@@ -48,6 +48,8 @@ SIGNATURES = {
                                           _c_p]),
     "nvfp4_test_gemv_fault": (None, [ctypes.c_uint, _c_i]),
     "nvfp4_packed_weight_bytes": (_c_sz, [_c_i, _c_i]),
+    "nvfp4_gemm_workspace_bytes": (_c_sz, [_c_i, _c_i, _c_i]),
+    "nvfp4_gemm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_pack_weights": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_sz, _c_p]),
     "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_bf16_gemv": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p]),

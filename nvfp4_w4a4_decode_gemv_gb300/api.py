@@ -12,7 +12,7 @@ from ._lib import THRESHOLD_FIXED, THRESHOLD_RESET, THRESHOLD_WINDOW, ResetParam
 
 __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
-    "nvfp4_gemv_smallm_cudacore", "DEVERR_FLAG_TIMEOUT",
+    "nvfp4_gemv_smallm_cudacore", "DEVERR_FLAG_TIMEOUT", "nvfp4_gemm_packed", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
     "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
     "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
@@ -190,6 +190,35 @@ def nvfp4_gemv_smallm_packed(x: NVFP4Tensor, w: NVFP4PackedWeight, y: torch.Tens
     check(lib().nvfp4_gemv_smallm_packed(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.packed),
                                          ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(),
                                          stream_handle(stream)), "nvfp4_gemv_smallm_packed")
+    return y
+
+
+def nvfp4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_gemm_workspace_bytes(M, N, K))
+
+
+_gemm_ws: dict = {}
+
+
+def nvfp4_gemm_packed(x: NVFP4Tensor, w: NVFP4PackedWeight, y: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] = dequant(x) @ dequant(w)^T for a prefill-sized batch (M <= 128) on packed weights."""
+    M, N, K = x.rows, w.N, x.K
+    if w.K != K:
+        raise ValueError("x and w disagree on K")
+    y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x.codes.device)
+    if workspace is None:
+        dev = x.codes.device
+        key = dev.index if dev.index is not None else torch.cuda.current_device()
+        need = nvfp4_gemm_workspace_bytes(M, N, K)
+        if need == 0:
+            raise ValueError(f"unsupported GEMM shape M={M} N={N} K={K}")
+        if key not in _gemm_ws or _gemm_ws[key].numel() < need:
+            _gemm_ws[key] = torch.zeros(need, dtype=torch.uint8, device=dev)
+        workspace = _gemm_ws[key]
+    check(lib().nvfp4_gemm_packed(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.packed),
+                                  ptr(w.global_scale), N, K, ptr(y), ptr(workspace), workspace.numel(),
+                                  stream_handle(stream)), "nvfp4_gemm_packed")
     return y
 
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB_NAME = "libnvfp4_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["abi.cu", "quantize.cu", "gemv.cu", "gemv_tc.cu", "reset_sample.cu", "glue.cu"]
+SOURCES = ["abi.cu", "quantize.cu", "gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "reset_sample.cu", "glue.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + os.path.join(ROOT, "include")]

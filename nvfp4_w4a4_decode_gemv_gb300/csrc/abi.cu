@@ -6,6 +6,7 @@
 cudaError_t nvfp4_internal_read_error_gemv(unsigned int* out);
 cudaError_t nvfp4_internal_read_error_gemv_tc(unsigned int* out);
 cudaError_t nvfp4_internal_read_error_reset(unsigned int* out);
+cudaError_t nvfp4_internal_read_error_gemm(unsigned int* out);
 
 namespace {
 thread_local char g_last_cuda_error[256] = "no CUDA error";
@@ -61,5 +62,6 @@ extern "C" nvfp4_status nvfp4_device_status(unsigned int* code) {
   cudaError_t e = nvfp4_internal_read_error_gemv(code);
   if (e == cudaSuccess) e = nvfp4_internal_read_error_gemv_tc(code);
   if (e == cudaSuccess) e = nvfp4_internal_read_error_reset(code);
+  if (e == cudaSuccess) e = nvfp4_internal_read_error_gemm(code);
   return nvfp4_internal_cuda_status(e);
 }

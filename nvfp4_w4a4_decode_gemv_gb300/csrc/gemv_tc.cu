@@ -50,6 +50,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 NVFP4_DEFINE_ERROR_READER(nvfp4_internal_read_error_gemv_tc)
 
@@ -98,55 +99,6 @@ struct TcArgs {
   uint32_t flag_spins;           // polls of a record before the wait gives up (kFlagSpinLimit)
   int drop_records;              // test hook: non-zero = publish no record (the first contributor's wait runs out)
 };
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-NVFP4_DEVINL uint64_t smem_desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-NVFP4_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-NVFP4_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-NVFP4_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(da), "l"(db), "r"(kIdescBF16), "r"(acc)
-      : "memory");
-}
-
-NVFP4_DEVINL void mma_mxf4nvf4(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(da), "l"(db), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
-      : "memory");
-}
-
-// One 32-bit column for the warp's 32 lanes.
-NVFP4_DEVINL void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
-NVFP4_DEVINL void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-
-// Bounded wait by a whole warp: lane 0 polls, the outcome is broadcast so that
-// the warp stays converged (also when the wait gives up).
-NVFP4_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Stream-K split: CTA q of G owns units [q U / G, (q+1) U / G).
-NVFP4_DEVINL long long unit_start(long long q, long long U, long long G) { return (q * U) / G; }
-NVFP4_DEVINL long long cta_of_unit(long long x, long long U, long long G) { return ((x + 1) * G - 1) / U; }
 
 // ---- Stream-K fix-up ---------------------------------------------------------------
 // A tile that one CTA covers whole goes straight to y.  A split tile's
@@ -411,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           if (BF)
-            mma_bf16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, (first_of_tile && q == 0) ? 0u : 1u);
+            mma_f16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdescBF16, (first_of_tile && q == 0) ? 0u : 1u);
           else
-            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, sfa + 4u * q, sfb + 4u * q,
+            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sfa + 4u * q, sfb + 4u * q,
                          (first_of_tile && q == 0) ? 0u : 1u);
         }
         mma_commit(&empty[s]);
@@ -605,6 +557,8 @@ void nvfp4_internal_test_gemv_fault(unsigned int flag_spin_limit, int drop_recor
   g_test_flag_spins.store(flag_spin_limit, std::memory_order_relaxed);
   g_test_drop_records.store(drop_records ? 1 : 0, std::memory_order_relaxed);
 }
+uint32_t nvfp4_internal_test_flag_spins() { return g_test_flag_spins.load(std::memory_order_relaxed); }
+int nvfp4_internal_test_drop_records() { return g_test_drop_records.load(std::memory_order_relaxed); }
 
 template <int M, int S, bool BF = false>
 static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm) {

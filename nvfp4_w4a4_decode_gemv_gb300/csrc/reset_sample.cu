@@ -415,6 +415,300 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
   }
 }
 
+// ---- one thread-block cluster per row (the sampler without top-p) ----------------------
+// Rows of up to kMaxClusterCtas x 1024 x PER logits: CTA r of a row's cluster
+// holds logits [r L, (r+1) L) of it, L = 1024 PER, in registers -- thread t the
+// PER consecutive logits from r L + PER t.  The row maximum and the per-CTA
+// sums are exchanged through distributed shared memory (two cluster
+// barriers), so no partial goes through global memory and no CTA waits on a
+// counter.  Every CTA then forms Z, A, H and, from the row state it read at
+// entry, the same T (the same operations in the same order); rank 0 writes the
+// new state.  The CTA whose range holds u * Z_T scans its own registers for
+// the token.
+//
+// FP64 is a narrow, long-latency pipe on this GPU, so it is kept off every
+// per-thread path: sums are FP32 within a thread and a warp, FP64 across warps
+// (a shuffle tree) and CTAs; the threshold rule compares means by
+// cross-multiplying (sum_a * n_b <= sum_b * n_a) instead of dividing; and the
+// token is located in FP64 only down to a warp, then in FP32 within it.
+constexpr int kCThreads = 1024;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kMaxClusterCtas = 8;                  // portable: every GPC can host such a cluster
+
+__device__ __forceinline__ void st_dsmem_f64(uint32_t addr, double v) {
+  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
+}
+
+template <int PER>
+__global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float* __restrict__ logits, int V, int CS,
+                                                                      const uint8_t* __restrict__ step_start,
+                                                                      const float* __restrict__ u, uint8_t* state,
+                                                                      int stride, Params p, int32_t* token,
+                                                                      float* H_out, float* T_out) {
+  constexpr int kCover = kCThreads * PER;
+  // e^x evaluated as 2^(x log2 e): one multiply and the hardware exp2.  The
+  // rounding of x log2 e gives a relative error of about |x| 1.2e-7 per term,
+  // so ~1e-7 of Z for the terms near the maximum that make up Z.
+  constexpr float kLog2e = 1.4426950408889634f;
+  __shared__ float s_wmax[kCWarps];
+  __shared__ float s_wred[5][kCWarps];              // per warp: n0, z1, a1, Z_T at T_low, at T_high
+  __shared__ float s_peer_max[kMaxClusterCtas];
+  __shared__ float s_peer[kMaxClusterCtas][5];      // per CTA: the same five sums
+  __shared__ double s_ring_rest;                    // the window's other w - 1 entropies
+  __shared__ RowState s_st;
+  __shared__ float s_T;
+  __shared__ int s_warp, s_rstar, s_zi;
+  __shared__ float s_tl;
+
+  const uint32_t rank = cluster_ctarank();
+  const int row = blockIdx.x / CS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* base = logits + (size_t)row * V;
+  const int lo = (int)rank * kCover;
+  const int hi = min(V, lo + kCover);
+  const int i0 = lo + threadIdx.x * PER;
+  // Peers may write into this CTA's shared memory only once it runs: arrive
+  // now, wait just before the first remote store.
+  if (CS > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  float v[PER];
+  if ((V & 3) == 0 && (PER & 3) == 0 && i0 + PER <= hi) {   // row start 16-byte aligned, all in range
+#pragma unroll
+    for (int k = 0; k < PER / 4; ++k) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(base + i0) + k);
+      v[4 * k] = q.x;
+      v[4 * k + 1] = q.y;
+      v[4 * k + 2] = q.z;
+      v[4 * k + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) v[k] = (i0 + k < hi) ? __ldg(base + i0 + k) : -INFINITY;
+  }
+
+  // ---- row maximum ----
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) mx = fmaxf(mx, v[k]);
+  mx = warp_max(mx);
+  if (lane == 0) s_wmax[warp] = mx;
+  __syncthreads();
+  mx = warp_max(s_wmax[lane]);                      // every warp reduces the 32 warp maxima itself
+  if (CS > 1) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (threadIdx.x < CS) st_dsmem_f32(dsmem_addr(&s_peer_max[rank], threadIdx.x), mx);
+    __syncwarp();
+    cluster_sync();
+    mx = warp_max(lane < CS ? s_peer_max[lane] : -INFINITY);
+  }
+  const float gm = mx;
+
+  // The row state (every CTA derives T from it; rank 0 updates it after the
+  // last cluster barrier, when every CTA has read it): the last warp reads it,
+  // its lanes the window ring in parallel (w <= 256: up to 8 entries a lane).
+  if (warp == kCWarps - 1) {
+    const RowState* st = reinterpret_cast<const RowState*>(state + (size_t)row * stride);
+    const RowState r = *st;
+    double rest = 0.0;
+    if (r.w == p.w && r.t + 1 > p.w) {
+      const double* ring = reinterpret_cast<const double*>(st + 1);
+      const int slot = r.t % p.w;
+      for (int i = lane; i < p.w; i += 32)
+        if (i != slot) rest += ring[i];
+    }
+    rest = warp_sum_d(rest);
+    if (lane == 0) {
+      s_st = r;
+      s_ring_rest = rest;
+    }
+  }
+
+  // ---- per-thread sums relative to the row maximum (FP32).  Logits equal to
+  // the maximum are counted, not summed; at T_high = 1 the T_high sum is the
+  // T = 1 sum.  A thread keeps its Z_T for both temperatures for the scan ----
+  const float cl = kLog2e * (1.0f / p.t_low), ch = kLog2e * (1.0f / p.t_high);
+  const bool th_one = (p.t_high == 1.0f);
+  float n0 = 0.f, z1 = 0.f, a1 = 0.f, zl = 0.f, zh = 0.f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    if (i0 + k < hi) {
+      const float s = v[k] - gm;
+      if (s == 0.0f) {
+        n0 += 1.0f;
+      } else {
+        const float e = exp2f(s * kLog2e);
+        z1 += e;
+        a1 += e * s;
+      }
+      zl += exp2f(s * cl);
+      if (!th_one) zh += exp2f(s * ch);
+    }
+  }
+  if (th_one) zh = n0 + z1;
+  const float my_zl = zl, my_zh = zh;
+  float f[5] = {n0, z1, a1, zl, zh};
+#pragma unroll
+  for (int i = 0; i < 5; ++i) f[i] = warp_sum(f[i]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 5; ++i) s_wred[i][warp] = f[i];
+  }
+  __syncthreads();
+  if (warp == 0) {                                  // this CTA's five sums over its 32 warps
+    float g[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) g[i] = warp_sum(s_wred[i][lane]);
+    if (lane < 5) {
+      const float acc = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : lane == 3 ? g[3] : g[4];
+      if (CS > 1) {
+        for (int r = 0; r < CS; ++r) st_dsmem_f32(dsmem_addr(&s_peer[rank][lane], r), acc);
+      } else {
+        s_peer[0][lane] = acc;
+      }
+    }
+    __syncwarp();
+  }
+  if (CS > 1) cluster_sync();
+  else __syncthreads();
+
+  // ---- H, the state rule and T (thread 0; every CTA the same).  Row sums in
+  // FP32 in CTA order; Z - 1 is (the maxima counted - 1) + the rest, so a
+  // nearly one-hot row keeps its relative precision.  The state sums are
+  // FP64 ----
+  if (threadIdx.x == 0) {
+    float cnt = 0.f, rest = 0.f, A = 0.f, ztl = 0.f, zth = 0.f;
+    for (int r = 0; r < CS; ++r) {
+      cnt += s_peer[r][0];
+      rest += s_peer[r][1];
+      A += s_peer[r][2];
+      ztl += s_peer[r][3];
+      zth += s_peer[r][4];
+    }
+    const float zm1 = (cnt - 1.0f) + rest;
+    const double H = (double)(log1pf(zm1) - A / (1.0f + zm1));
+    RowState ns = s_st;
+    const int w = p.w;
+    const bool state_ok = (ns.w == w);
+    bool low = false;
+    int t1 = 0, j = 0;
+    if (state_ok) {
+      if (ns.t == 0 || (step_start && step_start[row])) {
+        ns.j = 0;
+        ns.step_sum = 0.0;
+      }
+      ns.glob_sum += H;
+      ns.step_sum += H;
+      t1 = ns.t + 1;
+      j = ns.j;
+      // The window mean is wsum / wn: the whole history while t1 <= w.
+      const double wsum = (t1 > w) ? s_ring_rest + H : ns.glob_sum;
+      const int wn = (t1 > w) ? w : t1;
+      // H_step = ssum / sn; H_bar = glob_sum / t1.  Means are compared by
+      // cross-multiplying (the counts are positive).
+      const double ssum = (j < w) ? wsum : ns.step_sum;
+      const int sn = (j < w) ? wn : j + 1;
+      bool above;                                   // H >= tau (then T_high)
+      if (p.threshold == RESET_THRESHOLD_FIXED) {
+        above = !(H < (double)p.tau0);
+      } else if (p.threshold == RESET_THRESHOLD_WINDOW) {
+        above = !(H * wn < wsum);
+      } else {
+        const bool confident = ssum * t1 <= ns.glob_sum * sn;   // H_step <= H_bar
+        above = confident ? !(H < (double)p.tau0) : !(H * sn < ssum);
+      }
+      low = !above;
+    }
+    const float T = low ? p.t_low : p.t_high;
+    s_T = T;
+    if (rank == 0) {
+      if (!state_ok) atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
+      if (state_ok) {
+        RowState* stw = reinterpret_cast<RowState*>(state + (size_t)row * stride);
+        reinterpret_cast<double*>(stw + 1)[ns.t % w] = H;
+        stw->glob_sum = ns.glob_sum;
+        stw->step_sum = ns.step_sum;
+        stw->t = t1;
+        stw->j = j + 1;
+      }
+      if (H_out) H_out[row] = (float)H;
+      if (T_out) T_out[row] = T;
+    }
+    // The CTA that holds u * Z_T: the first whose running total passes the
+    // target (the last CTA if rounding leaves the target at or past the total).
+    const int zi = low ? 3 : 4;
+    const float target = __ldg(u + row) * (low ? ztl : zth);
+    float before = 0.f;
+    int rstar = CS - 1;
+    for (int r = 0; r < CS; ++r) {
+      const float z = s_peer[r][zi];
+      if (before + z > target) {
+        rstar = r;
+        break;
+      }
+      before += z;
+    }
+    s_rstar = rstar;
+    s_zi = zi;
+    s_tl = target - before;                         // the target within CTA rstar
+  }
+  __syncthreads();
+  if ((int)rank != s_rstar) return;
+
+  // ---- the token in this CTA: the warp from the per-warp Z_T sums, the lane
+  // from the threads' kept totals, then the lane's own logits ----
+  const int zi = s_zi;
+  if (warp == 0) {
+    const float tl = s_tl;
+    const float wt = s_wred[zi][lane];
+    float wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    // The first warp whose running total passes the target; else the last
+    // warp that holds logits of this CTA.
+    const unsigned hit = __ballot_sync(0xffffffffu, wi > tl);
+    const int nlive = (hi - lo + 32 * PER - 1) / (32 * PER);
+    const int wsel = hit ? __ffs(hit) - 1 : nlive - 1;
+    const float wb = __shfl_sync(0xffffffffu, wi - wt, wsel);
+    if (lane == 0) {
+      s_warp = wsel;
+      s_tl = tl - wb;
+    }
+  }
+  __syncthreads();
+  if (warp == s_warp) {
+    const float tl = s_tl;
+    const float mine = (zi == 3) ? my_zl : my_zh;
+    float incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > tl);
+    const int lsel = hit ? __ffs(hit) - 1 : 31;
+    if (lane == lsel) {
+      const float cT = (zi == 3) ? cl : ch;
+      float run = incl - mine;
+      int tok = -1, last = -1;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        if (i0 + k < hi) {
+          run += exp2f((v[k] - gm) * cT);
+          last = i0 + k;
+          if (run > tl && tok < 0) tok = i0 + k;
+        }
+      }
+      // Rounding can leave the target just past the lane's last partial sum
+      // (or the lane may hold no logit): the sample is then the last logit of
+      // the warp's range that exists.
+      token[row] = tok >= 0 ? tok : (last >= 0 ? last : min(hi, lo + (warp + 1) * 32 * PER) - 1);
+    }
+  }
+}
+
 // ---- top-p launches ---------------------------------------------------------------
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
@@ -742,6 +1036,49 @@ nvfp4_status check_params(const reset_params* p) {
   return NVFP4_OK;
 }
 
+// The cluster sampler for V logits per row: PER logits per thread (12, 20 or
+// 32) and CS <= 8 CTAs per row; false when V needs more (the multi-launch
+// path then serves).
+template <int PER>
+nvfp4_status launch_cluster_per(const float* logits, int M, int V, int CS, const uint8_t* step_start, const float* u,
+                                void* state, const Params& prm, int32_t* token, float* H_out, float* T_out,
+                                cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(M * CS));
+  cfg.blockDim = dim3(kCThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return nvfp4_internal_cuda_status(cudaLaunchKernelEx(&cfg, reset_cluster_kernel<PER>, logits, V, CS, step_start, u,
+                                                       static_cast<uint8_t*>(state), (int)state_stride(prm.w), prm,
+                                                       token, H_out, T_out));
+}
+
+bool launch_cluster(const float* logits, int M, int V, const uint8_t* step_start, const float* u, void* state,
+                    const Params& prm, int32_t* token, float* H_out, float* T_out, cudaStream_t stream,
+                    nvfp4_status* st) {
+  const long long per_cta12 = (long long)kCThreads * 12, per_cta20 = (long long)kCThreads * 20,
+                  per_cta32 = (long long)kCThreads * 32;
+  if (V <= kMaxClusterCtas * per_cta12) {
+    *st = launch_cluster_per<12>(logits, M, V, (int)((V + per_cta12 - 1) / per_cta12), step_start, u, state, prm,
+                                 token, H_out, T_out, stream);
+  } else if (V <= kMaxClusterCtas * per_cta20) {
+    *st = launch_cluster_per<20>(logits, M, V, (int)((V + per_cta20 - 1) / per_cta20), step_start, u, state, prm,
+                                 token, H_out, T_out, stream);
+  } else if (V <= kMaxClusterCtas * per_cta32) {
+    *st = launch_cluster_per<32>(logits, M, V, (int)((V + per_cta32 - 1) / per_cta32), step_start, u, state, prm,
+                                 token, H_out, T_out, stream);
+  } else {
+    return false;
+  }
+  return true;
+}
+
 // The sampler's launches for M rows in `scratch` (laid out by sample_layout).
 nvfp4_status launch_sample(const float* logits, int M, int V, int NC, const uint8_t* step_start, const float* u,
                            void* state, const reset_params* p, int32_t* token, float* H_out, float* T_out,
@@ -754,6 +1091,10 @@ nvfp4_status launch_sample(const float* logits, int M, int V, int NC, const uint
   unsigned long long* csum = reinterpret_cast<unsigned long long*>(scratch + L.csum);
   const bool nucleus = p->top_p > 0.0f && p->top_p < 1.0f;
   Params prm{p->tau0, p->t_low, p->t_high, p->w, p->threshold, p->top_p};
+  if (!nucleus) {
+    nvfp4_status cst = NVFP4_OK;
+    if (launch_cluster(logits, M, V, step_start, u, state, prm, token, H_out, T_out, stream, &cst)) return cst;
+  }
   reset_sample_kernel<<<M * NC, kThreads, 0, stream>>>(logits, M, V, NC, step_start, u, static_cast<uint8_t*>(state),
                                                         (int)state_stride(p->w), prm, token, H_out, T_out, parts,
                                                         counters, nucleus ? nrows : nullptr, hist);

@@ -77,6 +77,19 @@ def test_gemv_argument_errors(lib):
     assert lib.nvfp4_gemv_workspace_bytes(1, 256, 100) == 0
 
 
+def test_gemm_argument_errors(lib):
+    args = lambda M, N, K, x=FAKE, ws=FAKE: (x, FAKE, FAKE, M, FAKE, FAKE, N, K, FAKE, ws, 1 << 30, None)
+    assert lib.nvfp4_gemm_packed(*args(129, 256, 256)) == 4          # M > 128
+    assert lib.nvfp4_gemm_packed(*args(0, 256, 256)) == 4
+    assert lib.nvfp4_gemm_packed(*args(64, 256, 272)) == 2           # K % 256
+    assert lib.nvfp4_gemm_packed(*args(64, 0, 256)) == 2
+    assert lib.nvfp4_gemm_packed(*args(64, 256, 256, x=None)) == 1
+    assert lib.nvfp4_gemm_packed(*args(64, 256, 256, x=FAKE + 8)) == 3
+    assert lib.nvfp4_gemm_packed(*args(64, 256, 256, ws=FAKE + 16)) == 3
+    assert lib.nvfp4_gemm_workspace_bytes(129, 256, 256) == 0
+    assert lib.nvfp4_gemm_workspace_bytes(128, 256, 100) == 0
+
+
 def test_packed_weight_argument_errors(lib):
     assert lib.nvfp4_packed_weight_bytes(1000, 768) == 8 * 3 * 18432      # ceil(1000/128) tiles x 3 chunks
     assert lib.nvfp4_packed_weight_bytes(128, 256) == 18432
