@@ -47,8 +47,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "4f75984507cf6f1d640c9e92baa13187753c4806dd0ae9c4f66e260e626eda16",
-                  "workload": "qwen3-32b", "bytes_per_launch": 68992451}
+                  "sha256": "c635ba148b62142a5e5ddecaeff6ea0e949bd58ac5f1280fa9eda49cf74b1662",
+                  "workload": "qwen3-32b", "bytes_per_launch": 68995654}
 
 
 def recorded_traffic(workload):
@@ -63,8 +63,10 @@ def recorded_traffic(workload):
     return TRAFFIC_RECORD["bytes_per_launch"]
 WORKLOADS = {"qwen3-32b": (synth.QWEN3_32B, list(range(1, 9))), "qwen3-8b": (synth.QWEN3_8B, [1, 2, 4, 8]),
              "qwen3-14b": (synth.QWEN3_14B, [1, 2, 4, 8]),
-             "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8]), "reset-sampler": (None, [8])}
+             "qwen3-32b-decode": (synth.QWEN3_32B, [1, 4, 8]), "reset-sampler": (None, [8]),
+             "qwen3-32b-prefill": (synth.QWEN3_32B, [128])}
 SAMPLER_METRIC = "ReSET sampler latency per decode step, FP32 logits [8, 151936] (entropy, state update, T, sample)"
+PREFILL_METRIC = "prefill NVFP4 GEMM (M=128 tokens) µs/call and achieved HBM GB/s, Qwen3-32B shapes"
 DECODE_METRIC = "Qwen3-32B-shaped decode step latency (64 NVFP4 layers + BF16 lm_head + ReSET sampler, one CUDA graph)"
 
 
@@ -432,7 +434,7 @@ def per_projection(calls, weights, ws, R=64, trials=5):
     return out
 
 
-def prefill_summary(M=128, R=16, trials=5):
+def prefill_summary(M=128, R=16, trials=5, only=None):
     """The prefill-sized GEMM (nvfp4_gemm_packed) on the Qwen3-32B projections
     at M = 128 tokens: per projection a graph of R chained calls over rotated
     weight copies (>= 2x L2 between two uses of one copy), L2 flushed before
@@ -446,6 +448,8 @@ def prefill_summary(M=128, R=16, trials=5):
     stream = torch.cuda.Stream()
     out = {}
     for i, (name, K, N) in enumerate(synth.QWEN3_32B):
+        if only and name != only:
+            continue
         g = torch.Generator(device=dev)
         g.manual_seed(1000 + i)
         wb = (torch.randn((N, K), generator=g, device=dev, dtype=torch.float32) * synth.W_STD).to(torch.bfloat16)
@@ -971,6 +975,28 @@ def main():
                                  "sample": sample},
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return
+    if args.workload == "qwen3-32b-prefill":
+        if args.impl == "reference" or world > 1:
+            if rank == 0:
+                print(json.dumps({"impl": args.impl, "unavailable": "the prefill workload is measured on one GPU, "
+                                                                     "for our kernel only"}))
+            return
+        res = prefill_summary(only=args.only, trials=max(3, args.steps))
+        names = [k for k in res if k != "method"]
+        by = sum(synth.gemv_bytes(128, N, K) for n, K, N in synth.QWEN3_32B if n in names)
+        us = sum(res[n]["us"] for n in names)
+        peak, peak_kind = measured_peaks()
+        gbs = by / (us * 1e-6) / 1e9
+        print(json.dumps({"metric": PREFILL_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "nvfp4 w4a4, fp32 accumulate", "data": "synthetic",
+                          "config": {"workload": "qwen3-32b prefill projections at M=128: " + ",".join(names)},
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                       "frac": round(gbs / peak, 4), "traffic": None,
+                                       "peak_source": f"{peak_kind} hbm_gbs"},
+                          "per_proj": res, "gpu_launches": 16 * len(names) * max(3, args.steps)}))
         return
     if args.workload in ("qwen3-32b-decode", "reset-sampler"):
         line = (run_decode if args.workload == "qwen3-32b-decode" else run_sampler)(args, world, rank)

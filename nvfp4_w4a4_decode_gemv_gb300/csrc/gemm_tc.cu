@@ -379,7 +379,13 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   const uint32_t spins = nvfp4_internal_test_flag_spins();
   a.flag_spins = spins ? spins : kFlagSpinLimit;
   a.drop_records = nvfp4_internal_test_drop_records();
-  long long G = nvfp4_internal_device_sms();
+  // One CTA per SM.  With fewer 128-row tiles than SMs, every tile gets the
+  // same whole number of CTAs (tiles x floor(SMs / tiles)): a split tile's
+  // partial sums are 64 KB per contributor at M = 128, so the fewer and more
+  // even the splits, the shorter the fix-up.
+  const long long sms = nvfp4_internal_device_sms();
+  const long long tiles = (N + kTR - 1) / kTR;
+  long long G = tiles < sms ? tiles * (sms / tiles) : sms;
   if (G > a.U) G = a.U;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
