@@ -825,7 +825,7 @@ def sampler_summary(top_p, n=200, trials=3):
     return {"workload": f"M={M}, V={V}, w=8, tau0=0.6, T=0.3/1.0" + (f", top-p {top_p:g}" if top_p < 1 else ""),
             "us_mean": round(mean_us, 2), "us_p50": round(float(np.percentile(single, 50)), 2),
             "us_p99": round(float(np.percentile(single, 99)), 2), "calls": n,
-            "launches_per_call": 5 if top_p < 1 else 1,
+            "launches_per_call": 1,
             "first_pass_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
             "method": f"mean: graph of {n} x [L2 flush + call] minus {n} x [flush], median of {trials}; "
                       f"p50/p99: {n} single calls between events (~2 us event-clock resolution)"}

@@ -61,7 +61,8 @@ struct Params {
   float tau0, t_low, t_high;
   int w;
   int threshold;            // RESET_THRESHOLD_*
-  float top_p;              // in (0, 1) when the nucleus launches follow, else ignored
+  float top_p;              // in (0, 1): sample from the nucleus, else from every token
+  float mscale;             // integer-mass scale of the nucleus: 2^(62 - ceil(log2 V))
 };
 
 constexpr int kHistBins = 2048;   // per-row histogram of one radix level
@@ -101,6 +102,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -435,11 +441,725 @@ constexpr int kCThreads = 1024;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxClusterCtas = 8;                  // portable: every GPC can host such a cluster
 
-__device__ __forceinline__ void st_dsmem_f64(uint32_t addr, double v) {
-  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void ld_dsmem_2u64(uint32_t addr, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.shared::cluster.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr) : "memory");
+}
+
+// ---- top-p inside the row's cluster ------------------------------------------------
+// Masses are integers, floor(2^a x mscale) with a = (l - max) log2(e) / T, so
+// every bin, sum and scan below sees the same numbers and every sum is exact in
+// any order: the token depends neither on the cluster's size nor on
+// scheduling.  The boundary key is the smallest order key whose inclusive mass
+// reaches ceil(top_p Z); a token is kept iff its key is at most the boundary --
+// the smallest set of most probable tokens that reaches top_p, every logit tied
+// to its least probable member included.  Each thread keeps 2^a mscale of its
+// logits in shared memory (dynamic, PER x 4 KB), so the mass is evaluated once.
+
+constexpr int kCand = 4096;            // crossing-bin keys gathered on rank 0, kCand / CS (rounded down to 32) a CTA
+constexpr int kSuper = kHistBins / 32; // super-bins of 32 bins: the crossing is found in two 32-wide steps
+constexpr int kSubBins = 256;          // rank 0 splits the crossing bin into 256 log-mass sub-bins
+constexpr float kBinsPerOctave = 64.0f;
+
+// floor(x) for 0 <= x < 2^63 with integer operations only (a 64-bit conversion
+// instruction runs on this GPU's narrow FP64 pipe).  x below 1 gives 0.
+__device__ __forceinline__ unsigned long long mass_bits(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const int sh = (int)(b >> 23) - 150;                // x = mant 2^sh for 1 <= x
+  const unsigned long long mant = (b & 0x7FFFFFu) | 0x800000u;
+  return b < 0x3F800000u ? 0ull : (sh >= 0 ? mant << sh : mant >> -sh);
+}
+
+// ceil(p z) (up) or floor(p z), exactly, for a float 0 <= p <= 1 and z < 2^63:
+// p = mant 2^-sh, the 128-bit product z mant shifted right by sh >= 23.
+__device__ __forceinline__ unsigned long long scale_u64(float p, unsigned long long z, bool up) {
+  const uint32_t b = __float_as_uint(p);
+  const int e = (int)((b >> 23) & 0xFFu);
+  const unsigned long long mant = e ? ((b & 0x7FFFFFu) | 0x800000u) : (b & 0x7FFFFFu);
+  const int sh = 150 - (e ? e : 1);
+  const unsigned long long lo = z * mant, hi = __umul64hi(z, mant);
+  unsigned long long q;
+  bool dropped;
+  if (sh >= 128) {
+    q = 0ull;
+    dropped = (hi | lo) != 0ull;
+  } else if (sh >= 64) {
+    const int s2 = sh - 64;
+    q = hi >> s2;
+    dropped = lo != 0ull || (s2 > 0 && (hi & ((1ull << s2) - 1ull)) != 0ull);
+  } else {
+    q = (lo >> sh) | (hi << (64 - sh));
+    dropped = (lo & ((1ull << sh) - 1ull)) != 0ull;
+  }
+  return q + ((up && dropped) ? 1ull : 0ull);
+}
+
+// Log-mass bin floor(-64 a): 1/64 octave of mass a bin, the last bin taking
+// everything from 32 octaves below the maximum down.  It never decreases as
+// the logit falls, so a bin is a contiguous range of order keys.
+__device__ __forceinline__ int logmass_bin(float a) {
+  const float x = a * -kBinsPerOctave;
+  return x < (float)(kHistBins - 1) ? (int)x : kHistBins - 1;
+}
+
+// Adds m to bin d of a histogram kept as 32-bit words (low words at d, high
+// words at nb + d): shared-memory 32-bit atomics, where a contended 64-bit one
+// is many times slower.  A per-CTA bin total stays below 2^62, so the high
+// word (the high halves plus the carries) cannot wrap.
+__device__ __forceinline__ void hist_add_u64(uint32_t* h32, int nb, int d, unsigned long long m) {
+  const uint32_t ml = (uint32_t)m;
+  uint32_t mh = (uint32_t)(m >> 32);
+  if (ml) {
+    const uint32_t old = atomicAdd(&h32[d], ml);
+    mh += (old + ml < old) ? 1u : 0u;                 // the low word wrapped
+  }
+  if (mh) atomicAdd(&h32[nb + d], mh);
+}
+
+// Inclusive scan over a warp.
+__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  return x;
+}
+__device__ __forceinline__ unsigned int warp_incl_u32(unsigned int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  return x;
+}
+
+// Warp 0: the digit of a 256-bin histogram (32-bit words, low at d, high at
+// 256 + d) where the running mass, started at acc, first reaches need.
+// Returns the digit in every lane and sets *before to the mass ahead of it.
+__device__ __forceinline__ int warp_cross256(const uint32_t* r32, unsigned long long acc, unsigned long long need,
+                                             unsigned long long* before) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long bm[8], lt = 0ull;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    bm[i] = r32[8 * lane + i] | ((unsigned long long)r32[256 + 8 * lane + i] << 32);
+    lt += bm[i];
+  }
+  const unsigned long long li = warp_incl_u64(lt);
+  const unsigned hit = __ballot_sync(0xffffffffu, acc + li >= need);
+  const int ls = hit ? __ffs(hit) - 1 : 31;
+  unsigned long long run = acc + li - lt;
+  int dg = 8 * lane + 7;
+  bool found = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (!found && run + bm[i] >= need) {
+      dg = 8 * lane + i;
+      found = true;
+    }
+    if (!found && i < 7) run += bm[i];
+  }
+  *before = __shfl_sync(0xffffffffu, run, ls);
+  return __shfl_sync(0xffffffffu, dg, ls);
+}
+
+// The token in this CTA given the boundary key, the target within the CTA's
+// kept mass and each thread's kept mass `mine`: token = min{ i : P_i > tloc },
+// P the running kept mass in index order (P > u Zk <=> P > floor(u Zk) for
+// integers).  The warp from the per-warp kept masses, the lane from the
+// threads' totals, then the lane's logits one per lane of the warp.  Returns
+// the token in every lane of the chosen warp, -1 elsewhere.
+template <int PER>
+__device__ __forceinline__ int nucleus_select(const float (&v)[PER], int i0, int hi, const float* s_mx, uint32_t kstar,
+                                              unsigned long long tloc, unsigned long long mine) {
+  __shared__ unsigned long long s_pw[kCWarps];
+  __shared__ int s_wsel;
+  __shared__ unsigned long long s_wtl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long ws = warp_sum_u64(mine);
+  if (lane == 0) s_pw[warp] = ws;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long wt = s_pw[lane];
+    const unsigned long long wi = warp_incl_u64(wt);
+    const unsigned hit = __ballot_sync(0xffffffffu, wi > tloc);
+    const int wsel = hit ? __ffs(hit) - 1 : 31;
+    const unsigned long long wb = __shfl_sync(0xffffffffu, wi - wt, wsel);
+    if (lane == 0) {
+      s_wsel = wsel;
+      s_wtl = tloc - wb;
+    }
+  }
+  __syncthreads();
+  if (warp != s_wsel) return -1;
+  const unsigned long long tl = s_wtl;
+  const unsigned long long incl = warp_incl_u64(mine);
+  const unsigned hit = __ballot_sync(0xffffffffu, incl > tl);
+  const int lsel = hit ? __ffs(hit) - 1 : 31;
+  // lane j takes logit j of lane lsel
+  const unsigned long long base = __shfl_sync(0xffffffffu, incl - mine, lsel);
+  const int is = __shfl_sync(0xffffffffu, i0, lsel);
+  float lj = 0.0f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const float x = __shfl_sync(0xffffffffu, v[j], lsel);
+    if (lane == j) lj = x;
+  }
+  const bool live = lane < PER && is + lane < hi;
+  const unsigned long long mj =
+      (live && nucleus_key(lj) <= kstar) ? mass_bits(s_mx[lane * kCThreads + 32 * warp + lsel]) : 0ull;
+  const unsigned long long run = base + warp_incl_u64(mj);
+  const unsigned h2 = __ballot_sync(0xffffffffu, live && run > tl);
+  const unsigned lv = __ballot_sync(0xffffffffu, live);
+  // exact sums always find it; else the lane's last logit
+  return min(is + (h2 ? __ffs(h2) - 1 : (lv ? 31 - __clz(lv) : 0)), hi - 1);
+}
+
+// The same, each thread's kept mass summed over all its logits.
+template <int PER>
+__device__ __forceinline__ int nucleus_pick(const float (&v)[PER], int i0, int hi, const float* s_mx, uint32_t kstar,
+                                            unsigned long long tloc) {
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    if (i0 + k < hi && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + threadIdx.x]);
+  return nucleus_select<PER>(v, i0, hi, s_mx, kstar, tloc, mine);
+}
+
+// The boundary key by a three-level radix search over the order keys (11, 11
+// and 10 bits) across the cluster.  Per level: each CTA bins its own logits'
+// masses; after a cluster barrier each CTA sums a 1/CS slice of the bins over
+// every CTA and pushes its slice total; after a second barrier the CTA whose
+// slice holds the crossing finds the digit and pushes it to every CTA; a third
+// barrier publishes it.  Then the CTAs' kept masses are exchanged and the CTA
+// holding floor(u Zk) picks the token.  Used when the crossing log-mass bin
+// holds more keys than the gather below has room for (large ties).
+template <int PER>
+__device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int i0, int hi, const Params& p,
+                                                     uint32_t rank, int CS, float u_row, unsigned long long* s_hist,
+                                                     const float* s_mx) {
+  __shared__ unsigned long long s_slice[kMaxClusterCtas];  // per CTA: its slice total (levels), its kept mass
+  __shared__ unsigned long long s_res[3];          // the level's digit, mass below it, mass of its bin
+  __shared__ unsigned long long s_w64[kCWarps], s_wex[kCWarps];
+  __shared__ int s_pick;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  uint32_t* h32 = reinterpret_cast<uint32_t*>(s_hist);
+  unsigned int prefix = 0;
+  unsigned long long below = 0ull, target = 0ull, binmass = 0ull;
+#pragma unroll 1
+  for (int level = 0; level < 3; ++level) {
+    const int nb = level == 2 ? 1024 : kHistBins;
+    for (int b = t; b < kHistBins; b += kCThreads) s_hist[b] = 0ull;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      if (i0 + k < hi) {
+        const uint32_t key = nucleus_key(v[k]);
+        const bool match = level == 0 ? true : level == 1 ? (key >> 21) == prefix : (key >> 10) == prefix;
+        if (match) {
+          const uint32_t d = level == 0 ? key >> 21 : level == 1 ? (key >> 10) & 0x7FFu : key & 0x3FFu;
+          hist_add_u64(h32, kHistBins, (int)d, mass_bits(s_mx[k * kCThreads + t]));
+        }
+      }
+    }
+    __syncthreads();
+    {                                               // fold the words into 64-bit bins in place
+      const unsigned long long c0 = h32[t] | ((unsigned long long)h32[kHistBins + t] << 32);
+      const unsigned long long c1 =
+          h32[t + kCThreads] | ((unsigned long long)h32[kHistBins + t + kCThreads] << 32);
+      __syncthreads();
+      s_hist[t] = c0;
+      s_hist[t + kCThreads] = c1;
+    }
+    cluster_sync();                                 // every CTA's histogram is complete
+    // This CTA's slice of the row histogram, bins [rank sl, rank sl + sl):
+    // thread t holds the `per` consecutive bins from rank sl + t per (per is 1,
+    // or 2 when one CTA covers 2048 bins).
+    const int sl = (nb + CS - 1) / CS;
+    const int per = (sl + kCThreads - 1) / kCThreads;
+    const int send = min(nb, ((int)rank + 1) * sl);  // end of this CTA's slice
+    const int b0 = (int)rank * sl + t * per;
+    unsigned long long bins[2] = {0ull, 0ull};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int bb = b0 + j;
+      if (j < per && bb < send) {
+        unsigned long long x[kMaxClusterCtas];
+#pragma unroll
+        for (int r = 0; r < kMaxClusterCtas; ++r) x[r] = r < CS ? ld_dsmem_u64(dsmem_addr(&s_hist[bb], (uint32_t)r)) : 0ull;
+#pragma unroll
+        for (int r = 0; r < kMaxClusterCtas; ++r) bins[j] += x[r];
+      }
+    }
+    const unsigned long long bin = bins[0] + bins[1];   // this thread's total
+    const unsigned long long ws = warp_sum_u64(bin);
+    if (lane == 0) s_w64[warp] = ws;
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long tot = warp_sum_u64(s_w64[lane]);
+      if (lane < CS) st_dsmem_u64(dsmem_addr(&s_slice[rank], (uint32_t)lane), tot);
+      __syncwarp();
+    }
+    cluster_sync();                                 // slice totals published; peers are done with s_hist
+    if (level == 0) {
+      unsigned long long z = 0ull;
+      for (int r = 0; r < CS; ++r) z += s_slice[r];
+      // z >= 1: the maximum's mass is mscale; the target is in [1, z]
+      const unsigned long long tg = scale_u64(p.top_p, z, true);
+      target = tg < 1ull ? 1ull : (tg > z ? z : tg);
+    }
+    // the slice holding the crossing: the first whose running total reaches the target
+    int rstar = CS - 1;
+    unsigned long long pre = below;
+    for (int r = 0; r < CS; ++r) {
+      if (pre + s_slice[r] >= target) {
+        rstar = r;
+        break;
+      }
+      pre += s_slice[r];
+    }
+    if ((int)rank == rstar) {
+      // exclusive scan of the threads' totals in bin order
+      const unsigned long long incl = warp_incl_u64(bin);
+      if (lane == 31) s_w64[warp] = incl;
+      if (t == 0) s_pick = 0x7fffffff;
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned long long wv = s_w64[lane];
+        s_wex[lane] = warp_incl_u64(wv) - wv;
+      }
+      __syncthreads();
+      const unsigned long long excl = pre + s_wex[warp] + incl - bin;
+      // the thread whose bins hold the crossing
+      if (b0 < send && excl + bin >= target && excl < target) atomicMin(&s_pick, t);
+      __syncthreads();
+      // The levels see the same integers, so the range chosen at the level
+      // before reaches the target; the fallback (the slice's last bin) is not
+      // reached.
+      const int last_t = (send - 1 - (int)rank * sl) / per;
+      const int tp = s_pick != 0x7fffffff ? s_pick : last_t;
+      if (t == tp) {
+        // within the thread's bins: the first that reaches the target, else
+        // its last bin
+        const bool two = per == 2 && b0 + 1 < send;
+        const bool first = !two || excl + bins[0] >= target;
+        const int bsel = first ? b0 : b0 + 1;
+        const unsigned long long bm = first ? bins[0] : bins[1];
+        const unsigned long long ex = first ? excl : excl + bins[0];
+        for (int r = 0; r < CS; ++r) {
+          st_dsmem_u64(dsmem_addr(&s_res[0], (uint32_t)r), (unsigned long long)bsel);
+          st_dsmem_u64(dsmem_addr(&s_res[1], (uint32_t)r), ex);
+          st_dsmem_u64(dsmem_addr(&s_res[2], (uint32_t)r), bm);
+        }
+      }
+      __syncwarp();
+    }
+    cluster_sync();                                 // the digit is everywhere
+    const unsigned int digit = (unsigned int)s_res[0];
+    below = s_res[1];
+    binmass = s_res[2];
+    prefix = level == 0 ? digit : level == 1 ? (prefix << 11) | digit : (prefix << 10) | digit;
+  }
+  const unsigned int kstar = prefix;               // the boundary key
+  const unsigned long long zk = below + binmass;   // the nucleus's mass
+
+  // ---- the CTAs' kept masses, then the CTA holding floor(u Zk) ----
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    if (i0 + k < hi && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + t]);
+  const unsigned long long ws = warp_sum_u64(mine);
+  if (lane == 0) s_w64[warp] = ws;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long tot = warp_sum_u64(s_w64[lane]);
+    if (lane < CS) st_dsmem_u64(dsmem_addr(&s_slice[rank], (uint32_t)lane), tot);
+    __syncwarp();
+  }
+  cluster_sync();
+  unsigned long long tgt = scale_u64(u_row, zk, false);   // floor(u Zk) in [0, Zk)
+  if (tgt >= zk) tgt = zk - 1ull;
+  int rstar = CS - 1;
+  unsigned long long pre = 0ull;
+  for (int r = 0; r < CS; ++r) {
+    if (pre + s_slice[r] > tgt) {
+      rstar = r;
+      break;
+    }
+    pre += s_slice[r];
+  }
+  if ((int)rank != rstar) return -1;
+  return nucleus_pick<PER>(v, i0, hi, s_mx, kstar, tgt - pre);
+}
+
+// Top-p inside the row's cluster (every CTA of the cluster calls it, with T
+// known), in three cluster barriers:
+//  1. each CTA evaluates its logits' masses once and bins them by log-mass
+//     (1/64 octave a bin, exact integer totals) in shared memory, with the
+//     totals of 64 super-bins of 32 bins; barrier;
+//  2. in every CTA one warp reads the 64 super-bin totals of every CTA, finds
+//     the super-bin where the running mass reaches ceil(top_p Z), then reads
+//     its 32 bins of every CTA and finds the crossing bin -- the same in every
+//     CTA; each CTA sends rank 0 its mass before that bin and, for each of its
+//     logits inside it, the order key, the mass and a sub-bin (1/256 of the
+//     bin); barrier;
+//  3. rank 0 finds the boundary key among the gathered ones: a histogram of
+//     the 256 sub-bins, then an exact comparison of the keys in the crossing
+//     sub-bin (a radix search over the key bits when that holds more than 32);
+//     it forms each CTA's kept mass, locates floor(u Zk) and tells the CTA
+//     that holds it; barrier; that CTA picks the token.  While rank 0
+//     searches, the other CTAs sum each thread's mass before the crossing bin,
+//     so the pick only adds the thread's logits inside it.
+// A bin spans 1/64 octave of probability, so the crossing bin holds few
+// logits; if some CTA finds more than its share of kCand, every CTA runs the
+// radix search above instead.
+//
+// Dynamic shared memory: PER x 1024 floats (2^a mscale of logit k of thread t
+// at k 1024 + t), then rank 0's gathered masses, keys and sub-bins.
+template <int PER>
+constexpr size_t cluster_nucleus_smem() {
+  return (size_t)PER * kCThreads * sizeof(float) + (size_t)kCand * (sizeof(unsigned long long) + sizeof(uint32_t) + 1);
 }
 
 template <int PER>
+__device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, int hi, float gm, float cT,
+                                               const Params& p, uint32_t rank, int CS, float u_row) {
+  static_assert(kHistBins == 2 * kCThreads && kSuper == 64, "two bins a thread, two super-bins a lane");
+  static_assert(PER <= 32, "one match bit (and one lane of the pick) a logit");
+  static_assert(kCThreads >= kSubBins && kCand % kCThreads == 0, "one sub-bin a thread");
+  __shared__ __align__(16) unsigned long long s_hist[kHistBins];  // this CTA's bins (32-bit words while binning)
+  __shared__ __align__(16) unsigned long long s_sup[kSuper];      // this CTA's super-bin totals
+  __shared__ unsigned int s_ccnt[kMaxClusterCtas];      // rank 0: how many logits CTA r sent
+  __shared__ unsigned long long s_cmass[kMaxClusterCtas];  // rank 0: CTA r's mass before the crossing bin
+  __shared__ unsigned long long s_kept[kMaxClusterCtas];   // rank 0: CTA r's kept mass
+  __shared__ unsigned long long s_w64[kCWarps];
+  __shared__ unsigned int s_wcnt[kCWarps];
+  __shared__ unsigned long long s_x[3];                 // the crossing bin, the mass before it, the target
+  __shared__ unsigned long long s_rh[kSubBins];         // rank 0: sub-bin / digit masses (32-bit words)
+  __shared__ unsigned int s_rc[kSubBins];               // rank 0: sub-bin counts
+  __shared__ uint32_t s_k32[32];                        // rank 0: the crossing sub-bin's keys ...
+  __shared__ unsigned long long s_m32[32];              // ... and masses
+  __shared__ unsigned int s_n32;
+  __shared__ unsigned long long s_sel[3];               // rank 0: sub-bin, mass before it, boundary key
+  __shared__ unsigned long long s_fin[2];               // from rank 0: the boundary key, the target in this CTA
+  __shared__ unsigned int s_status;                     // from rank 0: 0 done, 1 pick the token, 2 radix search
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  float* s_mx = reinterpret_cast<float*>(s_dyn);
+  unsigned long long* s_cm = reinterpret_cast<unsigned long long*>(s_dyn + (size_t)PER * kCThreads * sizeof(float));
+  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_cm + kCand);
+  uint8_t* s_cb = reinterpret_cast<uint8_t*>(s_ck + kCand);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const float ms = p.mscale;
+  uint32_t* h32 = reinterpret_cast<uint32_t*>(s_hist);
+  const int b0 = 2 * t;                                 // this thread's two bins
+
+  // ---- 1. masses, this CTA's log-mass histogram and super-bin totals ----
+  s_hist[b0] = 0ull;
+  s_hist[b0 + 1] = 0ull;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    if (i0 + k < hi) {
+      const float a = (v[k] - gm) * cT;
+      const float x = exp2f(a) * ms;
+      s_mx[k * kCThreads + t] = x;
+      const unsigned long long m = mass_bits(x);
+      if (m) hist_add_u64(h32, kHistBins, logmass_bin(a), m);
+    }
+  }
+  __syncthreads();
+  {                                                     // fold the words into 64-bit bins in place
+    const unsigned long long c0 = h32[b0] | ((unsigned long long)h32[kHistBins + b0] << 32);
+    const unsigned long long c1 = h32[b0 + 1] | ((unsigned long long)h32[kHistBins + b0 + 1] << 32);
+    __syncthreads();
+    s_hist[b0] = c0;
+    s_hist[b0 + 1] = c1;
+    // lanes 0-15 of warp w hold super-bin 2w, lanes 16-31 super-bin 2w + 1
+    unsigned long long sp = c0 + c1;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    if ((lane & 15) == 0) s_sup[2 * warp + (lane >> 4)] = sp;
+  }
+  cluster_sync();                                       // every CTA's bins are complete
+
+  // ---- 2. warp 0: the crossing super-bin, then the crossing bin ----
+  if (warp == 0) {
+    unsigned long long sa = 0ull, sb = 0ull;
+    {
+      unsigned long long q0[kMaxClusterCtas], q1[kMaxClusterCtas];
+#pragma unroll
+      for (int r = 0; r < kMaxClusterCtas; ++r) {
+        q0[r] = 0ull;
+        q1[r] = 0ull;
+        if (r < CS) ld_dsmem_2u64(dsmem_addr(&s_sup[2 * lane], (uint32_t)r), q0[r], q1[r]);
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxClusterCtas; ++r) {
+        sa += q0[r];
+        sb += q1[r];
+      }
+    }
+    const unsigned long long lt = sa + sb;
+    const unsigned long long li = warp_incl_u64(lt);
+    const unsigned long long z = __shfl_sync(0xffffffffu, li, 31);   // >= 1: the maximum's mass is mscale
+    unsigned long long target = scale_u64(p.top_p, z, true);
+    target = target < 1ull ? 1ull : (target > z ? z : target);
+    const unsigned h1 = __ballot_sync(0xffffffffu, li >= target);
+    const int l1 = h1 ? __ffs(h1) - 1 : 31;
+    const unsigned long long ex1 = __shfl_sync(0xffffffffu, li - lt, l1);
+    const unsigned long long sa1 = __shfl_sync(0xffffffffu, sa, l1);
+    const bool first = ex1 + sa1 >= target;
+    const int S = 2 * l1 + (first ? 0 : 1);
+    const unsigned long long bS = first ? ex1 : ex1 + sa1;   // mass before super-bin S
+    unsigned long long fb = 0ull;
+    {
+      unsigned long long q[kMaxClusterCtas];
+#pragma unroll
+      for (int r = 0; r < kMaxClusterCtas; ++r) q[r] = r < CS ? ld_dsmem_u64(dsmem_addr(&s_hist[32 * S + lane], (uint32_t)r)) : 0ull;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterCtas; ++r) fb += q[r];
+    }
+    const unsigned long long fi = warp_incl_u64(fb);
+    const unsigned h2 = __ballot_sync(0xffffffffu, bS + fi >= target);
+    const int l2 = h2 ? __ffs(h2) - 1 : 31;
+    if (lane == l2) {
+      s_x[0] = (unsigned long long)(32 * S + l2);
+      s_x[1] = bS + fi - fb;
+      s_x[2] = target;
+    }
+  }
+  __syncthreads();
+  const int dstar = (int)s_x[0];
+  const unsigned long long below = s_x[1], target = s_x[2];
+
+  // ---- this CTA's mass before the crossing bin and its logits inside it -> rank 0 ----
+  const int Cr = (kCand / CS) & ~31;                    // logits a CTA may send
+  const unsigned long long mb = (b0 < dstar ? s_hist[b0] : 0ull) + (b0 + 1 < dstar ? s_hist[b0 + 1] : 0ull);
+  uint32_t match = 0u, lower = 0u;                      // logits in / before the crossing bin
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    if (i0 + k < hi) {
+      const int d = logmass_bin((v[k] - gm) * cT);
+      if (d == dstar) match |= 1u << k;
+      if (d < dstar) lower |= 1u << k;
+    }
+  }
+  const unsigned int cnt = __popc(match);
+  const unsigned int ci = warp_incl_u32(cnt);
+  const unsigned long long mw = warp_sum_u64(mb);
+  if (lane == 31) s_wcnt[warp] = ci;
+  if (lane == 0) s_w64[warp] = mw;                      // (its last reader passed two barriers ago)
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned int wc = s_wcnt[lane];
+    const unsigned int wci = warp_incl_u32(wc);
+    const unsigned long long mt = warp_sum_u64(s_w64[lane]);
+    __syncwarp();
+    s_wcnt[lane] = wci - wc;
+    if (lane == 31) {
+      st_dsmem_u32(dsmem_addr(&s_ccnt[rank], 0u), wci);
+      st_dsmem_u64(dsmem_addr(&s_cmass[rank], 0u), mt);
+    }
+  }
+  __syncthreads();
+  if (match) {
+    unsigned int slot = s_wcnt[warp] + ci - cnt;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      if ((match >> k) & 1u) {
+        if (slot < (unsigned)Cr) {
+          const int j = (int)rank * Cr + (int)slot;
+          // sub-bin: the fraction of -64 a past the bin's start, x 256 (exact steps)
+          const float f = ((v[k] - gm) * cT * -kBinsPerOctave - (float)dstar) * (float)kSubBins;
+          const uint32_t sbin = f < (float)(kSubBins - 1) ? (uint32_t)f : (uint32_t)(kSubBins - 1);
+          st_dsmem_u64(dsmem_addr(&s_cm[j], 0u), mass_bits(s_mx[k * kCThreads + t]));
+          st_dsmem_u32(dsmem_addr(&s_ck[j], 0u), nucleus_key(v[k]));
+          st_dsmem_u8(dsmem_addr(&s_cb[j], 0u), sbin);
+        }
+        ++slot;
+      }
+    }
+  }
+  cluster_sync();                                       // the gathered logits and masses are on rank 0
+
+  // ---- 3. rank 0: the boundary key, the kept masses, the CTA holding the sample ----
+  unsigned long long mine = 0ull;                       // this thread's mass before the crossing bin
+  if (rank == 0) {
+    bool over = false;
+    for (int r = 0; r < CS; ++r) over |= s_ccnt[r] > (unsigned)Cr;
+    if (over) {
+      if (t < CS) st_dsmem_u32(dsmem_addr(&s_status, (uint32_t)t), 2u);
+    } else {
+      constexpr int kQ = kCand / kCThreads;
+      uint32_t ck[kQ];
+      unsigned long long cm[kQ];
+      int csb[kQ];
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int s = t + q * kCThreads;
+        int r = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxClusterCtas; ++i) r += s >= i * Cr ? 1 : 0;
+        const bool ok = r < CS && s - r * Cr < (int)s_ccnt[r];
+        ck[q] = ok ? s_ck[s] : 0xFFFFFFFFu;
+        cm[q] = ok ? s_cm[s] : 0ull;
+        csb[q] = ok ? (int)s_cb[s] : -1;
+      }
+      // The smallest key K with (mass of gathered keys <= K) >= target - below.
+      // Sub-bins never decrease with the key, so every key of a lower sub-bin
+      // is below every key of a higher one.
+      const unsigned long long need = target - below;  // >= 1: the bins before the crossing fall short
+      uint32_t* r32 = reinterpret_cast<uint32_t*>(s_rh);
+      if (t < kSubBins) {
+        s_rh[t] = 0ull;
+        s_rc[t] = 0u;
+      }
+      if (t == 0) s_n32 = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        if (csb[q] >= 0) {
+          if (cm[q]) hist_add_u64(r32, kSubBins, csb[q], cm[q]);
+          atomicAdd(&s_rc[csb[q]], 1u);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        unsigned long long acc;
+        const int sbs = warp_cross256(r32, 0ull, need, &acc);
+        if (lane == 0) {
+          s_sel[0] = (unsigned long long)sbs;
+          s_sel[1] = acc;
+        }
+      }
+      __syncthreads();
+      const int sbs = (int)s_sel[0];
+      unsigned long long acc = s_sel[1];
+      const unsigned int n32 = s_rc[sbs];
+      uint32_t kstar;
+      if (n32 <= 32u) {
+        // the crossing sub-bin's keys, compared exactly in one warp
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          if (csb[q] == sbs) {
+            const unsigned int j = atomicAdd(&s_n32, 1u);
+            s_k32[j] = ck[q];
+            s_m32[j] = cm[q];
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          const bool has = (unsigned)lane < n32;
+          const uint32_t kl = has ? s_k32[lane] : 0xFFFFFFFFu;
+          const unsigned long long ml = has ? s_m32[lane] : 0ull;
+          unsigned long long cum = 0ull;                // mass of the sub-bin's keys <= kl
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t kj = __shfl_sync(0xffffffffu, kl, j);
+            const unsigned long long mj = __shfl_sync(0xffffffffu, ml, j);
+            if (kj <= kl) cum += mj;
+          }
+          uint32_t best = (has && acc + cum >= need) ? kl : 0xFFFFFFFFu;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
+          if (lane == 0) s_sel[2] = best;
+        }
+        __syncthreads();
+        kstar = (uint32_t)s_sel[2];
+      } else {
+        // many keys in one sub-bin (ties, or a dense bin): eight key bits a round
+        uint32_t prefix = 0u;
+#pragma unroll 1
+        for (int round = 0; round < 4; ++round) {
+          const int sh = 24 - 8 * round;
+          if (t < kSubBins) s_rh[t] = 0ull;
+          __syncthreads();
+#pragma unroll
+          for (int q = 0; q < kQ; ++q)
+            if (csb[q] == sbs && cm[q] && (round == 0 || (ck[q] >> (sh + 8)) == prefix))
+              hist_add_u64(r32, kSubBins, (int)((ck[q] >> sh) & 0xFFu), cm[q]);
+          __syncthreads();
+          if (warp == 0) {
+            unsigned long long before;
+            const int dg = warp_cross256(r32, acc, need, &before);
+            if (lane == 0) {
+              s_sel[0] = (unsigned long long)dg;
+              s_sel[1] = before;
+            }
+          }
+          __syncthreads();
+          prefix = (prefix << 8) | (uint32_t)s_sel[0];
+          acc = s_sel[1];
+          __syncthreads();
+        }
+        kstar = prefix;
+      }
+      // each CTA's kept mass: its mass before the bin + its gathered keys <= kstar
+      // (warp r sums CTA r's range)
+      if (warp < CS) {
+        const int n = (int)s_ccnt[warp];
+        unsigned long long kw = 0ull;
+        for (int j = lane; j < n; j += 32)
+          if (s_ck[warp * Cr + j] <= kstar) kw += s_cm[warp * Cr + j];
+        kw = warp_sum_u64(kw);
+        if (lane == 0) s_kept[warp] = s_cmass[warp] + kw;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // zk >= target >= 1; the sample is floor(u zk) in [0, zk), in the first
+        // CTA whose running kept mass passes it
+        const unsigned long long kr = lane < CS ? s_kept[lane] : 0ull;
+        const unsigned long long ki = warp_incl_u64(kr);
+        const unsigned long long zk = __shfl_sync(0xffffffffu, ki, 31);
+        unsigned long long tgt = scale_u64(u_row, zk, false);
+        if (tgt >= zk) tgt = zk - 1ull;
+        const unsigned hr = __ballot_sync(0xffffffffu, lane < CS && ki > tgt);
+        const int rstar = hr ? __ffs(hr) - 1 : CS - 1;
+        if (lane == rstar) {
+          st_dsmem_u64(dsmem_addr(&s_fin[0], (uint32_t)rstar), (unsigned long long)kstar);
+          st_dsmem_u64(dsmem_addr(&s_fin[1], (uint32_t)rstar), tgt - (ki - kr));
+        }
+        if (lane < CS) st_dsmem_u32(dsmem_addr(&s_status, (uint32_t)lane), lane == rstar ? 1u : 0u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      if ((lower >> k) & 1u) mine += mass_bits(s_mx[k * kCThreads + t]);
+  }
+  cluster_sync();                                       // the verdict is in every CTA
+  const unsigned int status = s_status;
+  if (status == 2u) return cluster_nucleus_radix<PER>(v, i0, hi, p, rank, CS, u_row, s_hist, s_mx);
+  if (status != 1u) return -1;
+  const uint32_t kstar = (uint32_t)s_fin[0];
+  if (rank == 0) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      if ((lower >> k) & 1u) mine += mass_bits(s_mx[k * kCThreads + t]);
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    if (((match >> k) & 1u) && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + t]);
+  return nucleus_select<PER>(v, i0, hi, s_mx, kstar, s_fin[1], mine);
+}
+
+template <int PER, bool NUC>
 __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float* __restrict__ logits, int V, int CS,
                                                                       const uint8_t* __restrict__ step_start,
                                                                       const float* __restrict__ u, uint8_t* state,
@@ -540,8 +1260,10 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
         z1 += e;
         a1 += e * s;
       }
-      zl += exp2f(s * cl);
-      if (!th_one) zh += exp2f(s * ch);
+      if constexpr (!NUC) {                         // top-p forms its own masses at the chosen T
+        zl += exp2f(s * cl);
+        if (!th_one) zh += exp2f(s * ch);
+      }
     }
   }
   if (th_one) zh = n0 + z1;
@@ -652,6 +1374,12 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
     s_tl = target - before;                         // the target within CTA rstar
   }
   __syncthreads();
+  if constexpr (NUC) {                              // top-p (NUC is set iff 0 < top_p < 1)
+    const float cT = (s_T == p.t_low) ? cl : ch;
+    const int tok = cluster_nucleus<PER>(v, i0, hi, gm, cT, p, rank, CS, __ldg(u + row));
+    if (tok >= 0 && (threadIdx.x & 31) == 0) token[row] = tok;
+    return;
+  }
   if ((int)rank != s_rstar) return;
 
   // ---- the token in this CTA: the warp from the per-warp Z_T sums, the lane
@@ -710,11 +1438,6 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
 }
 
 // ---- top-p launches ---------------------------------------------------------------
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 
 // Exclusive scan of one value per thread across the CTA; *total gets the sum.
 __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* s_w,
@@ -1039,7 +1762,7 @@ nvfp4_status check_params(const reset_params* p) {
 // The cluster sampler for V logits per row: PER logits per thread (12, 20 or
 // 32) and CS <= 8 CTAs per row; false when V needs more (the multi-launch
 // path then serves).
-template <int PER>
+template <int PER, bool NUC>
 nvfp4_status launch_cluster_per(const float* logits, int M, int V, int CS, const uint8_t* step_start, const float* u,
                                 void* state, const Params& prm, int32_t* token, float* H_out, float* T_out,
                                 cudaStream_t stream) {
@@ -1054,29 +1777,55 @@ nvfp4_status launch_cluster_per(const float* logits, int M, int V, int CS, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return nvfp4_internal_cuda_status(cudaLaunchKernelEx(&cfg, reset_cluster_kernel<PER>, logits, V, CS, step_start, u,
+  if (NUC) {
+    // top-p keeps each logit's 2^a mscale and rank 0's gathered logits in
+    // dynamic shared memory, above the default 48 KB: granted once per device
+    const int bytes = (int)cluster_nucleus_smem<PER>();
+    static PerDeviceInt granted;
+    cudaError_t err = cudaSuccess;
+    granted.get(
+        [&](int, cudaError_t* e) {
+          *e = cudaFuncSetAttribute(reset_cluster_kernel<PER, NUC>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+          return *e == cudaSuccess ? 1 : 0;
+        },
+        &err);
+    if (err != cudaSuccess) return nvfp4_internal_cuda_status(err);
+    cfg.dynamicSmemBytes = (size_t)bytes;
+  }
+  return nvfp4_internal_cuda_status(cudaLaunchKernelEx(&cfg, reset_cluster_kernel<PER, NUC>, logits, V, CS, step_start, u,
                                                        static_cast<uint8_t*>(state), (int)state_stride(prm.w), prm,
                                                        token, H_out, T_out));
 }
 
-bool launch_cluster(const float* logits, int M, int V, const uint8_t* step_start, const float* u, void* state,
-                    const Params& prm, int32_t* token, float* H_out, float* T_out, cudaStream_t stream,
-                    nvfp4_status* st) {
+template <bool NUC>
+bool launch_cluster_nuc(const float* logits, int M, int V, const uint8_t* step_start, const float* u, void* state,
+                        const Params& prm, int32_t* token, float* H_out, float* T_out, cudaStream_t stream,
+                        nvfp4_status* st) {
   const long long per_cta12 = (long long)kCThreads * 12, per_cta20 = (long long)kCThreads * 20,
                   per_cta32 = (long long)kCThreads * 32;
   if (V <= kMaxClusterCtas * per_cta12) {
-    *st = launch_cluster_per<12>(logits, M, V, (int)((V + per_cta12 - 1) / per_cta12), step_start, u, state, prm,
-                                 token, H_out, T_out, stream);
+    *st = launch_cluster_per<12, NUC>(logits, M, V, (int)((V + per_cta12 - 1) / per_cta12), step_start, u, state,
+                                      prm, token, H_out, T_out, stream);
   } else if (V <= kMaxClusterCtas * per_cta20) {
-    *st = launch_cluster_per<20>(logits, M, V, (int)((V + per_cta20 - 1) / per_cta20), step_start, u, state, prm,
-                                 token, H_out, T_out, stream);
+    *st = launch_cluster_per<20, NUC>(logits, M, V, (int)((V + per_cta20 - 1) / per_cta20), step_start, u, state,
+                                      prm, token, H_out, T_out, stream);
   } else if (V <= kMaxClusterCtas * per_cta32) {
-    *st = launch_cluster_per<32>(logits, M, V, (int)((V + per_cta32 - 1) / per_cta32), step_start, u, state, prm,
-                                 token, H_out, T_out, stream);
+    *st = launch_cluster_per<32, NUC>(logits, M, V, (int)((V + per_cta32 - 1) / per_cta32), step_start, u, state,
+                                      prm, token, H_out, T_out, stream);
   } else {
     return false;
   }
   return true;
+}
+
+// The cluster sampler when the row fits one cluster (V <= 8 x 1024 x 32);
+// false otherwise (the multi-launch path then serves).
+bool launch_cluster(const float* logits, int M, int V, const uint8_t* step_start, const float* u, void* state,
+                    const Params& prm, int32_t* token, float* H_out, float* T_out, cudaStream_t stream,
+                    nvfp4_status* st) {
+  const bool nuc = prm.top_p > 0.0f && prm.top_p < 1.0f;
+  return nuc ? launch_cluster_nuc<true>(logits, M, V, step_start, u, state, prm, token, H_out, T_out, stream, st)
+             : launch_cluster_nuc<false>(logits, M, V, step_start, u, state, prm, token, H_out, T_out, stream, st);
 }
 
 // The sampler's launches for M rows in `scratch` (laid out by sample_layout).
@@ -1090,8 +1839,8 @@ nvfp4_status launch_sample(const float* logits, int M, int V, int NC, const uint
   unsigned long long* hist = reinterpret_cast<unsigned long long*>(scratch + L.hist);
   unsigned long long* csum = reinterpret_cast<unsigned long long*>(scratch + L.csum);
   const bool nucleus = p->top_p > 0.0f && p->top_p < 1.0f;
-  Params prm{p->tau0, p->t_low, p->t_high, p->w, p->threshold, p->top_p};
-  if (!nucleus) {
+  Params prm{p->tau0, p->t_low, p->t_high, p->w, p->threshold, p->top_p, mass_scale(V)};
+  {
     nvfp4_status cst = NVFP4_OK;
     if (launch_cluster(logits, M, V, step_start, u, state, prm, token, H_out, T_out, stream, &cst)) return cst;
   }

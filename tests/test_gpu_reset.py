@@ -205,6 +205,42 @@ def test_top_p_keeps_whole_tie_groups(top_p):
     assert api.device_status() == 0
 
 
+@pytest.mark.parametrize("top_p", [0.5, 0.95])
+def test_top_p_tie_groups_full_vocab(top_p):
+    """V = 151936 (eight CTAs a row, 512 gathered keys each): tie groups of
+    ~30k logits fill one log-mass bin, more than the gather holds, so the
+    boundary comes from the three-level radix search."""
+    M, V = 2, synth.LM_HEAD_VOCAB
+    sampler = api.ResetSampler(M, V, top_p=top_p)
+    p = R.ResetParams(top_p=_f32(top_p))
+    us = synth.reset_uniforms(3, M, seed=12)
+    for t in range(3):
+        logits = _tie_logits(M, V, seed=200 + t)
+        tok, H, T = sampler(logits.cuda(), None, torch.from_numpy(us[t]).cuda())
+        torch.cuda.synchronize()
+        ln = logits.numpy().astype(np.float64)
+        for r in range(M):
+            assert _token_ok(ln[r], float(T.cpu()[r]), float(us[t, r]), int(tok.cpu()[r]), p.top_p)
+    assert api.device_status() == 0
+
+
+def test_top_p_bf16_valued_logits_full_vocab():
+    """Logits rounded to BF16 (a model's output): ties of a few hundred per
+    value, which the gather holds, across M = 8 rows of V = 151936."""
+    M, V, steps = 8, synth.LM_HEAD_VOCAB, 3
+    sampler = api.ResetSampler(M, V, top_p=0.95)
+    p = R.ResetParams(top_p=_f32(0.95))
+    us = synth.reset_uniforms(steps, M, seed=13)
+    for t in range(steps):
+        logits = synth.reset_logits(t, M, V, 2.0).to(torch.bfloat16).float()
+        tok, H, T = sampler(logits.cuda(), None, torch.from_numpy(us[t]).cuda())
+        torch.cuda.synchronize()
+        ln = logits.numpy().astype(np.float64)
+        for r in range(M):
+            assert _token_ok(ln[r], float(T.cpu()[r]), float(us[t, r]), int(tok.cpu()[r]), p.top_p)
+    assert api.device_status() == 0
+
+
 def test_top_p_single_token_nucleus_and_u_extremes():
     """One dominant logit: at top_p <= its probability only it is kept, for
     every u, including u = 0 and the largest float below 1."""
