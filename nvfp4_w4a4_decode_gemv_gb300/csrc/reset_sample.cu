@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) reset_sample_kernel(const float* __r
       } else {
         const float e = expf(s);
         z1 += e;
-        a1 += e * s;
+        if (e > 0.0f) a1 += e * s;       // a -inf logit adds nothing (not 0 x -inf)
       }
       zl += expf(s * inv_tl);
       zh += expf(s * inv_th);
@@ -455,9 +455,6 @@ __device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t addr) {
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ void ld_dsmem_2u64(uint32_t addr, unsigned long long& a, unsigned long long& b) {
-  asm volatile("ld.shared::cluster.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr) : "memory");
-}
 
 // ---- top-p inside the row's cluster ------------------------------------------------
 // Masses are integers, floor(2^a x mscale) with a = (l - max) log2(e) / T, so
@@ -475,12 +472,13 @@ constexpr int kSubBins = 256;          // rank 0 splits the crossing bin into 25
 constexpr float kBinsPerOctave = 64.0f;
 
 // floor(x) for 0 <= x < 2^63 with integer operations only (a 64-bit conversion
-// instruction runs on this GPU's narrow FP64 pipe).  x below 1 gives 0.
+// instruction runs on this GPU's narrow FP64 pipe).  x below 1, from 2^63 up,
+// infinite, NaN or negative gives 0.
 __device__ __forceinline__ unsigned long long mass_bits(float x) {
   const uint32_t b = __float_as_uint(x);
-  const int sh = (int)(b >> 23) - 150;                // x = mant 2^sh for 1 <= x
+  const int sh = (int)(b >> 23) - 150;                // x = mant 2^sh for 1 <= x, -23 <= sh <= 39
   const unsigned long long mant = (b & 0x7FFFFFu) | 0x800000u;
-  return b < 0x3F800000u ? 0ull : (sh >= 0 ? mant << sh : mant >> -sh);
+  return (b < 0x3F800000u || b >= 0x5F000000u) ? 0ull : (sh >= 0 ? mant << sh : mant >> -sh);
 }
 
 // ceil(p z) (up) or floor(p z), exactly, for a float 0 <= p <= 1 and z < 2^63:
@@ -579,15 +577,23 @@ __device__ __forceinline__ int warp_cross256(const uint32_t* r32, unsigned long 
   return __shfl_sync(0xffffffffu, dg, ls);
 }
 
+// The integer mass of logit l at T (cT = log2(e) / T): mass_bits(2^a mscale)
+// with a = (l - max) cT.  Every use evaluates the same expression, so every
+// bin, sum and scan sees the same integers.
+__device__ __forceinline__ unsigned long long cluster_mass(float l, float gm, float cT, float ms) {
+  return mass_bits(exp2f((l - gm) * cT) * ms);
+}
+
 // The token in this CTA given the boundary key, the target within the CTA's
 // kept mass and each thread's kept mass `mine`: token = min{ i : P_i > tloc },
 // P the running kept mass in index order (P > u Zk <=> P > floor(u Zk) for
 // integers).  The warp from the per-warp kept masses, the lane from the
 // threads' totals, then the lane's logits one per lane of the warp.  Returns
-// the token in every lane of the chosen warp, -1 elsewhere.
+// the token in every lane of the chosen warp, -1 elsewhere.  s_v holds logit k
+// of thread t at k 1024 + t.
 template <int PER>
-__device__ __forceinline__ int nucleus_select(const float (&v)[PER], int i0, int hi, const float* s_mx, uint32_t kstar,
-                                              unsigned long long tloc, unsigned long long mine) {
+__device__ __forceinline__ int nucleus_select(const float* s_v, int i0, int hi, float gm, float cT, float ms,
+                                              uint32_t kstar, unsigned long long tloc, unsigned long long mine) {
   __shared__ unsigned long long s_pw[kCWarps];
   __shared__ int s_wsel;
   __shared__ unsigned long long s_wtl;
@@ -615,15 +621,9 @@ __device__ __forceinline__ int nucleus_select(const float (&v)[PER], int i0, int
   // lane j takes logit j of lane lsel
   const unsigned long long base = __shfl_sync(0xffffffffu, incl - mine, lsel);
   const int is = __shfl_sync(0xffffffffu, i0, lsel);
-  float lj = 0.0f;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const float x = __shfl_sync(0xffffffffu, v[j], lsel);
-    if (lane == j) lj = x;
-  }
   const bool live = lane < PER && is + lane < hi;
-  const unsigned long long mj =
-      (live && nucleus_key(lj) <= kstar) ? mass_bits(s_mx[lane * kCThreads + 32 * warp + lsel]) : 0ull;
+  const float lj = live ? s_v[lane * kCThreads + 32 * warp + lsel] : 0.0f;
+  const unsigned long long mj = (live && nucleus_key(lj) <= kstar) ? cluster_mass(lj, gm, cT, ms) : 0ull;
   const unsigned long long run = base + warp_incl_u64(mj);
   const unsigned h2 = __ballot_sync(0xffffffffu, live && run > tl);
   const unsigned lv = __ballot_sync(0xffffffffu, live);
@@ -633,13 +633,15 @@ __device__ __forceinline__ int nucleus_select(const float (&v)[PER], int i0, int
 
 // The same, each thread's kept mass summed over all its logits.
 template <int PER>
-__device__ __forceinline__ int nucleus_pick(const float (&v)[PER], int i0, int hi, const float* s_mx, uint32_t kstar,
-                                            unsigned long long tloc) {
+__device__ __forceinline__ int nucleus_pick(const float* s_v, int i0, int hi, float gm, float cT, float ms,
+                                            uint32_t kstar, unsigned long long tloc) {
   unsigned long long mine = 0ull;
-#pragma unroll
-  for (int k = 0; k < PER; ++k)
-    if (i0 + k < hi && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + threadIdx.x]);
-  return nucleus_select<PER>(v, i0, hi, s_mx, kstar, tloc, mine);
+#pragma unroll 4
+  for (int k = 0; k < PER; ++k) {
+    const float l = s_v[k * kCThreads + threadIdx.x];
+    if (i0 + k < hi && nucleus_key(l) <= kstar) mine += cluster_mass(l, gm, cT, ms);
+  }
+  return nucleus_select<PER>(s_v, i0, hi, gm, cT, ms, kstar, tloc, mine);
 }
 
 // The boundary key by a three-level radix search over the order keys (11, 11
@@ -649,11 +651,12 @@ __device__ __forceinline__ int nucleus_pick(const float (&v)[PER], int i0, int h
 // slice holds the crossing finds the digit and pushes it to every CTA; a third
 // barrier publishes it.  Then the CTAs' kept masses are exchanged and the CTA
 // holding floor(u Zk) picks the token.  Used when the crossing log-mass bin
-// holds more keys than the gather below has room for (large ties).
+// holds more keys than the gather below has room for (large ties); kept out
+// of line, off the common path's code.
 template <int PER>
-__device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int i0, int hi, const Params& p,
-                                                     uint32_t rank, int CS, float u_row, unsigned long long* s_hist,
-                                                     const float* s_mx) {
+__device__ __noinline__ int cluster_nucleus_radix(const float* s_v, int i0, int hi, float gm, float cT, float ms,
+                                                  float top_p, uint32_t rank, int CS, float u_row,
+                                                  unsigned long long* s_hist) {
   __shared__ unsigned long long s_slice[kMaxClusterCtas];  // per CTA: its slice total (levels), its kept mass
   __shared__ unsigned long long s_res[3];          // the level's digit, mass below it, mass of its bin
   __shared__ unsigned long long s_w64[kCWarps], s_wex[kCWarps];
@@ -667,14 +670,15 @@ __device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int 
     const int nb = level == 2 ? 1024 : kHistBins;
     for (int b = t; b < kHistBins; b += kCThreads) s_hist[b] = 0ull;
     __syncthreads();
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < PER; ++k) {
+      const float l = s_v[k * kCThreads + t];
       if (i0 + k < hi) {
-        const uint32_t key = nucleus_key(v[k]);
+        const uint32_t key = nucleus_key(l);
         const bool match = level == 0 ? true : level == 1 ? (key >> 21) == prefix : (key >> 10) == prefix;
         if (match) {
           const uint32_t d = level == 0 ? key >> 21 : level == 1 ? (key >> 10) & 0x7FFu : key & 0x3FFu;
-          hist_add_u64(h32, kHistBins, (int)d, mass_bits(s_mx[k * kCThreads + t]));
+          hist_add_u64(h32, kHistBins, (int)d, cluster_mass(l, gm, cT, ms));
         }
       }
     }
@@ -721,7 +725,7 @@ __device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int 
       unsigned long long z = 0ull;
       for (int r = 0; r < CS; ++r) z += s_slice[r];
       // z >= 1: the maximum's mass is mscale; the target is in [1, z]
-      const unsigned long long tg = scale_u64(p.top_p, z, true);
+      const unsigned long long tg = scale_u64(top_p, z, true);
       target = tg < 1ull ? 1ull : (tg > z ? z : tg);
     }
     // the slice holding the crossing: the first whose running total reaches the target
@@ -781,9 +785,11 @@ __device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int 
 
   // ---- the CTAs' kept masses, then the CTA holding floor(u Zk) ----
   unsigned long long mine = 0ull;
-#pragma unroll
-  for (int k = 0; k < PER; ++k)
-    if (i0 + k < hi && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + t]);
+#pragma unroll 1
+  for (int k = 0; k < PER; ++k) {
+    const float l = s_v[k * kCThreads + t];
+    if (i0 + k < hi && nucleus_key(l) <= kstar) mine += cluster_mass(l, gm, cT, ms);
+  }
   const unsigned long long ws = warp_sum_u64(mine);
   if (lane == 0) s_w64[warp] = ws;
   __syncthreads();
@@ -805,20 +811,61 @@ __device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int 
     pre += s_slice[r];
   }
   if ((int)rank != rstar) return -1;
-  return nucleus_pick<PER>(v, i0, hi, s_mx, kstar, tgt - pre);
+  return nucleus_select<PER>(s_v, i0, hi, gm, cT, ms, kstar, tgt - pre, mine);
+}
+
+// Rank 0, when more than 32 gathered keys share the crossing sub-bin (ties,
+// or a dense bin): the boundary key by eight key bits a round over the
+// sub-bin's keys, from acc (the mass of the gathered keys in lower sub-bins).
+// Every thread of rank 0 calls it; out of line, off the common path's code.
+__device__ __noinline__ uint32_t gathered_radix(const uint32_t* s_ck, const unsigned long long* s_cm,
+                                                const uint8_t* s_cb, const unsigned int* s_ccnt, int Cr, int CS,
+                                                int sbs, unsigned long long acc, unsigned long long need,
+                                                unsigned long long* s_rh, unsigned long long* s_sel) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  uint32_t* r32 = reinterpret_cast<uint32_t*>(s_rh);
+  uint32_t prefix = 0u;
+#pragma unroll 1
+  for (int round = 0; round < 4; ++round) {
+    const int sh = 24 - 8 * round;
+    if (t < kSubBins) s_rh[t] = 0ull;
+    __syncthreads();
+    for (int r = 0; r < CS; ++r) {
+      const int n = (int)s_ccnt[r];
+      for (int j = t; j < n; j += kCThreads) {
+        const int s = r * Cr + j;
+        const uint32_t key = s_ck[s];
+        if ((int)s_cb[s] == sbs && s_cm[s] && (round == 0 || (key >> (sh + 8)) == prefix))
+          hist_add_u64(r32, kSubBins, (int)((key >> sh) & 0xFFu), s_cm[s]);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long before;
+      const int dg = warp_cross256(r32, acc, need, &before);
+      if (lane == 0) {
+        s_sel[0] = (unsigned long long)dg;
+        s_sel[1] = before;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | (uint32_t)s_sel[0];
+    acc = s_sel[1];
+    __syncthreads();
+  }
+  return prefix;
 }
 
 // Top-p inside the row's cluster (every CTA of the cluster calls it, with T
 // known), in three cluster barriers:
-//  1. each CTA evaluates its logits' masses once and bins them by log-mass
-//     (1/64 octave a bin, exact integer totals) in shared memory, with the
-//     totals of 64 super-bins of 32 bins; barrier;
-//  2. in every CTA one warp reads the 64 super-bin totals of every CTA, finds
-//     the super-bin where the running mass reaches ceil(top_p Z), then reads
-//     its 32 bins of every CTA and finds the crossing bin -- the same in every
-//     CTA; each CTA sends rank 0 its mass before that bin and, for each of its
-//     logits inside it, the order key, the mass and a sub-bin (1/256 of the
-//     bin); barrier;
+//  1. each CTA bins its logits' masses by log-mass (1/64 octave a bin, exact
+//     integer totals) in shared memory, with the totals of 64 super-bins of
+//     32 bins, pushed to every CTA; barrier;
+//  2. in every CTA one warp finds the super-bin where the running mass
+//     reaches ceil(top_p Z), then reads its 32 bins of every CTA and finds the
+//     crossing bin -- the same in every CTA; each CTA sends rank 0 its mass
+//     before that bin and, for each of its logits inside it, the order key,
+//     the mass and a sub-bin (1/256 of the bin); barrier;
 //  3. rank 0 finds the boundary key among the gathered ones: a histogram of
 //     the 256 sub-bins, then an exact comparison of the keys in the crossing
 //     sub-bin (a radix search over the key bits when that holds more than 32);
@@ -830,21 +877,23 @@ __device__ __forceinline__ int cluster_nucleus_radix(const float (&v)[PER], int 
 // logits; if some CTA finds more than its share of kCand, every CTA runs the
 // radix search above instead.
 //
-// Dynamic shared memory: PER x 1024 floats (2^a mscale of logit k of thread t
-// at k 1024 + t), then rank 0's gathered masses, keys and sub-bins.
+// The logits are read from shared memory (s_v: logit k of thread t at
+// k 1024 + t), not registers, which the 1024-thread CTA has 64 of a thread.
+// Dynamic shared memory: the logits, then rank 0's gathered masses, keys and
+// sub-bins.
 template <int PER>
 constexpr size_t cluster_nucleus_smem() {
   return (size_t)PER * kCThreads * sizeof(float) + (size_t)kCand * (sizeof(unsigned long long) + sizeof(uint32_t) + 1);
 }
 
 template <int PER>
-__device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, int hi, float gm, float cT,
-                                               const Params& p, uint32_t rank, int CS, float u_row) {
+__device__ __forceinline__ int cluster_nucleus(const float* s_v, int i0, int hi, float gm, float cT, const Params& p,
+                                               uint32_t rank, int CS, float u_row) {
   static_assert(kHistBins == 2 * kCThreads && kSuper == 64, "two bins a thread, two super-bins a lane");
   static_assert(PER <= 32, "one match bit (and one lane of the pick) a logit");
   static_assert(kCThreads >= kSubBins && kCand % kCThreads == 0, "one sub-bin a thread");
   __shared__ __align__(16) unsigned long long s_hist[kHistBins];  // this CTA's bins (32-bit words while binning)
-  __shared__ __align__(16) unsigned long long s_sup[kSuper];      // this CTA's super-bin totals
+  __shared__ unsigned long long s_sup[kMaxClusterCtas][kSuper];   // every CTA's super-bin totals
   __shared__ unsigned int s_ccnt[kMaxClusterCtas];      // rank 0: how many logits CTA r sent
   __shared__ unsigned long long s_cmass[kMaxClusterCtas];  // rank 0: CTA r's mass before the crossing bin
   __shared__ unsigned long long s_kept[kMaxClusterCtas];   // rank 0: CTA r's kept mass
@@ -860,7 +909,6 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
   __shared__ unsigned long long s_fin[2];               // from rank 0: the boundary key, the target in this CTA
   __shared__ unsigned int s_status;                     // from rank 0: 0 done, 1 pick the token, 2 radix search
   extern __shared__ __align__(16) unsigned char s_dyn[];
-  float* s_mx = reinterpret_cast<float*>(s_dyn);
   unsigned long long* s_cm = reinterpret_cast<unsigned long long*>(s_dyn + (size_t)PER * kCThreads * sizeof(float));
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_cm + kCand);
   uint8_t* s_cb = reinterpret_cast<uint8_t*>(s_ck + kCand);
@@ -869,19 +917,15 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
   uint32_t* h32 = reinterpret_cast<uint32_t*>(s_hist);
   const int b0 = 2 * t;                                 // this thread's two bins
 
-  // ---- 1. masses, this CTA's log-mass histogram and super-bin totals ----
+  // ---- 1. this CTA's log-mass histogram and super-bin totals ----
   s_hist[b0] = 0ull;
   s_hist[b0 + 1] = 0ull;
   __syncthreads();
-#pragma unroll
+#pragma unroll 4
   for (int k = 0; k < PER; ++k) {
-    if (i0 + k < hi) {
-      const float a = (v[k] - gm) * cT;
-      const float x = exp2f(a) * ms;
-      s_mx[k * kCThreads + t] = x;
-      const unsigned long long m = mass_bits(x);
-      if (m) hist_add_u64(h32, kHistBins, logmass_bin(a), m);
-    }
+    const float a = (s_v[k * kCThreads + t] - gm) * cT;
+    const unsigned long long m = mass_bits(exp2f(a) * ms);
+    if (i0 + k < hi && m) hist_add_u64(h32, kHistBins, logmass_bin(a), m);
   }
   __syncthreads();
   {                                                     // fold the words into 64-bit bins in place
@@ -890,29 +934,24 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
     __syncthreads();
     s_hist[b0] = c0;
     s_hist[b0 + 1] = c1;
-    // lanes 0-15 of warp w hold super-bin 2w, lanes 16-31 super-bin 2w + 1
+    // lanes 0-15 of warp w hold super-bin 2w, lanes 16-31 super-bin 2w + 1:
+    // pushed to every CTA of the cluster
     unsigned long long sp = c0 + c1;
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
-    if ((lane & 15) == 0) s_sup[2 * warp + (lane >> 4)] = sp;
+    if ((lane & 15) == 0)
+      for (int r = 0; r < CS; ++r) st_dsmem_u64(dsmem_addr(&s_sup[rank][2 * warp + (lane >> 4)], (uint32_t)r), sp);
   }
-  cluster_sync();                                       // every CTA's bins are complete
+  cluster_sync();                                       // every CTA's bins and super-bin totals are in place
 
   // ---- 2. warp 0: the crossing super-bin, then the crossing bin ----
   if (warp == 0) {
     unsigned long long sa = 0ull, sb = 0ull;
-    {
-      unsigned long long q0[kMaxClusterCtas], q1[kMaxClusterCtas];
 #pragma unroll
-      for (int r = 0; r < kMaxClusterCtas; ++r) {
-        q0[r] = 0ull;
-        q1[r] = 0ull;
-        if (r < CS) ld_dsmem_2u64(dsmem_addr(&s_sup[2 * lane], (uint32_t)r), q0[r], q1[r]);
-      }
-#pragma unroll
-      for (int r = 0; r < kMaxClusterCtas; ++r) {
-        sa += q0[r];
-        sb += q1[r];
+    for (int r = 0; r < kMaxClusterCtas; ++r) {
+      if (r < CS) {
+        sa += s_sup[r][2 * lane];
+        sb += s_sup[r][2 * lane + 1];
       }
     }
     const unsigned long long lt = sa + sb;
@@ -949,22 +988,27 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
   const unsigned long long below = s_x[1], target = s_x[2];
 
   // ---- this CTA's mass before the crossing bin and its logits inside it -> rank 0 ----
+  // -64 a is an exact scaling, so the bin test d <= -64 a < d + 1 is
+  // a <= -d/64 and a > -(d + 1)/64 (the last bin has no lower end); NaN is
+  // in neither, and has no mass.
   const int Cr = (kCand / CS) & ~31;                    // logits a CTA may send
   const unsigned long long mb = (b0 < dstar ? s_hist[b0] : 0ull) + (b0 + 1 < dstar ? s_hist[b0 + 1] : 0ull);
+  const float a_hi = (float)dstar * (-1.0f / kBinsPerOctave);
+  const float a_lo = dstar == kHistBins - 1 ? -INFINITY : (float)(dstar + 1) * (-1.0f / kBinsPerOctave);
   uint32_t match = 0u, lower = 0u;                      // logits in / before the crossing bin
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
+    const float a = (s_v[k * kCThreads + t] - gm) * cT;
     if (i0 + k < hi) {
-      const int d = logmass_bin((v[k] - gm) * cT);
-      if (d == dstar) match |= 1u << k;
-      if (d < dstar) lower |= 1u << k;
+      if (a <= a_hi && a > a_lo) match |= 1u << k;
+      if (a > a_hi) lower |= 1u << k;
     }
   }
   const unsigned int cnt = __popc(match);
   const unsigned int ci = warp_incl_u32(cnt);
   const unsigned long long mw = warp_sum_u64(mb);
   if (lane == 31) s_wcnt[warp] = ci;
-  if (lane == 0) s_w64[warp] = mw;                      // (its last reader passed two barriers ago)
+  if (lane == 0) s_w64[warp] = mw;
   __syncthreads();
   if (warp == 0) {
     const unsigned int wc = s_wcnt[lane];
@@ -980,20 +1024,22 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
   __syncthreads();
   if (match) {
     unsigned int slot = s_wcnt[warp] + ci - cnt;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      if ((match >> k) & 1u) {
-        if (slot < (unsigned)Cr) {
-          const int j = (int)rank * Cr + (int)slot;
-          // sub-bin: the fraction of -64 a past the bin's start, x 256 (exact steps)
-          const float f = ((v[k] - gm) * cT * -kBinsPerOctave - (float)dstar) * (float)kSubBins;
-          const uint32_t sbin = f < (float)(kSubBins - 1) ? (uint32_t)f : (uint32_t)(kSubBins - 1);
-          st_dsmem_u64(dsmem_addr(&s_cm[j], 0u), mass_bits(s_mx[k * kCThreads + t]));
-          st_dsmem_u32(dsmem_addr(&s_ck[j], 0u), nucleus_key(v[k]));
-          st_dsmem_u8(dsmem_addr(&s_cb[j], 0u), sbin);
-        }
-        ++slot;
+    uint32_t mm = match;
+    while (mm) {
+      const int k = __ffs(mm) - 1;
+      mm &= mm - 1u;
+      if (slot < (unsigned)Cr) {
+        const int j = (int)rank * Cr + (int)slot;
+        const float l = s_v[k * kCThreads + t];
+        const float a = (l - gm) * cT;
+        // sub-bin: the fraction of -64 a past the bin's start, x 256 (exact steps)
+        const float f = (a * -kBinsPerOctave - (float)dstar) * (float)kSubBins;
+        const uint32_t sbin = f < (float)(kSubBins - 1) ? (uint32_t)f : (uint32_t)(kSubBins - 1);
+        st_dsmem_u64(dsmem_addr(&s_cm[j], 0u), mass_bits(exp2f(a) * ms));
+        st_dsmem_u32(dsmem_addr(&s_ck[j], 0u), nucleus_key(l));
+        st_dsmem_u8(dsmem_addr(&s_cb[j], 0u), sbin);
       }
+      ++slot;
     }
   }
   cluster_sync();                                       // the gathered logits and masses are on rank 0
@@ -1016,10 +1062,13 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
         int r = 0;
 #pragma unroll
         for (int i = 1; i < kMaxClusterCtas; ++i) r += s >= i * Cr ? 1 : 0;
+        const uint32_t kk = s_ck[s];                    // (slots past a CTA's count hold stale words)
+        const unsigned long long mm = s_cm[s];
+        const int bb = (int)s_cb[s];
         const bool ok = r < CS && s - r * Cr < (int)s_ccnt[r];
-        ck[q] = ok ? s_ck[s] : 0xFFFFFFFFu;
-        cm[q] = ok ? s_cm[s] : 0ull;
-        csb[q] = ok ? (int)s_cb[s] : -1;
+        ck[q] = ok ? kk : 0xFFFFFFFFu;
+        cm[q] = ok ? mm : 0ull;
+        csb[q] = ok ? bb : -1;
       }
       // The smallest key K with (mass of gathered keys <= K) >= target - below.
       // Sub-bins never decrease with the key, so every key of a lower sub-bin
@@ -1050,7 +1099,7 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
       }
       __syncthreads();
       const int sbs = (int)s_sel[0];
-      unsigned long long acc = s_sel[1];
+      const unsigned long long acc = s_sel[1];
       const unsigned int n32 = s_rc[sbs];
       uint32_t kstar;
       if (n32 <= 32u) {
@@ -1083,32 +1132,7 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
         __syncthreads();
         kstar = (uint32_t)s_sel[2];
       } else {
-        // many keys in one sub-bin (ties, or a dense bin): eight key bits a round
-        uint32_t prefix = 0u;
-#pragma unroll 1
-        for (int round = 0; round < 4; ++round) {
-          const int sh = 24 - 8 * round;
-          if (t < kSubBins) s_rh[t] = 0ull;
-          __syncthreads();
-#pragma unroll
-          for (int q = 0; q < kQ; ++q)
-            if (csb[q] == sbs && cm[q] && (round == 0 || (ck[q] >> (sh + 8)) == prefix))
-              hist_add_u64(r32, kSubBins, (int)((ck[q] >> sh) & 0xFFu), cm[q]);
-          __syncthreads();
-          if (warp == 0) {
-            unsigned long long before;
-            const int dg = warp_cross256(r32, acc, need, &before);
-            if (lane == 0) {
-              s_sel[0] = (unsigned long long)dg;
-              s_sel[1] = before;
-            }
-          }
-          __syncthreads();
-          prefix = (prefix << 8) | (uint32_t)s_sel[0];
-          acc = s_sel[1];
-          __syncthreads();
-        }
-        kstar = prefix;
+        kstar = gathered_radix(s_ck, s_cm, s_cb, s_ccnt, Cr, CS, sbs, acc, need, s_rh, s_sel);
       }
       // each CTA's kept mass: its mass before the bin + its gathered keys <= kstar
       // (warp r sums CTA r's range)
@@ -1139,24 +1163,34 @@ __device__ __forceinline__ int cluster_nucleus(const float (&v)[PER], int i0, in
       }
     }
   } else {
-#pragma unroll
-    for (int k = 0; k < PER; ++k)
-      if ((lower >> k) & 1u) mine += mass_bits(s_mx[k * kCThreads + t]);
+    uint32_t lw = lower;
+    while (lw) {
+      const int k = __ffs(lw) - 1;
+      lw &= lw - 1u;
+      mine += cluster_mass(s_v[k * kCThreads + t], gm, cT, ms);
+    }
   }
   cluster_sync();                                       // the verdict is in every CTA
   const unsigned int status = s_status;
-  if (status == 2u) return cluster_nucleus_radix<PER>(v, i0, hi, p, rank, CS, u_row, s_hist, s_mx);
+  if (status == 2u) return cluster_nucleus_radix<PER>(s_v, i0, hi, gm, cT, ms, p.top_p, rank, CS, u_row, s_hist);
   if (status != 1u) return -1;
   const uint32_t kstar = (uint32_t)s_fin[0];
   if (rank == 0) {
-#pragma unroll
-    for (int k = 0; k < PER; ++k)
-      if ((lower >> k) & 1u) mine += mass_bits(s_mx[k * kCThreads + t]);
+    uint32_t lw = lower;
+    while (lw) {
+      const int k = __ffs(lw) - 1;
+      lw &= lw - 1u;
+      mine += cluster_mass(s_v[k * kCThreads + t], gm, cT, ms);
+    }
   }
-#pragma unroll
-  for (int k = 0; k < PER; ++k)
-    if (((match >> k) & 1u) && nucleus_key(v[k]) <= kstar) mine += mass_bits(s_mx[k * kCThreads + t]);
-  return nucleus_select<PER>(v, i0, hi, s_mx, kstar, s_fin[1], mine);
+  uint32_t mw2 = match;
+  while (mw2) {
+    const int k = __ffs(mw2) - 1;
+    mw2 &= mw2 - 1u;
+    const float l = s_v[k * kCThreads + t];
+    if (nucleus_key(l) <= kstar) mine += cluster_mass(l, gm, cT, ms);
+  }
+  return nucleus_select<PER>(s_v, i0, hi, gm, cT, ms, kstar, s_fin[1], mine);
 }
 
 template <int PER, bool NUC>
@@ -1172,11 +1206,10 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
   constexpr float kLog2e = 1.4426950408889634f;
   __shared__ float s_wmax[kCWarps];
   __shared__ float s_wred[5][kCWarps];              // per warp: n0, z1, a1, Z_T at T_low, at T_high
-  __shared__ float s_peer_max[kMaxClusterCtas];
-  __shared__ float s_peer[kMaxClusterCtas][5];      // per CTA: the same five sums
+  __shared__ float s_peer[kMaxClusterCtas][6];      // per CTA: its maximum, then the same five sums
   __shared__ double s_ring_rest;                    // the window's other w - 1 entropies
   __shared__ RowState s_st;
-  __shared__ float s_T;
+  __shared__ float s_T, s_gm;
   __shared__ int s_warp, s_rstar, s_zi;
   __shared__ float s_tl;
 
@@ -1205,8 +1238,16 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
 #pragma unroll
     for (int k = 0; k < PER; ++k) v[k] = (i0 + k < hi) ? __ldg(base + i0 + k) : -INFINITY;
   }
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  if constexpr (NUC) {                              // top-p reads the logits from shared memory
+    float* s_v = reinterpret_cast<float*>(s_dyn);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) s_v[k * kCThreads + threadIdx.x] = v[k];
+  }
 
-  // ---- row maximum ----
+  // ---- this CTA's maximum: the sums below are relative to it, and thread 0
+  // rescales each CTA's sums to the row maximum, so the maximum and the sums
+  // cross the cluster in one exchange ----
   float mx = -INFINITY;
 #pragma unroll
   for (int k = 0; k < PER; ++k) mx = fmaxf(mx, v[k]);
@@ -1214,14 +1255,7 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
   if (lane == 0) s_wmax[warp] = mx;
   __syncthreads();
   mx = warp_max(s_wmax[lane]);                      // every warp reduces the 32 warp maxima itself
-  if (CS > 1) {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (threadIdx.x < CS) st_dsmem_f32(dsmem_addr(&s_peer_max[rank], threadIdx.x), mx);
-    __syncwarp();
-    cluster_sync();
-    mx = warp_max(lane < CS ? s_peer_max[lane] : -INFINITY);
-  }
-  const float gm = mx;
+  const float mb = (mx == -INFINITY) ? 0.0f : mx;   // a CTA of -inf logits sums zeros
 
   // The row state (every CTA derives T from it; rank 0 updates it after the
   // last cluster barrier, when every CTA has read it): the last warp reads it,
@@ -1252,13 +1286,13 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     if (i0 + k < hi) {
-      const float s = v[k] - gm;
+      const float s = v[k] - mb;
       if (s == 0.0f) {
         n0 += 1.0f;
       } else {
         const float e = exp2f(s * kLog2e);
         z1 += e;
-        a1 += e * s;
+        if (e > 0.0f) a1 += e * s;                  // a -inf logit adds nothing (not 0 x -inf)
       }
       if constexpr (!NUC) {                         // top-p forms its own masses at the chosen T
         zl += exp2f(s * cl);
@@ -1276,12 +1310,13 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
     for (int i = 0; i < 5; ++i) s_wred[i][warp] = f[i];
   }
   __syncthreads();
-  if (warp == 0) {                                  // this CTA's five sums over its 32 warps
+  if (CS > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer runs: remote stores allowed
+  if (warp == 0) {                                  // this CTA's maximum and five sums over its 32 warps
     float g[5];
 #pragma unroll
     for (int i = 0; i < 5; ++i) g[i] = warp_sum(s_wred[i][lane]);
-    if (lane < 5) {
-      const float acc = lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : lane == 3 ? g[3] : g[4];
+    if (lane < 6) {
+      const float acc = lane == 0 ? mx : lane == 1 ? g[0] : lane == 2 ? g[1] : lane == 3 ? g[2] : lane == 4 ? g[3] : g[4];
       if (CS > 1) {
         for (int r = 0; r < CS; ++r) st_dsmem_f32(dsmem_addr(&s_peer[rank][lane], r), acc);
       } else {
@@ -1293,90 +1328,117 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
   if (CS > 1) cluster_sync();
   else __syncthreads();
 
-  // ---- H, the state rule and T (thread 0; every CTA the same).  Row sums in
-  // FP32 in CTA order; Z - 1 is (the maxima counted - 1) + the rest, so a
-  // nearly one-hot row keeps its relative precision.  The state sums are
-  // FP64 ----
-  if (threadIdx.x == 0) {
-    float cnt = 0.f, rest = 0.f, A = 0.f, ztl = 0.f, zth = 0.f;
-    for (int r = 0; r < CS; ++r) {
-      cnt += s_peer[r][0];
-      rest += s_peer[r][1];
-      A += s_peer[r][2];
-      ztl += s_peer[r][3];
-      zth += s_peer[r][4];
-    }
-    const float zm1 = (cnt - 1.0f) + rest;
-    const double H = (double)(log1pf(zm1) - A / (1.0f + zm1));
-    RowState ns = s_st;
-    const int w = p.w;
-    const bool state_ok = (ns.w == w);
-    bool low = false;
-    int t1 = 0, j = 0;
-    if (state_ok) {
-      if (ns.t == 0 || (step_start && step_start[row])) {
-        ns.j = 0;
-        ns.step_sum = 0.0;
-      }
-      ns.glob_sum += H;
-      ns.step_sum += H;
-      t1 = ns.t + 1;
-      j = ns.j;
-      // The window mean is wsum / wn: the whole history while t1 <= w.
-      const double wsum = (t1 > w) ? s_ring_rest + H : ns.glob_sum;
-      const int wn = (t1 > w) ? w : t1;
-      // H_step = ssum / sn; H_bar = glob_sum / t1.  Means are compared by
-      // cross-multiplying (the counts are positive).
-      const double ssum = (j < w) ? wsum : ns.step_sum;
-      const int sn = (j < w) ? wn : j + 1;
-      bool above;                                   // H >= tau (then T_high)
-      if (p.threshold == RESET_THRESHOLD_FIXED) {
-        above = !(H < (double)p.tau0);
-      } else if (p.threshold == RESET_THRESHOLD_WINDOW) {
-        above = !(H * wn < wsum);
+  // ---- the row maximum, H, the state rule and T (warp 0; every CTA the
+  // same).  Lane r rescales CTA r's FP32 sums by e^(its maximum - the row
+  // maximum), its A also gaining that difference x its Z; the lanes' sums are
+  // reduced in a fixed order.  Z - 1 is (the row maxima counted - 1) + the
+  // rest, so a nearly one-hot row keeps its relative precision.  Lane 0
+  // applies the state rule, with FP64 sums ----
+  if (warp == 0) {
+    const bool has = lane < CS;
+    const float mr = has ? s_peer[lane][0] : -INFINITY;
+    const float gmax = warp_max(mr);
+    const bool live = has && mr != -INFINITY;       // a CTA of only -inf logits has no mass
+    const float d = live ? mr - gmax : 0.0f;
+    const float fl = live ? exp2f(d * cl) : 0.0f, fh = live ? exp2f(d * ch) : 0.0f;
+    float c_cnt = 0.f, c_rest = 0.f, c_A = 0.f;
+    if (live) {
+      const float n0r = s_peer[lane][1], z1r = s_peer[lane][2], a1r = s_peer[lane][3];
+      if (d == 0.0f) {
+        c_cnt = n0r;
+        c_rest = z1r;
+        c_A = a1r;
       } else {
-        const bool confident = ssum * t1 <= ns.glob_sum * sn;   // H_step <= H_bar
-        above = confident ? !(H < (double)p.tau0) : !(H * sn < ssum);
+        const float f = exp2f(d * kLog2e), zr = n0r + z1r;
+        c_rest = f * zr;
+        c_A = f * (a1r + d * zr);
       }
-      low = !above;
     }
-    const float T = low ? p.t_low : p.t_high;
-    s_T = T;
-    if (rank == 0) {
-      if (!state_ok) atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
+    const float zlr = live ? fl * s_peer[lane][4] : 0.0f, zhr = live ? fh * s_peer[lane][5] : 0.0f;
+    const float cnt = warp_sum(c_cnt), rest = warp_sum(c_rest), A = warp_sum(c_A);
+    const float ztl = warp_sum(zlr), zth = warp_sum(zhr);
+    int low = 0;
+    if (lane == 0) {
+      const float zm1 = (cnt - 1.0f) + rest;
+      const double H = (double)(log1pf(zm1) - A / (1.0f + zm1));
+      RowState ns = s_st;
+      const int w = p.w;
+      const bool state_ok = (ns.w == w);
+      int t1 = 0, j = 0;
       if (state_ok) {
-        RowState* stw = reinterpret_cast<RowState*>(state + (size_t)row * stride);
-        reinterpret_cast<double*>(stw + 1)[ns.t % w] = H;
-        stw->glob_sum = ns.glob_sum;
-        stw->step_sum = ns.step_sum;
-        stw->t = t1;
-        stw->j = j + 1;
+        if (ns.t == 0 || (step_start && step_start[row])) {
+          ns.j = 0;
+          ns.step_sum = 0.0;
+        }
+        ns.glob_sum += H;
+        ns.step_sum += H;
+        t1 = ns.t + 1;
+        j = ns.j;
+        // The window mean is wsum / wn: the whole history while t1 <= w.
+        const double wsum = (t1 > w) ? s_ring_rest + H : ns.glob_sum;
+        const int wn = (t1 > w) ? w : t1;
+        // H_step = ssum / sn; H_bar = glob_sum / t1.  Means are compared by
+        // cross-multiplying (the counts are positive).
+        const double ssum = (j < w) ? wsum : ns.step_sum;
+        const int sn = (j < w) ? wn : j + 1;
+        bool above;                                   // H >= tau (then T_high)
+        if (p.threshold == RESET_THRESHOLD_FIXED) {
+          above = !(H < (double)p.tau0);
+        } else if (p.threshold == RESET_THRESHOLD_WINDOW) {
+          above = !(H * wn < wsum);
+        } else {
+          const bool confident = ssum * t1 <= ns.glob_sum * sn;   // H_step <= H_bar
+          above = confident ? !(H < (double)p.tau0) : !(H * sn < ssum);
+        }
+        low = !above;
       }
-      if (H_out) H_out[row] = (float)H;
-      if (T_out) T_out[row] = T;
+      const float T = low ? p.t_low : p.t_high;
+      if (rank == 0) {
+        if (!state_ok) atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_STATE_W);
+        if (state_ok) {
+          RowState* stw = reinterpret_cast<RowState*>(state + (size_t)row * stride);
+          reinterpret_cast<double*>(stw + 1)[ns.t % w] = H;
+          stw->glob_sum = ns.glob_sum;
+          stw->step_sum = ns.step_sum;
+          stw->t = t1;
+          stw->j = j + 1;
+        }
+        if (H_out) H_out[row] = (float)H;
+        if (T_out) T_out[row] = T;
+      }
     }
+    low = __shfl_sync(0xffffffffu, low, 0);
     // The CTA that holds u * Z_T: the first whose running total passes the
-    // target (the last CTA if rounding leaves the target at or past the total).
-    const int zi = low ? 3 : 4;
+    // target, else the last CTA with mass.  The target within it is in its
+    // own units (relative to its maximum), as its per-warp and per-thread
+    // sums are.
+    const float zr = low ? zlr : zhr;
     const float target = __ldg(u + row) * (low ? ztl : zth);
-    float before = 0.f;
-    int rstar = CS - 1;
-    for (int r = 0; r < CS; ++r) {
-      const float z = s_peer[r][zi];
-      if (before + z > target) {
-        rstar = r;
-        break;
-      }
-      before += z;
+    float zi = zr;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, zi, o);
+      if (lane >= o) zi += n;
     }
-    s_rstar = rstar;
-    s_zi = zi;
-    s_tl = target - before;                         // the target within CTA rstar
+    const unsigned hit = __ballot_sync(0xffffffffu, has && zi > target);
+    const unsigned pos = __ballot_sync(0xffffffffu, zr > 0.0f);
+    const int rstar = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const float before = __shfl_sync(0xffffffffu, zi - zr, rstar);
+    const float fsel = __shfl_sync(0xffffffffu, low ? fl : fh, rstar);
+    if (lane == 0) {
+      s_gm = gmax;
+      s_T = low ? p.t_low : p.t_high;
+      s_rstar = rstar;
+      s_zi = low ? 3 : 4;
+      s_tl = fsel > 0.0f ? (target - before) / fsel : 0.0f;   // the target within CTA rstar
+    }
   }
   __syncthreads();
+  const float gm = s_gm;
   if constexpr (NUC) {                              // top-p (NUC is set iff 0 < top_p < 1)
     const float cT = (s_T == p.t_low) ? cl : ch;
-    const int tok = cluster_nucleus<PER>(v, i0, hi, gm, cT, p, rank, CS, __ldg(u + row));
+    const int tok =
+        cluster_nucleus<PER>(reinterpret_cast<const float*>(s_dyn), i0, hi, gm, cT, p, rank, CS, __ldg(u + row));
     if (tok >= 0 && (threadIdx.x & 31) == 0) token[row] = tok;
     return;
   }
@@ -1424,7 +1486,7 @@ __global__ void __launch_bounds__(kCThreads, 1) reset_cluster_kernel(const float
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         if (i0 + k < hi) {
-          run += exp2f((v[k] - gm) * cT);
+          run += exp2f((v[k] - mb) * cT);
           last = i0 + k;
           if (run > tl && tok < 0) tok = i0 + k;
         }

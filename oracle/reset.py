@@ -64,12 +64,15 @@ class ResetParams:
 
 
 def token_entropy(logits: np.ndarray) -> float:
-    """H = ln Z - (sum_i e^{s_i} s_i) / Z with s = l - max l, in FP64 (nats)."""
+    """H = ln Z - (sum_i e^{s_i} s_i) / Z with s = l - max l, in FP64 (nats).
+    A logit of -inf has probability 0 and adds nothing to the sum (the
+    convention 0 log 0 = 0 of H = -sum p log p)."""
     l = np.asarray(logits, dtype=np.float64)
     s = l - np.max(l)
     e = np.exp(s)
     Z = np.sum(e)
-    return float(np.log(Z) - np.sum(e * s) / Z)
+    es = np.multiply(e, s, out=np.zeros_like(e), where=e > 0)
+    return float(np.log(Z) - np.sum(es) / Z)
 
 
 def nucleus_mask(logits: np.ndarray, T: float, top_p: float) -> np.ndarray:

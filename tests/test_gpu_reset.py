@@ -241,6 +241,38 @@ def test_top_p_bf16_valued_logits_full_vocab():
     assert api.device_status() == 0
 
 
+@pytest.mark.parametrize("top_p", [1.0, 0.95])
+def test_masked_logits_full_vocab(top_p):
+    """-inf logits (masked tokens) add nothing to H or Z and are never
+    sampled, including a CTA whose whole range is masked (rows 0 and 2: the
+    last and the first 20480 logits of V = 151936)."""
+    M, V, steps = 4, synth.LM_HEAD_VOCAB, 3
+    sampler = api.ResetSampler(M, V, top_p=top_p)
+    p = R.ResetParams(top_p=_f32(top_p))
+    states = [R.RowState(w=8) for _ in range(M)]
+    us = synth.reset_uniforms(steps, M, seed=14)
+    for t in range(steps):
+        logits = synth.reset_logits(t, M, V, 3.0)
+        logits[0, 143360:] = -np.inf
+        logits[1, ::5] = -np.inf
+        logits[2, :20480] = -np.inf
+        g = torch.Generator().manual_seed(t)
+        logits[3][torch.rand(V, generator=g) < 0.5] = -np.inf
+        tok, H, T = sampler(logits.cuda(), None, torch.from_numpy(us[t]).cuda())
+        torch.cuda.synchronize()
+        tok, H, T = tok.cpu().numpy(), H.cpu().numpy(), T.cpu().numpy()
+        ln = logits.numpy().astype(np.float64)
+        for r in range(M):
+            Hr = R.token_entropy(ln[r])
+            res = R.reset_update(states[r], Hr, t == 0, p)
+            assert abs(H[r] - Hr) <= 1e-4 * max(abs(Hr), 1e-6), (t, r, H[r], Hr)
+            if not R.temperature_is_ambiguous(res, p):
+                assert T[r] == np.float32(res.T), (t, r, T[r], res)
+            assert np.isfinite(ln[r, int(tok[r])]), (t, r, tok[r])
+            assert _token_ok(ln[r], float(T[r]), float(us[t, r]), int(tok[r]), p.top_p), (t, r, tok[r])
+    assert api.device_status() == 0
+
+
 def test_top_p_single_token_nucleus_and_u_extremes():
     """One dominant logit: at top_p <= its probability only it is kept, for
     every u, including u = 0 and the largest float below 1."""

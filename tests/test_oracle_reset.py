@@ -46,6 +46,23 @@ def test_entropy_dominant_and_shift_invariant():
     assert R.token_entropy(x) == pytest.approx(R.token_entropy(x + 40.0), rel=1e-12)
 
 
+def test_entropy_masked_logits_add_nothing():
+    """-inf logits (masked tokens) have probability 0: the entropy is that of
+    the remaining logits, e.g. the binary entropy for two finite ones."""
+    a = 0.7
+    p = 1 / (1 + math.exp(-a))
+    want = -(p * math.log(p) + (1 - p) * math.log(1 - p))
+    l = np.array([-np.inf, a, -np.inf, 0.0, -np.inf])
+    assert R.token_entropy(l) == pytest.approx(want, rel=1e-12)
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(400) * 2
+    m = x.copy()
+    m[::3] = -np.inf
+    assert R.token_entropy(m) == pytest.approx(R.token_entropy(x[np.isfinite(m)]), rel=1e-12)
+    # masked tokens are never sampled
+    assert all(np.isfinite(m[R.sample_inverse_cdf(m, 1.0, u)]) for u in (0.0, 0.3, 0.999))
+
+
 @pytest.mark.parametrize("T,u,tok", [
     (1.0, 0.0, 0), (1.0, 0.05, 0), (1.0, 0.15, 1), (1.0, 0.35, 2), (1.0, 0.65, 3), (1.0, 0.999, 3),
     # T = 0.5 squares the probabilities: [1, 4, 9, 16] / 30 -> C = [1, 5, 14, 30] / 30
