@@ -748,7 +748,7 @@ def run_sampler(args, world, rank):
     return {
         "metric": SAMPLER_METRIC, "value": round(ms_mean * 1e3, 2), "unit": "us/step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_mean, 4), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (entropy and sample), fp64 (merge, state)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (entropy and sample), integer masses (top-p), fp64 (state sums)",
         "data": "synthetic (seeded N(0, sigma) logits per step, sigma in {1,3,8}; geometric step boundaries; "
                 "PCG64 uniforms)",
         "config": {"workload": sampler_workload(args),
@@ -756,13 +756,14 @@ def run_sampler(args, world, rank):
         "p50_us": round(float(np.percentile(ms, 50)) * 1e3, 2), "p99_us": round(float(np.percentile(ms, 99)) * 1e3, 2),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "traffic": None,
-                     "kernel": "reset_sample_kernel" + (" + 4 top-p launches" if args.top_p < 1.0 else "") +
-                               ": first-pass logits bytes (4 M V) / call time; latency-bound",
+                     "kernel": "reset_cluster_kernel (one thread-block cluster per row" +
+                               (", top-p inside" if args.top_p < 1.0 else "") +
+                               "): first-pass logits bytes (4 M V) / call time; latency-bound",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(ms_mean * 1e3, 2), "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0, "note": "device-resident logits, as the lm_head leaves them"},
         "clocks": clk.summary(),
-        "gpu_launches": args.steps * (5 if args.top_p < 1.0 else 1),
+        "gpu_launches": args.steps,                 # one cluster launch per call (V <= 262144)
     }
 
 

@@ -410,17 +410,21 @@ nvfp4_status reset_sample(const float* logits, int M, int V, const uint8_t* step
  * pool and only hands out fixed input/output buffers, or a latency-critical
  * decode loop that must not call cudaMalloc because it synchronizes the device.
  *
- * The scratch (per-row counters, per-chunk partial sums, the top-p records
- * and histograms) lives in a 1,217,280-byte array that the library reserves
- * statically on every GPU that loads it, until the process exits.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library routine.
- *   Limit: M * ceil(V / 2048) <= 4096 (M = 8 allows V up to 1,048,576);
- *          larger calls return NVFP4_ERR_SHAPE without launching anything.
+ * Rows of up to 262,144 logits (one thread-block cluster a row, with or
+ * without top-p) need no scratch.  Longer rows take a multi-launch path whose
+ * scratch (per-row counters, per-chunk partial sums, the top-p records and
+ * histograms) lives in a 1,217,280-byte array that the library reserves
+ * statically on every GPU that loads it, until the process exits.  Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library routine.
+ *   Limit (V > 262,144 only): M * ceil(V / 2048) <= 4096 (M = 8 allows V up
+ *          to 1,048,576); larger calls return NVFP4_ERR_SHAPE without
+ *          launching anything.
  *   The first call on a device looks up that device's copy of the array
  *   (cudaGetSymbolAddress); make it before any stream capture on that device.
- *   Every call on a device uses the same array and clears its counters (a
- *   256-byte memset on `stream`); calls that overlap on the GPU (for example
- *   on two unordered streams) race and give wrong results -- order them.
+ *   Every call with V > 262,144 uses the same array and clears its counters
+ *   (a 256-byte memset on `stream`); such calls that overlap on the GPU (for
+ *   example on two unordered streams) race and give wrong results -- order
+ *   them.
  */
 nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, const uint8_t* step_start,
                                   const float* u, void* state, const reset_params* p, int32_t* token,

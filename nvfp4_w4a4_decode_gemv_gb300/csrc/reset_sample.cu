@@ -2010,15 +2010,22 @@ extern "C" nvfp4_status reset_sample_noalloc(const float* logits, int M, int V, 
       !nvfp4_internal_aligned(token, 4))
     return NVFP4_ERR_ALIGN;
   const int NC = (V + kChunk - 1) / kChunk;
-  if (NC > 1024 || (long long)M * NC > kNoAllocMaxChunks) return NVFP4_ERR_SHAPE;   // beyond the static scratch
-  if (sample_layout(M, NC).total > kNoAllocScratchBytes) return NVFP4_ERR_SHAPE;
+  // Rows of up to 8 x 1024 x 32 logits take one cluster a row and use no
+  // scratch; longer rows take the multi-launch path and its static array.
+  const bool one_cluster = V <= kMaxClusterCtas * kCThreads * 32;
+  if (!one_cluster) {
+    if (NC > 1024 || (long long)M * NC > kNoAllocMaxChunks) return NVFP4_ERR_SHAPE;   // beyond the static scratch
+    if (sample_layout(M, NC).total > kNoAllocScratchBytes) return NVFP4_ERR_SHAPE;
+  }
   nvfp4_status ds = nvfp4_internal_check_device();
   if (ds != NVFP4_OK) return ds;
   uint8_t* scratch = nullptr;
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
-  // The array keeps the previous call's contents: clear the row counters.
-  e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
-  if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
+  if (!one_cluster) {
+    // The array keeps the previous call's contents: clear the row counters.
+    e = cudaMemsetAsync(scratch, 0, kCounterBytes, stream);
+    if (e != cudaSuccess) return nvfp4_internal_cuda_status(e);
+  }
   return launch_sample(logits, M, V, NC, step_start, u, state, p, token, H_out, T_out, scratch, stream);
 }

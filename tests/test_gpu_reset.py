@@ -173,6 +173,15 @@ def test_top_p_full_size_prefix():
          synth.reset_uniforms(steps, M, seed=3), top_p=0.95)
 
 
+@pytest.mark.parametrize("top_p", [1.0, 0.95])
+def test_rows_longer_than_one_cluster(top_p):
+    """V = 300001 > 8 x 1024 x 32: the multi-launch path (chunk partials, a
+    last-CTA merge and, with top-p, the four nucleus launches)."""
+    M, V, steps = 2, 300001, 4
+    _run(M, V, steps, synth.reset_sigmas(steps, seed=15), synth.reset_boundaries(steps, M, p=0.3, seed=15),
+         synth.reset_uniforms(steps, M, seed=15), top_p=top_p)
+
+
 @pytest.mark.parametrize("top_p,threshold", [(0.5, "reset"), (0.9, "window"), (0.05, "fixed")])
 @pytest.mark.parametrize("V", [1, 3, 2047, 2049, 6001])
 def test_top_p_ragged_vocab(V, top_p, threshold):

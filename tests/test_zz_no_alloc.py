@@ -84,7 +84,8 @@ def test_noalloc_across_shapes_and_top_p():
     w = 8
     _status(L)
     seq = [(8, synth.LM_HEAD_VOCAB, 1.0), (3, 2049, 0.9), (64, 4096, 0.95), (1, 1, 1.0),
-           (8, synth.LM_HEAD_VOCAB, 0.95), (5, 70001, 1.0), (3, 2049, 0.9)]
+           (8, synth.LM_HEAD_VOCAB, 0.95), (5, 70001, 1.0), (2, 300001, 0.95), (3, 2049, 0.9),
+           (2, 300001, 1.0), (64, synth.LM_HEAD_VOCAB, 0.95)]
     for i, (M, V, top_p) in enumerate(seq):
         params = ResetParams(0.6, 0.3, 1.0, w, 0, top_p)
         st_ref, st_new = _state(L, M, w), _state(L, M, w)
