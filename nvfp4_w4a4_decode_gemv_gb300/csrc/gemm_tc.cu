@@ -25,6 +25,7 @@
 // it 16 token columns at a time.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -64,6 +65,8 @@ struct GemmArgs {
   unsigned int* records;         // [G][M][128] words: a CTA's partial sums of its first tile; zero between calls
   int M, N, K, C;
   long long U;
+  int tiles;                     // 128-row tiles: ceil(N / 128)
+  int whole_tiles;               // non-zero: CTA q takes tiles [q tiles / G, (q + 1) tiles / G) whole, no split
   uint32_t flag_spins;
   int drop_records;              // test hook (nvfp4_test_gemv_fault)
 };
@@ -96,29 +99,32 @@ constexpr int kBatch = 4;
 
 NVFP4_DEVINL void take_batch(const GemmArgs& a, long long q0, long long q1, int m0, int row, float (&v)[16]) {
   unsigned int w[kBatch][16];
+  // Every live word's load is issued before any is looked at (the loads are
+  // ordered asm statements: a check between them would wait out each one's
+  // L2 round trip in turn); only the words still zero are polled again.
 #pragma unroll
   for (int j = 0; j < kBatch; ++j)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[j][i] = 0u;
+    for (int i = 0; i < 16; ++i)
+      w[j][i] = (q0 + j <= q1 && m0 + i < a.M) ? ld_relaxed_gpu(record(a, q0 + j, m0 + i, row)) : ~0u;
   uint32_t spins = 0;
   for (;;) {
     bool ready = true;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const bool liveq = q0 + j <= q1;
+    for (int j = 0; j < kBatch; ++j)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool live = liveq && m0 + i < a.M;
-        if (w[j][i] == 0u) w[j][i] = live ? ld_relaxed_gpu(record(a, q0 + j, m0 + i, row)) : ~0u;
-        ready = ready && w[j][i] != 0u;
-      }
-    }
+      for (int i = 0; i < 16; ++i) ready = ready && w[j][i] != 0u;
     if (ready) break;
     if (++spins >= a.flag_spins) {
       atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
       break;
     }
     __nanosleep(32);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (w[j][i] == 0u) w[j][i] = ld_relaxed_gpu(record(a, q0 + j, m0 + i, row));
   }
 #pragma unroll
   for (int j = 0; j < kBatch; ++j) {
@@ -146,8 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
-  const long long u0 = unit_start(blockIdx.x, a.U, G);
-  const long long u1 = unit_start(blockIdx.x + 1, a.U, G);
+  const long long u0 = a.whole_tiles ? ((long long)blockIdx.x * a.tiles / G) * a.C : unit_start(blockIdx.x, a.U, G);
+  const long long u1 =
+      a.whole_tiles ? ((long long)(blockIdx.x + 1) * a.tiles / G) * a.C : unit_start(blockIdx.x + 1, a.U, G);
   const int nunits = (int)(u1 - u0);
   const int C = a.C;
   const int tile0 = (int)(u0 / C), chunk0 = (int)(u0 % C);
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       tc_fence_after();
       const long long t0 = (long long)tile * C;
       const long long first = cta_of_unit(t0, a.U, G), last = cta_of_unit(t0 + C - 1, a.U, G);
-      const bool whole = first == last;
+      const bool whole = a.whole_tiles || first == last;
       const bool fin = !whole && first == (long long)blockIdx.x;   // this CTA finishes the split tile
       const int n = tile * kTR + row;
       const uint32_t dcol = tmem + ((uint32_t)(p * 32) << 16) + (uint32_t)(d * kNT);
@@ -379,13 +386,33 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   const uint32_t spins = nvfp4_internal_test_flag_spins();
   a.flag_spins = spins ? spins : kFlagSpinLimit;
   a.drop_records = nvfp4_internal_test_drop_records();
-  // One CTA per SM.  With fewer 128-row tiles than SMs, every tile gets the
-  // same whole number of CTAs (tiles x floor(SMs / tiles)): a split tile's
-  // partial sums are 64 KB per contributor at M = 128, so the fewer and more
-  // even the splits, the shorter the fix-up.
+  // One CTA per SM, in one of two plans, whichever leaves the busiest CTA the
+  // less work in units of one [128-row x 256-K] MMA step:
+  //  - whole tiles: CTA q takes tiles [q T / G, (q + 1) T / G), at most
+  //    ceil(T / SMs) of them; nothing to merge;
+  //  - split tiles: with fewer tiles than SMs every tile gets the same whole
+  //    number of CTAs (T x floor(SMs / T)), else Stream-K over all SMs; a split
+  //    tile's finishing CTA then merges 64 KB of partial sums per contributor
+  //    at M = 128, which measured as long as about 4.5 MMA steps per 16 tokens.
+  // (Qwen3-32B at M = 128: whole tiles for qkv, o and gate_up, split tiles for
+  // down, whose 40 tiles of 100 steps would leave 112 SMs idle.)
   const long long sms = nvfp4_internal_device_sms();
   const long long tiles = (N + kTR - 1) / kTR;
-  long long G = tiles < sms ? tiles * (sms / tiles) : sms;
+  a.tiles = (int)tiles;
+  const long long per = (tiles + sms - 1) / sms;
+  const long long g_whole = (tiles + per - 1) / per;
+  long long g_split = tiles < sms ? tiles * (sms / tiles) : sms;
+  if (g_split > a.U) g_split = a.U;
+  const bool splits = !(g_split <= tiles && tiles % g_split == 0);
+  const long long cost_whole = per * a.C;
+  const long long cost_split = (a.U + g_split - 1) / g_split + (splits ? (9 * ((M + 15) / 16) + 1) / 2 : 0);
+  static const int mode = [] {            // tuning knob NVFP4_GEMM_MODE: "tiles" or "split" forces a plan
+    const char* v = getenv("NVFP4_GEMM_MODE");
+    return (v && v[0] == 't') ? 1 : (v && v[0] == 's') ? 2 : 0;
+  }();
+  const bool whole = mode == 1 || (mode == 0 && cost_whole <= cost_split);
+  long long G = whole ? g_whole : g_split;
+  a.whole_tiles = whole ? 1 : 0;
   if (G > a.U) G = a.U;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);

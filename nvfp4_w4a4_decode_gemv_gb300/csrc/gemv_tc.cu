@@ -166,29 +166,36 @@ NVFP4_DEVINL void publish_record(const TcArgs& a, int row, const float (&acc)[kN
 template <int M>
 NVFP4_DEVINL void take_records(const TcArgs& a, long long q0, long long last, int row, float (&v)[4][M]) {
   unsigned int w[4][M];
+  // Every live word's load is issued before any is looked at (the loads are
+  // ordered asm statements: a check between them would wait out each one's
+  // L2 round trip in turn); only the words still zero are polled again.
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 4; ++i) {
+    const bool live = q0 + i <= last;
+    const unsigned int* rec = record<M>(a, live ? q0 + i : q0, row);
 #pragma unroll
-    for (int m = 0; m < M; ++m) w[i][m] = 0u;
+    for (int m = 0; m < M; ++m) w[i][m] = live ? ld_relaxed_gpu(rec + m * kTR) : ~0u;
+  }
   uint32_t spins = 0;
-  for (;;) {                    // load the words not seen yet (all of them the first time)
+  for (;;) {
     bool ready = true;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool live = q0 + i <= last;
-      const unsigned int* rec = record<M>(a, live ? q0 + i : q0, row);
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        if (w[i][m] == 0u) w[i][m] = live ? ld_relaxed_gpu(rec + m * kTR) : ~0u;
-        ready = ready && w[i][m] != 0u;
-      }
-    }
+      for (int m = 0; m < M; ++m) ready = ready && w[i][m] != 0u;
     if (ready) break;
     if (++spins >= a.flag_spins) {
       atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_FLAG_TIMEOUT);
       break;
     }
     __nanosleep(32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const unsigned int* rec = record<M>(a, q0 + i <= last ? q0 + i : q0, row);
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+        if (w[i][m] == 0u) w[i][m] = ld_relaxed_gpu(rec + m * kTR);
+    }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

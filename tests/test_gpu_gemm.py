@@ -42,6 +42,17 @@ def test_gemm_every_m_class_ragged(M):
     assert api.device_status() == 0
 
 
+@pytest.mark.parametrize("M", [1, 17, 100, 128])
+def test_gemm_split_tiles_ragged_m(M):
+    """N = 300 (3 tiles), K = 25600: every tile split across 50 CTAs, their
+    partial sums merged by the tile's first CTA, for ragged token counts."""
+    x, w, X, P = _operands(M, 300, 25600, seed=60 + M)
+    y = to_np(api.nvfp4_gemm_packed(X, P))
+    y_ref, bound = _oracle(x, w)
+    assert_within(y, y_ref, bound)
+    assert api.device_status() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 1, 256), (128, 129, 256), (96, 3000, 2816), (128, 384, 25600),
                                    (40, 64, 8192), (128, 4096, 4096)])
 def test_gemm_shapes(M, N, K):
@@ -111,7 +122,7 @@ def test_gemm_canaries(M, N, K):
 
 
 def test_gemm_fixup_wait_runs_out_and_is_reported():
-    M, N, K = 128, 1000, 768         # 24 units: one per CTA, every tile split three ways
+    M, N, K = 16, 1000, 2560         # 80 units: one per CTA, every tile split ten ways
     x, w, X, P = _operands(M, N, K, seed=400)
     ws = torch.zeros(api.nvfp4_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
