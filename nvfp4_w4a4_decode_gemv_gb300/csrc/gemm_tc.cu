@@ -66,6 +66,7 @@ struct GemmArgs {
   int M, N, K, C;
   long long U;
   int tiles;                     // 128-row tiles: ceil(N / 128)
+  int y_tma;                     // non-zero: a CTA's last tile goes out through shared memory and tm_y
   int whole_tiles;               // non-zero: CTA q takes tiles [q tiles / G, (q + 1) tiles / G) whole, no split
   uint32_t flag_spins;
   int drop_records;              // test hook (nvfp4_test_gemv_fault)
@@ -137,8 +138,21 @@ NVFP4_DEVINL void take_batch(const GemmArgs& a, long long q0, long long q1, int 
   }
 }
 
+// A CTA's last tile of y: the 128 x 128 FP32 block goes through the ring's
+// shared memory (free by then: every unit's MMAs have completed) as two
+// [128 tokens x 64 rows] boxes, written by two bulk tensor stores -- the tile's
+// 64 KB in two copies instead of 128 scalar stores a thread.  Rows >= N and
+// tokens >= M fall outside tm_y and are not written.
+constexpr int kYBox = 64;                   // weight rows (FP32 columns of y) per store box: 256 bytes
+NVFP4_DEVINL void tma_store_2d(const void* tmap, int32_t x, int32_t y, const void* smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_xcodes,
                                                               const __grid_constant__ CUtensorMap tm_xscales,
+                                                              const __grid_constant__ CUtensorMap tm_y,
                                                               const GemmArgs a) {
   constexpr int S = kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -148,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint64_t* empty = sf_ready + S;
   uint64_t* acc_full = empty + S;           // [0], [1]: alternating tiles
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* y_staged = acc_empty + 2;       // the 4 epilogue warps have staged the last tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_staged + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
@@ -169,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mbar_init(&acc_full[d], 1);
       mbar_init(&acc_empty[d], 4);
     }
+    mbar_init(y_staged, 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -300,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const bool fin = !whole && first == (long long)blockIdx.x;   // this CTA finishes the split tile
       const int n = tile * kTR + row;
       const uint32_t dcol = tmem + ((uint32_t)(p * 32) << 16) + (uint32_t)(d * kNT);
+      const bool staged = a.y_tma && tile == tile_last && (whole || fin);
+      // box (row / 64): [token m][row % 64] floats, 256 bytes a token
+      float* stage = reinterpret_cast<float*>(smem + (row / kYBox) * (kNT * kYBox * 4)) + (row % kYBox);
       for (int m0 = 0; m0 < a.M; m0 += 16) {
         float v[16];
         read16(dcol + (uint32_t)m0, v);
@@ -308,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (long long q = first + 1; q <= last; q += kBatch)
               take_batch(a, q, q + kBatch - 1 < last ? q + kBatch - 1 : last, m0, row, v);
           }
-          if (n < a.N) {
+          if (staged) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stage[(m0 + i) * kYBox] = v[i] * yscale;
+          } else if (n < a.N) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               if (m0 + i < a.M) a.y[(size_t)(m0 + i) * a.N + n] = v[i] * yscale;
@@ -322,6 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[d]);
+      if (staged) {
+        // Each warp makes its writes visible to the copy engine and arrives; one
+        // thread waits (bounded) for the four, then issues the copies and waits
+        // for them.  The other threads do not wait.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(y_staged);
+        if (p == 2 && lane == 0 && mbar_wait(y_staged, 0)) {
+          for (int b = 0; b < kTR / kYBox; ++b)
+            tma_store_2d(&tm_y, (tile * kTR + b * kYBox) * 4, 0, smem + b * (kNT * kYBox * 4));
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        }
+      }
     }
   }
   tc_fence_before();
@@ -332,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   }
 }
 
-constexpr size_t gemm_smem_bytes() { return (size_t)kStages * kSlot + 1024 + (3 * kStages + 4) * sizeof(uint64_t) + 16; }
+constexpr size_t gemm_smem_bytes() { return (size_t)kStages * kSlot + 1024 + (3 * kStages + 5) * sizeof(uint64_t) + 16; }
 
 }  // namespace
 
@@ -424,7 +460,12 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mx, ms, a);
+  // y through bulk tensor stores when its rows are 16-byte multiples (N % 4 == 0)
+  // on a 16-byte aligned base; else plain stores (tm_y unused).
+  CUtensorMap my;
+  memset(&my, 0, sizeof(my));
+  a.y_tma = (N % 4 == 0) && nvfp4_internal_encode_2d(&my, y, (uint64_t)N * 4, (uint64_t)M, kYBox * 4, kNT, false);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mx, ms, my, a);
 }
 
 nvfp4_status nvfp4_internal_cuda_status(cudaError_t e);
