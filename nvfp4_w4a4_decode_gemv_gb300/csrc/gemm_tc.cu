@@ -235,36 +235,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (one thread) ----------------
+    // The loop is unrolled by ring stage, so each unit's descriptors and scale
+    // columns are compile-time offsets from the stage-0 values: this thread
+    // is the unit loop's limit (an MMA issue holds it, and every instruction
+    // between the MMAs adds to the unit), so it does as little as it can.
     if (lane == 0 && nunits > 0) {
       const uint64_t da0 = smem_desc_sw128(smem_u32(smem));
       const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB));
-      int tile_idx = -1;
-      int c = chunk0;
-      int s = 0;
+      const uint32_t sf0 = tmem + kColSF;
+      int tile_idx = 0;
+      int left = C - chunk0;                // units left in the current tile
+      bool first = true;                    // the next unit starts a tile
       uint32_t phase = 0;
       int issued = 0;
       uint32_t d_tmem = tmem;
-      for (int k = 0; k < nunits; ++k) {
-        const bool first_of_tile = (k == 0) || (c == 0);
-        if (first_of_tile) {
-          ++tile_idx;
-          if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) break;
-          d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
-        }
-        if (!mbar_wait(&sf_ready[s], phase)) break;
-        tc_fence_after();
-        const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
-        const uint32_t sfa = tmem + kColSF + 32u * s;
-        const uint32_t sfb = sfa + 16u;
+      bool ok = true;
+      while (ok && issued < nunits) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sfa + 4u * q, sfb + 4u * q,
-                       (first_of_tile && q == 0) ? 0u : 1u);
-        mma_commit(&empty[s]);
-        issued = k + 1;
-        if (++c == C) c = 0;
-        if (k + 1 == nunits || c == 0) mma_commit(&acc_full[tile_idx & 1]);   // last unit of this tile
-        if (++s == S) { s = 0; phase ^= 1u; }
+        for (int st = 0; st < S; ++st) {
+          if (issued == nunits) break;
+          if (first) {
+            if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
+          }
+          if (!mbar_wait(&sf_ready[st], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t doff = (uint64_t)((st * kSlot) >> 4);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sf0 + 32u * st + 4u * q,
+                         sf0 + 32u * st + 16u + 4u * q, (first && q == 0) ? 0u : 1u);
+          mma_commit(&empty[st]);
+          ++issued;
+          first = false;
+          if (--left == 0 || issued == nunits) {        // last unit of this tile
+            mma_commit(&acc_full[tile_idx & 1]);
+            ++tile_idx;
+            left = C;
+            first = true;
+          }
+        }
+        phase ^= 1u;
       }
       if (issued > 0) mbar_wait(&empty[(issued - 1) % S], ((issued - 1) / S) & 1);
     }
