@@ -67,6 +67,7 @@ struct GemmArgs {
   long long U;
   int tiles;                     // 128-row tiles: ceil(N / 128)
   int y_tma;                     // non-zero: a CTA's last tile goes out through shared memory and tm_y
+  int cluster_k;                 // > 1: tile q / k of one CTA cluster of k, merged over distributed shared memory
   int whole_tiles;               // non-zero: CTA q takes tiles [q tiles / G, (q + 1) tiles / G) whole, no split
   uint32_t flag_spins;
   int drop_records;              // test hook (nvfp4_test_gemv_fault)
@@ -144,10 +145,38 @@ NVFP4_DEVINL void take_batch(const GemmArgs& a, long long q0, long long q1, int 
 // 64 KB in two copies instead of 128 scalar stores a thread.  Rows >= N and
 // tokens >= M fall outside tm_y and are not written.
 constexpr int kYBox = 64;                   // weight rows (FP32 columns of y) per store box: 256 bytes
+constexpr int kMaxClusterK = 3;             // CTAs a tile in the cluster plan
 NVFP4_DEVINL void tma_store_2d(const void* tmap, int32_t x, int32_t y, const void* smem_src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
                "r"(y), "r"(smem_u32(smem_src))
                : "memory");
+}
+
+// Cluster-scope mbarrier operations and a distributed-shared-memory load, for
+// the merge of a tile split across the CTAs of one cluster.
+NVFP4_DEVINL void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(dsmem_addr(local_bar, rank))
+               : "memory");
+}
+NVFP4_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kMbarSpinLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  atomicOr(&g_nvfp4_device_error, NVFP4_DEVERR_MBAR_TIMEOUT);
+  return false;
+}
+NVFP4_DEVINL float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_xcodes,
@@ -163,13 +192,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   uint64_t* acc_full = empty + S;           // [0], [1]: alternating tiles
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* y_staged = acc_empty + 2;       // the 4 epilogue warps have staged the last tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_staged + 1);
+  uint64_t* part_ready = y_staged + 1;      // cluster rank 0: the other ranks' partial sums are staged
+  uint64_t* consumed = part_ready + 1;      // other ranks: rank 0 has read this CTA's partial sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(consumed + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
-  const long long u0 = a.whole_tiles ? ((long long)blockIdx.x * a.tiles / G) * a.C : unit_start(blockIdx.x, a.U, G);
-  const long long u1 =
-      a.whole_tiles ? ((long long)(blockIdx.x + 1) * a.tiles / G) * a.C : unit_start(blockIdx.x + 1, a.U, G);
+  const int ck = a.cluster_k > 1 ? a.cluster_k : 1;
+  const uint32_t crank = ck > 1 ? cluster_ctarank() : 0u;   // = blockIdx.x % ck: clusters are consecutive CTAs
+  long long u0, u1;
+  if (ck > 1) {                                  // one tile, its ck consecutive K ranges on the cluster's CTAs
+    const long long t = blockIdx.x / ck;
+    u0 = t * a.C + ((long long)crank * a.C) / ck;
+    u1 = t * a.C + ((long long)(crank + 1) * a.C) / ck;
+  } else if (a.whole_tiles) {
+    u0 = ((long long)blockIdx.x * a.tiles / G) * a.C;
+    u1 = ((long long)(blockIdx.x + 1) * a.tiles / G) * a.C;
+  } else {
+    u0 = unit_start(blockIdx.x, a.U, G);
+    u1 = unit_start(blockIdx.x + 1, a.U, G);
+  }
   const int nunits = (int)(u1 - u0);
   const int C = a.C;
   const int tile0 = (int)(u0 / C), chunk0 = (int)(u0 % C);
@@ -185,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mbar_init(&acc_empty[d], 4);
     }
     mbar_init(y_staged, 4);
+    mbar_init(part_ready, 128 * (ck > 1 ? ck - 1 : 1));   // every epilogue thread of every other rank
+    mbar_init(consumed, 128);                              // every epilogue thread of rank 0
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -195,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // A cluster's CTAs arrive once their barriers are initialised; a thread waits
+  // before its first remote operation (the epilogue warps) or at the end.
+  if (ck > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch_dependents();
 
@@ -321,25 +368,84 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int p = warp & 3;
     const int row = p * 32 + lane;
     griddep_wait();            // y and the records belong to the preceding kernel's era
+    if (ck > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     const float yscale = __fmul_rn(__ldcg(a.xg), __ldcg(a.wg));
     const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
     for (int tile = tile0, tile_idx = 0; tile <= tile_last; ++tile, ++tile_idx) {
       const int d = tile_idx & 1;
       if (!mbar_wait_warp(&acc_full[d], (tile_idx >> 1) & 1)) break;
       tc_fence_after();
-      const long long t0 = (long long)tile * C;
-      const long long first = cta_of_unit(t0, a.U, G), last = cta_of_unit(t0 + C - 1, a.U, G);
-      const bool whole = a.whole_tiles || first == last;
-      const bool fin = !whole && first == (long long)blockIdx.x;   // this CTA finishes the split tile
+      // Split tiles: a cluster's ranks 1..k-1 stage their partial sums in their
+      // own shared memory and rank 0 adds them; otherwise the tile's first CTA
+      // adds the others' records (Stream-K).
+      const bool cl = ck > 1;
+      const bool partner = cl && crank != 0;
+      bool whole, fin;
+      long long first = 0, last = 0;
+      if (cl) {
+        whole = false;
+        fin = crank == 0;
+      } else {
+        const long long t0 = (long long)tile * C;
+        first = cta_of_unit(t0, a.U, G);
+        last = cta_of_unit(t0 + C - 1, a.U, G);
+        whole = a.whole_tiles || first == last;
+        fin = !whole && first == (long long)blockIdx.x;   // this CTA finishes the split tile
+      }
       const int n = tile * kTR + row;
       const uint32_t dcol = tmem + ((uint32_t)(p * 32) << 16) + (uint32_t)(d * kNT);
       const bool staged = a.y_tma && tile == tile_last && (whole || fin);
-      // box (row / 64): [token m][row % 64] floats, 256 bytes a token
+      // box (row / 64): [token m][row % 64] floats, 256 bytes a token -- the
+      // staging of y, and of a cluster rank's partial sums
       float* stage = reinterpret_cast<float*>(smem + (row / kYBox) * (kNT * kYBox * 4)) + (row % kYBox);
+      if (fin && cl) {
+        // Rank 0: every thread acquires the partials, then adds the other ranks'
+        // values of its row in rank order, the next 16 tokens' loads issued
+        // before the current ones are added (a load's round trip is long).
+        if (!mbar_wait_cluster(part_ready, 0)) break;
+        float wq[kMaxClusterK - 1][16];
+#pragma unroll
+        for (int r = 1; r < kMaxClusterK; ++r)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            wq[r - 1][i] = r < ck ? ld_dsmem_f32(dsmem_addr(&stage[i * kYBox], (uint32_t)r)) : 0.0f;
+        for (int m0 = 0; m0 < a.M; m0 += 16) {
+          float v[16];
+          read16(dcol + (uint32_t)m0, v);
+          float wn[kMaxClusterK - 1][16];
+          const bool more = m0 + 16 < a.M;
+#pragma unroll
+          for (int r = 1; r < kMaxClusterK; ++r)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              wn[r - 1][i] = (more && r < ck) ? ld_dsmem_f32(dsmem_addr(&stage[(m0 + 16 + i) * kYBox], (uint32_t)r)) : 0.0f;
+#pragma unroll
+          for (int r = 1; r < kMaxClusterK; ++r)
+            if (r < ck) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += wq[r - 1][i];
+            }
+          if (staged) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stage[(m0 + i) * kYBox] = v[i] * yscale;
+          } else if (n < a.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (m0 + i < a.M) a.y[(size_t)(m0 + i) * a.N + n] = v[i] * yscale;
+          }
+#pragma unroll
+          for (int r = 0; r < kMaxClusterK - 1; ++r)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) wq[r][i] = wn[r][i];
+        }
+      } else
       for (int m0 = 0; m0 < a.M; m0 += 16) {
         float v[16];
         read16(dcol + (uint32_t)m0, v);
-        if (whole || fin) {
+        if (partner) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stage[(m0 + i) * kYBox] = v[i];
+        } else if (whole || fin) {
           if (fin) {                  // in CTA order: a fixed order of additions
             for (long long q = first + 1; q <= last; q += kBatch)
               take_batch(a, q, q + kBatch - 1 < last ? q + kBatch - 1 : last, m0, row, v);
@@ -361,6 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[d]);
+      if (partner) {
+        // This thread's partial sums are staged: tell rank 0, then keep the
+        // shared memory until rank 0 has read it (bounded wait).
+        mbar_arrive_remote(part_ready, 0u);
+        if (p == 2 && lane == 0) mbar_wait_cluster(consumed, 0);
+      } else if (fin && cl) {
+        // this thread has read its rows of every other rank's partial sums
+        for (int r = 1; r < ck; ++r) mbar_arrive_remote(consumed, (uint32_t)r);
+      }
       if (staged) {
         // Each warp makes its writes visible to the copy engine and arrives; one
         // thread waits (bounded) for the four, then issues the copies and waits
@@ -378,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   }
   tc_fence_before();
+  if (ck > 1 && warp < 6) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // (epilogue warps: above)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -385,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   }
 }
 
-constexpr size_t gemm_smem_bytes() { return (size_t)kStages * kSlot + 1024 + (3 * kStages + 5) * sizeof(uint64_t) + 16; }
+constexpr size_t gemm_smem_bytes() { return (size_t)kStages * kSlot + 1024 + (3 * kStages + 7) * sizeof(uint64_t) + 16; }
 
 }  // namespace
 
@@ -459,24 +575,50 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   const bool splits = !(g_split <= tiles && tiles % g_split == 0);
   const long long cost_whole = per * a.C;
   const long long cost_split = (a.U + g_split - 1) / g_split + (splits ? (9 * ((M + 15) / 16) + 1) / 2 : 0);
-  static const int mode = [] {            // tuning knob NVFP4_GEMM_MODE: "tiles" or "split" forces a plan
+  // With fewer tiles than SMs, a tile can also go to a cluster of k <= 3 CTAs
+  // (k <= units a tile) whose partial sums meet in shared memory: each other
+  // rank stages 64 KB at M = 128, rank 0 reads it over distributed shared
+  // memory and adds it -- measured as long as about 2 MMA steps per 16 tokens
+  // per rank.  Ties go to the larger cluster.
+  long long best_k = 1, cost_cluster = -1;
+  for (long long k = 2; k <= kMaxClusterK && tiles * k <= sms && k <= a.C; ++k) {
+    const long long c = (a.C + k - 1) / k + (k - 1) * 2 * ((M + 15) / 16);
+    if (cost_cluster < 0 || c <= cost_cluster) {
+      cost_cluster = c;
+      best_k = k;
+    }
+  }
+  static const int mode = [] {            // tuning knob NVFP4_GEMM_MODE: "tiles", "split" or "cluster" forces a plan
     const char* v = getenv("NVFP4_GEMM_MODE");
-    return (v && v[0] == 't') ? 1 : (v && v[0] == 's') ? 2 : 0;
+    return (v && v[0] == 't') ? 1 : (v && v[0] == 's') ? 2 : (v && v[0] == 'c') ? 3 : 0;
   }();
-  const bool whole = mode == 1 || (mode == 0 && cost_whole <= cost_split);
-  long long G = whole ? g_whole : g_split;
-  a.whole_tiles = whole ? 1 : 0;
+  int plan;                               // 1 whole tiles, 2 split tiles, 3 cluster
+  if (mode == 1 || mode == 2) {
+    plan = mode;
+  } else if (mode == 3) {
+    plan = best_k > 1 ? 3 : 1;
+  } else {
+    plan = cost_whole <= cost_split ? 1 : 2;
+    if (best_k > 1 && cost_cluster < (plan == 1 ? cost_whole : cost_split)) plan = 3;
+  }
+  long long G = plan == 1 ? g_whole : plan == 2 ? g_split : tiles * best_k;
+  a.whole_tiles = plan == 1 ? 1 : 0;
+  a.cluster_k = plan == 3 ? (int)best_k : 1;
   if (G > a.U) G = a.U;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = gemm_smem_bytes();
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)a.cluster_k;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.cluster_k > 1 ? 2 : 1;
   // y through bulk tensor stores when its rows are 16-byte multiples (N % 4 == 0)
   // on a 16-byte aligned base; else plain stores (tm_y unused).
   CUtensorMap my;

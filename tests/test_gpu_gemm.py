@@ -121,8 +121,22 @@ def test_gemm_canaries(M, N, K):
     assert_within(to_np(y.t), y_ref, bound)
 
 
+@pytest.mark.parametrize("M,N,K", [(33, 4999, 25600), (16, 5120, 25600)])
+def test_gemm_cluster_plan_canaries(M, N, K):
+    """40 tiles of 100 steps: each tile on a cluster of three CTAs whose
+    partial sums rank 0 adds over distributed shared memory; y inside guard
+    bands (N = 4999: scalar stores; N = 5120: the staged bulk stores)."""
+    x, w, X, P = _operands(M, N, K, seed=500 + M)
+    y = Guarded((M, N), torch.float32)
+    api.nvfp4_gemm_packed(X, P, y=y.t)
+    y.check("y")
+    y_ref, bound = _oracle(x, w)
+    assert_within(to_np(y.t), y_ref, bound)
+    assert api.device_status() == 0
+
+
 def test_gemm_fixup_wait_runs_out_and_is_reported():
-    M, N, K = 16, 1000, 2560         # 80 units: one per CTA, every tile split ten ways
+    M, N, K = 16, 300, 25600         # 300 units, 150 CTAs of two: every tile split across 50 CTAs
     x, w, X, P = _operands(M, N, K, seed=400)
     ws = torch.zeros(api.nvfp4_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
