@@ -17,8 +17,9 @@ quantizer runs).  The roofline times the GEMV kernels alone: one graph of the
 same GEMV launches, replayed right after the timed steps; per-M graphs of the
 GEMVs give the per-M breakdown.  A cold-L2 breakdown per (projection, M)
 follows (512 MB flush before each call).  `e2e` repeats the step through the
-eager C-ABI calls with the activations copied from pinned host memory and the
-outputs copied back inside the timed region.
+public API with the activations copied from pinned host memory and the
+outputs copied back inside the timed region: the step's calls captured in a
+CUDA graph and replayed (`e2e.eager`: issued one by one from Python).
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (for N > 1 under torch.distributed.run: N independent replicas, weak scaling).
@@ -548,10 +549,14 @@ def cold_per_call(calls, weights, ws, R=200, trials=7):
 
 
 def run_e2e(args, calls, weights, ws):
-    """Same step through the eager API: the step's activations arrive in one
-    copy from pinned host memory, and its outputs go back in one copy.  (One
-    copy per M group on a second stream, overlapped with the other groups'
-    compute, measured slower: 1.21 against 0.74 ms per step.)"""
+    """The step end to end through the public API, with the step's activations
+    arriving in one copy from pinned host memory and its outputs leaving in one
+    copy to pinned host memory, both inside the timed region.  `value`: the
+    step's 64 API calls captured once in a CUDA graph (as a decode loop runs
+    them) and replayed between the two copies; `eager`: the same calls issued
+    one by one from Python each step.  (One copy per M group on a second
+    stream, overlapped with the other groups' compute, measured slower: 1.21
+    against 0.74 ms per step.)"""
     from nvfp4_w4a4_decode_gemv_gb300 import api
     dev = calls[0]["x"].device
     # one arena per direction; every piece is a multiple of 512 bytes, so each
@@ -565,33 +570,60 @@ def run_e2e(args, calls, weights, ws):
     dev_x = [v.view(c["x"].shape) for v, c in zip(torch.split(dev_xa, x_sizes), calls)]
     dev_y = [v.view(c["y"].shape) for v, c in zip(torch.split(dev_ya, y_sizes), calls)]
 
-    def step():
-        dev_xa.copy_(host_x, non_blocking=True)
+    def compute():
         for j, c in enumerate(calls):
             api.nvfp4_quantize_act(dev_x[j], out=c["xq"])
             gemv_call(api, c, weights[c["name"]], ws, y=dev_y[j])
-        host_y.copy_(dev_ya, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    for j, c in enumerate(calls):        # the arena path computes what the per-call buffers hold
-        if not torch.equal(dev_y[j], c["y"]):
-            raise RuntimeError("end-to-end step disagrees with the device-resident step")
-    if not torch.equal(host_y, dev_ya.cpu()):
-        raise RuntimeError("end-to-end outputs did not all reach the host")
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        step()
-    t1.record()
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
+    def check():
+        for j, c in enumerate(calls):        # the arena path computes what the per-call buffers hold
+            if not torch.equal(dev_y[j], c["y"]):
+                raise RuntimeError("end-to-end step disagrees with the device-resident step")
+        if not torch.equal(host_y, dev_ya.cpu()):
+            raise RuntimeError("end-to-end outputs did not all reach the host")
+
+    stream = torch.cuda.Stream()
     step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
-    return {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "ms_per_step": round(ms / args.steps, 4),
+    out = {}
+    with torch.cuda.stream(stream):
+        dev_xa.copy_(host_x, non_blocking=True)
+        for _ in range(3):
+            compute()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            compute()
+        for mode in ("eager", "graph"):
+            def step():
+                dev_xa.copy_(host_x, non_blocking=True)
+                if mode == "graph":
+                    g.replay()
+                else:
+                    compute()
+                host_y.copy_(dev_ya, non_blocking=True)
+
+            for _ in range(max(3, args.warmup)):
+                step()
+            stream.synchronize()
+            check()
+            host_y.zero_()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(args.steps):
+                step()
+            t1.record()
+            t1.synchronize()
+            check()
+            ms = t0.elapsed_time(t1)
+            out[mode] = {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                         "ms_per_step": round(ms / args.steps, 4)}
+    del g
+    torch.cuda.synchronize()
+    return {"value": out["graph"]["value"], "unit": "GB/s", "ms_per_step": out["graph"]["ms_per_step"],
             "h2d_bytes_per_step": int(host_x.numel() * host_x.element_size()),
-            "d2h_bytes_per_step": int(host_y.numel() * host_y.element_size())}
+            "d2h_bytes_per_step": int(host_y.numel() * host_y.element_size()),
+            "method": "per step: pinned host->device copy of the activations, the step's 64 API calls "
+                      "(captured once in a CUDA graph, replayed), device->host copy of all outputs",
+            "eager": out["eager"]}
 
 
 def decode_stage_times(st, stream, reps=20):
