@@ -334,69 +334,53 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (one thread) ----------------
-    // Unrolled by ring stage: each unit's descriptors and scale columns are
-    // compile-time offsets from the stage-0 values, so this thread -- which an
-    // MMA issue holds, and which every instruction between MMAs delays -- does
-    // as little as it can per unit.
     if (lane == 0 && nunits > 0) {
       // Descriptors of slot 0; the start-address field (bits 0-13, address / 16)
       // moves by (slot offset + 32 q) / 16 within the 14-bit field.
       const uint64_t da0 = smem_desc_sw128(smem_u32(smem));
       const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB));
-      const uint32_t sf0 = tmem + kColSF;
       // The CTA's last tile accumulates in its own buffer (D_last), flushed by
       // the scale writers; the others alternate between D0 and D1.
       const int last_idx = (int)((u1 - 1) / C) - tile0;
-      int tile_idx = 0;
-      int left = C - chunk0;                // units left in the current tile
-      bool first = true;                    // the next unit starts a tile
+      int tile_idx = -1;
+      int c = chunk0;
+      int s = 0;
       uint32_t phase = 0;
       int issued = 0;
       uint32_t d_tmem = tmem;
-      bool ok = true;
-      while (ok && issued < nunits) {
-#pragma unroll
-        for (int st = 0; st < S; ++st) {
-          if (issued == nunits) break;
-          if (first) {
-            if (tile_idx == last_idx) {
-              d_tmem = tmem + (uint32_t)(2 * kNT);
-            } else {
-              if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) {
-                ok = false;
-                break;
-              }
-              d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
-            }
-          }
-          // The scale writers arrive on sf_ready only after they have seen the
-          // slot full, so sf_ready also orders the slot's data before the MMAs.
-          // BF16 has no scales: the MMA waits for the slot itself.
-          if (!mbar_wait(BF ? &full[st] : &sf_ready[st], phase)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t doff = (uint64_t)((st * kSlot) >> 4);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (BF)
-              mma_f16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdescBF16, (first && q == 0) ? 0u : 1u);
-            else
-              mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sf0 + 32u * st + 4u * q,
-                           sf0 + 32u * st + 16u + 4u * q, (first && q == 0) ? 0u : 1u);
-          }
-          mma_commit(&empty[st]);
-          ++issued;
-          first = false;
-          if (--left == 0 || issued == nunits) {        // last unit of this tile
-            mma_commit(&acc_full[tile_idx == last_idx ? 2 : (tile_idx & 1)]);
-            ++tile_idx;
-            left = C;
-            first = true;
+      for (int k = 0; k < nunits; ++k) {
+        const bool first_of_tile = (k == 0) || (c == 0);
+        if (first_of_tile) {
+          ++tile_idx;
+          if (tile_idx == last_idx) {
+            d_tmem = tmem + (uint32_t)(2 * kNT);
+          } else {
+            if (tile_idx >= 2 && !mbar_wait(&acc_empty[tile_idx & 1], ((tile_idx >> 1) - 1) & 1)) break;
+            d_tmem = tmem + (uint32_t)((tile_idx & 1) * kNT);
           }
         }
-        phase ^= 1u;
+        // The scale writers arrive on sf_ready only after they have seen the
+        // slot full, so sf_ready also orders the slot's data before the MMAs.
+        // BF16 has no scales: the MMA waits for the slot itself.
+        if (!mbar_wait(BF ? &full[s] : &sf_ready[s], phase)) break;
+        tc_fence_after();
+        const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
+        const uint32_t sfa = tmem + kColSF + 32u * s;
+        const uint32_t sfb = sfa + 16u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (BF)
+            mma_f16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdescBF16, (first_of_tile && q == 0) ? 0u : 1u);
+          else
+            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sfa + 4u * q, sfb + 4u * q,
+                         (first_of_tile && q == 0) ? 0u : 1u);
+        }
+        mma_commit(&empty[s]);
+        issued = k + 1;
+        if (++c == C) c = 0;
+        if (k + 1 == nunits || c == 0)                                          // last unit of this tile
+          mma_commit(&acc_full[tile_idx == last_idx ? 2 : (tile_idx & 1)]);
+        if (++s == S) { s = 0; phase ^= 1u; }
       }
       // Do not leave with MMAs in flight: wait (bounded) for the last commit.
       if (issued > 0) mbar_wait(&empty[(issued - 1) % S], ((issued - 1) / S) & 1);
