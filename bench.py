@@ -83,6 +83,9 @@ def parse():
                     help="headline line only: skip per_proj, the cold per-call table, sampler and decode_step")
     ap.add_argument("--decode-steps", type=int, default=1500, help="decode_step key: graph replays per M")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route", default="one-call", choices=["one-call", "two-call"],
+                    help="sweep: nvfp4_quantize_gemv_packed per projection (one launch where it pays), or "
+                         "nvfp4_quantize_act + nvfp4_gemv_smallm_packed")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--only", default=None, help="time a single call, e.g. gate_up:8 (for profiling)")
     ap.add_argument("--m", type=int, default=None, help="decode workload: the number of tokens M (1, 4 or 8)")
@@ -211,6 +214,25 @@ def gemv_call(api, c, w, ws, y=None):
     return api.nvfp4_gemv_smallm(c["xq"], w, y=y, workspace=ws)
 
 
+def project(api, c, w, ws, route, x=None, y=None):
+    """One projection of the sweep from its BF16 activation: the one-call route
+    (nvfp4_quantize_gemv_packed) or the quantizer followed by the GEMV."""
+    x = c["x"] if x is None else x
+    if route == "one-call":
+        return api.nvfp4_quantize_gemv_packed(x, w, y=c["y"] if y is None else y, workspace=ws)
+    api.nvfp4_quantize_act(x, out=c["xq"])
+    return gemv_call(api, c, w, ws, y=y)
+
+
+def one_launch(M, N, K, sms=152):
+    """Whether nvfp4_quantize_gemv_packed runs as one launch for this shape, by
+    the library's default rule (M <= 3, M * K <= 65536, a CTA's chunks <= 24
+    and its blocks <= 1024); used only to count launches."""
+    C, U = K // 256, -(-N // 128) * (K // 256)
+    G = min(2 * sms, U)
+    res = min(-(-U // G), C)
+    return M <= 3 and M * K <= 65536 and res <= 24 and res * M * 16 <= 1024
+
 def build_problem(shapes, Ms, rank, only=None, packed=True):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     dev = torch.device("cuda")
@@ -232,8 +254,9 @@ def build_problem(shapes, Ms, rank, only=None, packed=True):
             x = synth.activations(M, K, seed=100 * M + i).to(dev)
             calls.append(dict(M=M, name=name, K=K, N=N, x=x, xq=api.NVFP4Tensor.empty(M, K, dev),
                               y=torch.empty((M, N), dtype=torch.float32, device=dev),
-                              gemv_bytes=synth.gemv_bytes(M, N, K), q_bytes=synth.quantize_bytes(M, K)))
-    ws_bytes = max(api.nvfp4_gemv_workspace_bytes(c["M"], c["N"], c["K"]) for c in calls)
+                              gemv_bytes=synth.gemv_bytes(M, N, K), q_bytes=synth.quantize_bytes(M, K),
+                              qg_bytes=synth.quantize_gemv_bytes(M, N, K)))
+    ws_bytes = max(api.nvfp4_quantize_gemv_workspace_bytes(c["M"], c["N"], c["K"]) for c in calls)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
     return weights, calls, ws
@@ -243,6 +266,8 @@ def run_ours(args, world, rank):
     from nvfp4_w4a4_decode_gemv_gb300 import api
     shapes, Ms = WORKLOADS[args.workload]
     weights, calls, ws = build_problem(shapes, Ms, rank, args.only, packed=args.weights == "packed")
+    route = args.route if args.weights == "packed" else "two-call"
+    other = "two-call" if route == "one-call" else "one-call"
     groups = {}
     for c in calls:
         groups.setdefault(c["M"], []).append(c)
@@ -252,24 +277,31 @@ def run_ours(args, world, rank):
         for c in cs:
             gemv_call(api, c, weights[c["name"]], ws)
 
-    def step_m(cs):                  # the decode-chain order: quantize, project, quantize, project, ...
+    def step_m(cs, rt=route):        # the decode-chain order: qkv, o, gate_up, down, each from its BF16 activation
         for c in cs:
-            api.nvfp4_quantize_act(c["x"], out=c["xq"])
-            gemv_call(api, c, weights[c["name"]], ws)
+            project(api, c, weights[c["name"]], ws, rt)
 
-    for M in order:                  # initialises kernel attributes outside capture
-        step_m(groups[M])
+    for M in order:                  # initialises kernel attributes outside capture; the quantized
+        step_m(groups[M], "two-call")    # activations the GEMV-only graph reads
+        if route == "one-call":
+            step_m(groups[M])
     torch.cuda.synchronize()
-    # The whole step (every M, decode-chain order: quantize -> GEMV with
-    # programmatic dependent launches) is one CUDA graph; so are the GEMV
-    # launches alone, whose replays time the GEMV kernel for the roofline.  Per
-    # M, a graph of its GEMVs alone gives the per-M breakdown.
+    # The whole step (every M, decode-chain order, programmatic dependent
+    # launches between the kernels) is one CUDA graph; so are the GEMV
+    # launches alone (on the quantized activations), whose replays time the
+    # GEMV kernel for the roofline.  Per M, a graph of its GEMVs alone gives
+    # the per-M breakdown; the other route's step is a graph of its own.
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        g_step, g_gemv = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_step, g_gemv, g_other = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), None
         with torch.cuda.graph(g_step, stream=stream):
             for M in order:
                 step_m(groups[M])
+        if args.weights == "packed":       # the other route, timed after the main steps for comparison
+            g_other = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_other, stream=stream):
+                for M in order:
+                    step_m(groups[M], other)
         with torch.cuda.graph(g_gemv, stream=stream):
             for M in order:
                 gemv_all(groups[M])
@@ -304,6 +336,14 @@ def run_ours(args, world, rank):
                     ev_m[k][i][0].record()
                     ggraphs[M].replay()
                     ev_m[k][i][1].record()
+            if g_other is not None:
+                for _ in range(3):
+                    g_other.replay()
+                o0, o1 = ev(), ev()
+                o0.record()
+                for k in range(args.steps):
+                    g_other.replay()
+                o1.record()
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(world, t0.elapsed_time(t1))
@@ -311,10 +351,12 @@ def run_ours(args, world, rank):
     gemv_ms_total = float(np.mean([a.elapsed_time(b) for a, b in ev_gemv]))
     gemv_ms = {M: float(np.mean([ev_m[k][i][0].elapsed_time(ev_m[k][i][1]) for k in range(args.steps)]))
                for i, M in enumerate(order)}
+    other_ms = o0.elapsed_time(o1) / args.steps if g_other is not None else None
     per_call = None if args.no_extras else cold_per_call(calls, weights, ws)
     proj = None if args.no_extras else per_projection(calls, weights, ws)
 
-    step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
+    route_bytes = lambda c, rt: c["qg_bytes"] if rt == "one-call" else c["gemv_bytes"] + c["q_bytes"]
+    step_bytes = sum(route_bytes(c, route) for c in calls)
     value_gbs = aggregate_gbs(world, step_bytes, args.steps, ms_total)
     gemv_bytes_total = sum(c["gemv_bytes"] for c in calls)
     per_m = {f"M{M}": {"gemv_us_per_call": round(gemv_ms[M] * 1e3 / len(groups[M]), 2),
@@ -322,8 +364,8 @@ def run_ours(args, world, rank):
              for M in order}
     peak, peak_kind = measured_peaks()
     cuda_cores = False                # the CUDA-core kernel is a test cross-check, not a bench path
-    # per call: the quantizer and the GEMV (+ the activation-record kernel on the CUDA-core path)
-    launches_per_call = 3 if cuda_cores else 2
+    # the quantizer and the GEMV, or one launch of the GEMV that quantizes its activation
+    launches_per_step = sum(1 if route == "one-call" and one_launch(c["M"], c["N"], c["K"]) else 2 for c in calls)
     gemv_name = ("nvfp4_gemv_smallm_packed (tensor-core GEMV kernel)" if args.weights == "packed" else
                  "nvfp4_gemv_smallm (" + ("activation-record + CUDA-core GEMV kernels" if cuda_cores
                                           else "tensor-core GEMV kernel") + ")")
@@ -335,6 +377,10 @@ def run_ours(args, world, rank):
         "data": "synthetic (seeded N(0,0.02) weights; N(0,1) activations with 1% x20 outlier channels)",
         "config": {"workload": f"{args.workload} decode projections qkv/o/gate_up/down, M={Ms[0]}..{Ms[-1]}, "
                                f"quantize+GEMV per call",
+                   "route": route + (" (nvfp4_quantize_gemv_packed: one launch for M <= 3, quantizer + GEMV above)"
+                                     if route == "one-call" else " (nvfp4_quantize_act + nvfp4_gemv_smallm)"),
+                   "bytes": "per call: weights + BF16 activation + FP32 output (one-call route); two-call "
+                            "route: + the quantized activation written and read",
                    "calls_per_step": len(calls), "weights": args.weights, "weights_resident_gb": round(sum(
                        w.packed.numel() if hasattr(w, "packed") else w.codes.numel() + w.scales.numel()
                        for w in weights.values()) / 1e9, 3),
@@ -350,9 +396,14 @@ def run_ours(args, world, rank):
                                "(one graph of the step's GEMV launches alone, replayed right after the timed steps)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clocks,
-        "gpu_launches": len(calls) * launches_per_call * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "per_m": per_m,
     }
+    if other_ms is not None:
+        result["other_route"] = {"route": other, "ms_per_step": round(other_ms, 4),
+                                 "gbs": round(sum(route_bytes(c, other) for c in calls) / (other_ms * 1e-3) / 1e9, 1),
+                                 "method": "the same step through the other route, one graph replayed after the "
+                                           "timed steps"}
     if proj is not None:
         result["per_proj"] = proj
     if per_call is not None:
@@ -380,7 +431,8 @@ def per_projection(calls, weights, ws, R=64, trials=5):
     chain), replayed after an L2 flush.  Call r reads weight copy r mod n, with
     n chosen so that the other copies between two uses of one copy exceed
     2x the L2 size: every call streams its weights from HBM.  A second graph
-    chains quantize -> GEMV pairs.  Median over `trials` replays."""
+    chains quantize -> GEMV pairs, a third nvfp4_quantize_gemv_packed calls.
+    Median over `trials` replays."""
     from nvfp4_w4a4_decode_gemv_gb300 import api
     peak, _ = measured_peaks()
     l2 = _l2_bytes()
@@ -396,18 +448,21 @@ def per_projection(calls, weights, ws, R=64, trials=5):
         cp = copies[c["name"]]
         graphs = {}
         with torch.cuda.stream(stream):
-            for with_q in (False, True):
+            for with_q in (False, True, "one"):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     for r in range(R):
+                        if with_q == "one":
+                            api.nvfp4_quantize_gemv_packed(c["x"], cp[r % len(cp)], y=c["y"], workspace=ws)
+                            continue
                         if with_q:
                             api.nvfp4_quantize_act(c["x"], out=c["xq"])
                         gemv_call(api, c, cp[r % len(cp)], ws)
                 graphs[with_q] = g
-        t = {False: [], True: []}
+        t = {False: [], True: [], "one": []}
         with torch.cuda.stream(stream):
             for _ in range(trials):
-                for with_q in (False, True):
+                for with_q in (False, True, "one"):
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     flush.zero_()
                     e0.record()
@@ -415,12 +470,14 @@ def per_projection(calls, weights, ws, R=64, trials=5):
                     e1.record()
                     e1.synchronize()
                     t[with_q].append(e0.elapsed_time(e1) * 1e3 / R)
-        g_us, q_us = float(np.median(t[False])), float(np.median(t[True]))
+        g_us, q_us, o_us = float(np.median(t[False])), float(np.median(t[True])), float(np.median(t["one"]))
         gbs = c["gemv_bytes"] / (g_us * 1e-6) / 1e9
         qgbs = (c["gemv_bytes"] + c["q_bytes"]) / (q_us * 1e-6) / 1e9
         out[f"{c['name']}_M{c['M']}"] = {"gemv_us": round(g_us, 3), "gemv_gbs": round(gbs, 1),
                                          "frac": round(gbs / peak, 4), "frac_spec": round(gbs / SPEC_HBM_GBS, 4),
-                                         "quant_gemv_us": round(q_us, 3), "quant_gemv_gbs": round(qgbs, 1)}
+                                         "quant_gemv_us": round(q_us, 3), "quant_gemv_gbs": round(qgbs, 1),
+                                         "one_call_us": round(o_us, 3),
+                                         "one_call_gbs": round(c["qg_bytes"] / (o_us * 1e-6) / 1e9, 1)}
         del graphs
     del flush, copies
     torch.cuda.synchronize()
@@ -552,7 +609,8 @@ def run_e2e(args, calls, weights, ws):
     """The step end to end through the public API, with the step's activations
     arriving in one copy from pinned host memory and its outputs leaving in one
     copy to pinned host memory, both inside the timed region.  `value`: the
-    step's 64 API calls captured once in a CUDA graph (as a decode loop runs
+    step's API calls (one per projection on the one-call route, two on the
+    two-call route) captured once in a CUDA graph (as a decode loop runs
     them) and replayed between the two copies; `eager`: the same calls issued
     one by one from Python each step.  (One copy per M group on a second
     stream, overlapped with the other groups' compute, measured slower: 1.21
@@ -570,10 +628,11 @@ def run_e2e(args, calls, weights, ws):
     dev_x = [v.view(c["x"].shape) for v, c in zip(torch.split(dev_xa, x_sizes), calls)]
     dev_y = [v.view(c["y"].shape) for v, c in zip(torch.split(dev_ya, y_sizes), calls)]
 
+    route = args.route if args.weights == "packed" else "two-call"
+
     def compute():
         for j, c in enumerate(calls):
-            api.nvfp4_quantize_act(dev_x[j], out=c["xq"])
-            gemv_call(api, c, weights[c["name"]], ws, y=dev_y[j])
+            project(api, c, weights[c["name"]], ws, route, x=dev_x[j], y=dev_y[j])
 
     def check():
         for j, c in enumerate(calls):        # the arena path computes what the per-call buffers hold
@@ -583,7 +642,7 @@ def run_e2e(args, calls, weights, ws):
             raise RuntimeError("end-to-end outputs did not all reach the host")
 
     stream = torch.cuda.Stream()
-    step_bytes = sum(c["gemv_bytes"] + c["q_bytes"] for c in calls)
+    step_bytes = sum(c["qg_bytes"] if route == "one-call" else c["gemv_bytes"] + c["q_bytes"] for c in calls)
     out = {}
     with torch.cuda.stream(stream):
         dev_xa.copy_(host_x, non_blocking=True)
@@ -621,8 +680,9 @@ def run_e2e(args, calls, weights, ws):
     return {"value": out["graph"]["value"], "unit": "GB/s", "ms_per_step": out["graph"]["ms_per_step"],
             "h2d_bytes_per_step": int(host_x.numel() * host_x.element_size()),
             "d2h_bytes_per_step": int(host_y.numel() * host_y.element_size()),
-            "method": "per step: pinned host->device copy of the activations, the step's 64 API calls "
-                      "(captured once in a CUDA graph, replayed), device->host copy of all outputs",
+            "method": f"per step: pinned host->device copy of the activations, the step's {len(calls)} projections "
+                      f"({route} route; API calls captured once in a CUDA graph, replayed), device->host copy of "
+                      f"all outputs",
             "eager": out["eager"]}
 
 

@@ -225,6 +225,41 @@ nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, cons
                                       const uint8_t* wpacked, const float* wg, int N, int K, float* y,
                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * nvfp4_quantize_act of a BF16 activation followed by nvfp4_gemv_smallm_packed,
+ * as one call: y[m, n] = xg * wg * sum_k e2m1(xq[m,k]) e4m3(xs[m,k/16])
+ * e2m1(wq[n,k]) e4m3(ws[n,k/16]), where wq, ws are the codes and scales the
+ * packed image holds and xq, xs, xg exactly what nvfp4_quantize_act(x) would
+ * write (the
+ * activation quantizer "Q" in front of every decode projection: ReSET
+ * reading note §5.3, Table 3).  y holds the same bits as the two calls.
+ * For M <= 3 and M * K <= 65536 it is one launch (tuning knobs
+ * NVFP4_QGEMV_MAX_M, NVFP4_QGEMV_MAX_MK): every CTA of the GEMV reads the
+ * whole activation for its maximum and quantizes the 256-K chunks it
+ * multiplies into shared memory, so the quantized activation never goes
+ * through HBM and one kernel boundary of a decode chain disappears.  Larger
+ * activations, or a CTA that would hold more than 24 chunks or quantize more
+ * than 1024 blocks (NVFP4_QGEMV_MAX_BLOCKS), take two launches: the library
+ * quantizes into the workspace, then multiplies.
+ *   x        device, BF16 [M, K] row-major, 16-byte aligned
+ *   M        1..8 (else NVFP4_ERR_RANGE)
+ *   wpacked, wg, N, K   as nvfp4_gemv_smallm_packed
+ *   y        device, [M, N] FP32, 16-byte aligned (written)
+ *   xg_out   device float receiving the activation's global scale amax / 2688,
+ *            4-byte aligned, or NULL
+ *   workspace  device scratch of at least
+ *            nvfp4_quantize_gemv_workspace_bytes(M, N, K) bytes, 256-byte
+ *            aligned; the same contract as the GEMV workspace (zeroed once,
+ *            left ready, one per set of calls that overlap on the GPU); a
+ *            zeroed workspace may serve this call and the GEMV calls alike.
+ * Errors, co-residency and device error bits as nvfp4_gemv_smallm.
+ */
+size_t nvfp4_quantize_gemv_workspace_bytes(int M, int N, int K);
+
+nvfp4_status nvfp4_quantize_gemv_packed(const uint16_t* x_bf16, int M, const uint8_t* wpacked,
+                                        const float* wg, int N, int K, float* y, float* xg_out,
+                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill-sized NVFP4 GEMM (M up to 128)                                      */
 /* ------------------------------------------------------------------------ */

@@ -14,7 +14,7 @@ __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_smallm_cudacore", "DEVERR_FLAG_TIMEOUT", "nvfp4_gemm_packed", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
-    "NVFP4PackedWeight", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
+    "NVFP4PackedWeight", "nvfp4_quantize_gemv_packed", "nvfp4_quantize_gemv_workspace_bytes", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
     "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
     "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
@@ -110,6 +110,9 @@ class GemvWorkspace:
         need = nvfp4_gemv_workspace_bytes(M, N, K)
         if need == 0:
             raise ValueError(f"unsupported GEMV shape M={M} N={N} K={K}")
+        return self.get_bytes(need)
+
+    def get_bytes(self, need: int) -> torch.Tensor:
         if self.buf.numel() < need:
             self.buf = torch.zeros(need + 4096, dtype=torch.uint8, device=self.device)
         return self.buf
@@ -190,6 +193,33 @@ def nvfp4_gemv_smallm_packed(x: NVFP4Tensor, w: NVFP4PackedWeight, y: torch.Tens
     check(lib().nvfp4_gemv_smallm_packed(ptr(x.codes), ptr(x.scales), ptr(x.global_scale), M, ptr(w.packed),
                                          ptr(w.global_scale), N, K, ptr(y), ptr(ws), ws.numel(),
                                          stream_handle(stream)), "nvfp4_gemv_smallm_packed")
+    return y
+
+
+def nvfp4_quantize_gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_quantize_gemv_workspace_bytes(M, N, K))
+
+
+def nvfp4_quantize_gemv_packed(x_bf16: torch.Tensor, w: NVFP4PackedWeight, y: torch.Tensor | None = None,
+                               xg_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                               stream=None) -> torch.Tensor:
+    """nvfp4_quantize_act(x_bf16) then nvfp4_gemv_smallm_packed, as one call (one launch where it fits)."""
+    _need_cuda(x_bf16, y, xg_out)
+    if x_bf16.dtype != torch.bfloat16 or x_bf16.dim() != 2:
+        raise ValueError("x_bf16 must be a 2-D bfloat16 tensor")
+    M, K = x_bf16.shape
+    N = w.N
+    if w.K != K:
+        raise ValueError("x and w disagree on K")
+    y = y if y is not None else torch.empty((M, N), dtype=torch.float32, device=x_bf16.device)
+    if workspace is None:
+        need = nvfp4_quantize_gemv_workspace_bytes(M, N, K)
+        if need == 0:
+            raise ValueError(f"unsupported shape M={M} N={N} K={K}")
+        workspace = _ws_for(x_bf16.device).get_bytes(need)
+    check(lib().nvfp4_quantize_gemv_packed(ptr(x_bf16), M, ptr(w.packed), ptr(w.global_scale), N, K, ptr(y),
+                                           ptr(xg_out), ptr(workspace),
+                                           workspace.numel(), stream_handle(stream)), "nvfp4_quantize_gemv_packed")
     return y
 
 

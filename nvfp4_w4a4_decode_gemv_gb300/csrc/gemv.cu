@@ -507,6 +507,10 @@ cudaError_t nvfp4_internal_bf16_gemv_tc(const uint16_t* x, int M, const uint16_t
 cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const float* xg, int M, const uint8_t* wq,
                                    const uint8_t* ws, const uint8_t* wpacked, const float* wg, int N, int K, float* y,
                                    unsigned int* records, int grid_cap, int max_ctas_per_sm, cudaStream_t stream);
+cudaError_t nvfp4_internal_quantize_gemv_tc(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg, int N,
+                                            int K, float* y, float* xg_out, unsigned int* records, int grid_cap,
+                                            int max_ctas_per_sm, long long max_blocks, cudaStream_t stream,
+                                            bool* launched);
 size_t nvfp4_internal_packed_bytes(int N, int K);
 cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
                                         cudaStream_t stream);
@@ -645,6 +649,81 @@ extern "C" nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_
   return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(
       xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y, reinterpret_cast<unsigned int*>(wsb + wl.tcrec),
       gemv_grid_cap(), kMaxCtasPerSm, stream));
+}
+
+// The activation quantizer and the packed GEMV as one call.  One launch
+// (the kernel quantizes the activation chunks each CTA needs, after reading
+// the whole activation for its maximum) while M is at most the knob
+// NVFP4_QGEMV_MAX_M, M * K at most NVFP4_QGEMV_MAX_MK, no CTA quantizes more
+// than NVFP4_QGEMV_MAX_BLOCKS blocks and every CTA's chunks fit its shared
+// memory; otherwise
+// nvfp4_quantize_act into the workspace's tail, then the GEMV.
+namespace {
+int qgemv_max_mk() {
+  static const int v = env_int("NVFP4_QGEMV_MAX_MK", 65536);
+  return v;
+}
+// Blocks of 16 activation values one CTA may quantize (each CTA repeats the
+// work for the chunks it uses, so past this the two launches are faster).
+int qgemv_max_blocks() {
+  static const int v = env_int("NVFP4_QGEMV_MAX_BLOCKS", 1024);
+  return v;
+}
+// Tokens up to which the one-launch route is taken: every CTA reads the
+// whole activation for its maximum, and past three tokens those reads cost
+// more in a decode chain than the kernel boundary they remove.
+int qgemv_max_m() {
+  static const int v = env_int("NVFP4_QGEMV_MAX_M", 3);
+  return v;
+}
+struct QgLayout {
+  size_t codes, scales, global, total;
+};
+QgLayout qg_layout(int M, int N, int K) {
+  QgLayout l;
+  l.codes = ws_layout(M, N, K).total;
+  l.scales = l.codes + align256((size_t)M * K / 2);
+  l.global = l.scales + align256((size_t)M * K / 16);
+  l.total = l.global + 256;
+  return l;
+}
+}  // namespace
+
+extern "C" size_t nvfp4_quantize_gemv_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
+  return qg_layout(M, N, K).total;
+}
+
+extern "C" nvfp4_status nvfp4_quantize_gemv_packed(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg,
+                                                   int N, int K, float* y, float* xg_out, void* workspace,
+                                                   size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !wpacked || !wg || !y || !workspace) return NVFP4_ERR_NULL;
+  if (M < 1 || M > kMaxM) return NVFP4_ERR_RANGE;
+  if (N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return NVFP4_ERR_SHAPE;
+  if (!nvfp4_internal_aligned(x, 16) || !nvfp4_internal_aligned(wpacked, 16) || !nvfp4_internal_aligned(y, 16) ||
+      !nvfp4_internal_aligned(wg, 4) || (xg_out && !nvfp4_internal_aligned(xg_out, 4)) ||
+      !nvfp4_internal_aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  const QgLayout ql = qg_layout(M, N, K);
+  if (workspace_bytes < ql.total) return NVFP4_ERR_SHAPE;
+  nvfp4_status ds = nvfp4_internal_check_device();
+  if (ds != NVFP4_OK) return ds;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  unsigned int* records = reinterpret_cast<unsigned int*>(wsb + ws_layout(M, N, K).tcrec);
+  if (M <= qgemv_max_m() && (long long)M * K <= (long long)qgemv_max_mk()) {
+    bool launched = false;
+    const cudaError_t e = nvfp4_internal_quantize_gemv_tc(x, M, wpacked, wg, N, K, y, xg_out, records,
+                                                          gemv_grid_cap(), kMaxCtasPerSm, qgemv_max_blocks(), stream,
+                                                          &launched);
+    if (e != cudaSuccess || launched) return nvfp4_internal_cuda_status(e);
+  }
+  uint8_t* xq = wsb + ql.codes;
+  uint8_t* xs = wsb + ql.scales;
+  float* xg = xg_out ? xg_out : reinterpret_cast<float*>(wsb + ql.global);
+  const nvfp4_status qs = nvfp4_quantize_act(x, M, K, xq, xs, xg, stream);
+  if (qs != NVFP4_OK) return qs;
+  return nvfp4_internal_cuda_status(nvfp4_internal_gemv_tc(xq, xs, xg, M, nullptr, nullptr, wpacked, wg, N, K, y,
+                                                           records, gemv_grid_cap(), kMaxCtasPerSm, stream));
 }
 
 // BF16 GEMV on the tensor-core kernel: it needs only the records region of a

@@ -50,6 +50,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "quant_block.cuh"
 #include "tcgen05.cuh"
 
 NVFP4_DEFINE_ERROR_READER(nvfp4_internal_read_error_gemv_tc)
@@ -88,12 +89,27 @@ constexpr uint32_t kIdescBF16 =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNT >> 3) << 17) | ((uint32_t)(kTR >> 4) << 24);
 constexpr uint32_t kStageTxBF16 = kCodeBytes + kActCodeBytes;
 
+// Activation quantized in the kernel (nvfp4_quantize_gemv_packed).  The ring
+// slots carry weights only (one packed block); the CTA's activation chunks
+// stay in shared memory for the whole call: chunk i's token codes are one
+// 128-byte-swizzled atom of 8 rows at res + 1024 i (rows >= M zero), so the
+// MMA's 16-row B operand reads rows 8-15 from the next atom -- accumulator
+// columns 8-15, which nothing reads -- and an extra zero atom follows the
+// last chunk; chunk i's token scales are 16 rows x 16 bytes at res_sc + 256 i.
+constexpr int kSlotQX = kPackedBlock;       // 18432, 1024-aligned
+constexpr int kMaxRes = 24;                 // activation chunks a CTA may hold
+constexpr int kResCodeBytes = (kMaxRes + 1) * 1024;
+constexpr int kResScaleBytes = kMaxRes * 256;
+constexpr int kQThreads = 256;              // warps 2-9 quantize
+
 struct TcArgs {
   const uint8_t* wpacked;        // packed weights, or null: weights through the two tensor maps
   const float* xg;
   const float* wg;
   float* y;
   unsigned int* records;         // [G][M][128] words: a CTA's partial sums of its first tile; zero between calls
+  const uint16_t* x;             // QX: BF16 activation [M, K]
+  float* xg_out;                 // QX: receives the activation's global scale (may be null)
   int M, N, K, C, RT;
   long long U;                   // units = RT * C, numbered tile-major
   uint32_t flag_spins;           // polls of a record before the wait gives up (kFlagSpinLimit)
@@ -225,27 +241,147 @@ NVFP4_DEVINL void read_acc(uint32_t tmem, int quad, int d, uint64_t* acc_empty_d
   for (int i = 0; i < kNT; ++i) acc[i] = __uint_as_float(r[i]);
 }
 
-template <int M, int S, bool BF>
+NVFP4_DEVINL void qx_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kQThreads) : "memory"); }
+
+// The activation quantizer inside the GEMV (QX), run by warps 2-9 of every CTA.
+// Each CTA reads the whole BF16 activation for its maximum -- so no CTA waits
+// for another -- and quantizes the nres chunks it uses (chunk0, chunk0 + 1,
+// ... mod C) into the resident atoms and scale rows, with the same recipe and
+// roundings as the quantizer kernels (quant_block), so the codes are the ones
+// nvfp4_quantize_act writes.  The blocks a thread quantizes (the first kQR,
+// which is all of them for the shapes the host sends here) are loaded together
+// with the maximum's pass, so the activation crosses L2 once after the wait.
+// Returns the global scale amax / 2688.
+constexpr int kQR = 2;                       // blocks a quantizing thread holds in registers
+
+template <int M>
+NVFP4_DEVINL void qx_store_block(uint8_t* res, uint8_t* res_sc, int rb, const uint4 (&raw)[2], float g) {
+  const int i = rb / (16 * M), m = (rb >> 4) % M, j = rb & 15;
+  const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+  float v[16];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v[2 * e] = bf16_lo(w[e]);
+    v[2 * e + 1] = bf16_hi(w[e]);
+  }
+  uint2 codes;
+  const uint32_t sc = quant_block(v, block_absmax(v), g, codes);
+  // row m of the atom: 16-byte piece p at m*128 + ((p ^ m) * 16), as the TMA's
+  // 128-byte swizzle places it; block j is the half (j & 1) of piece j/2.
+  *reinterpret_cast<uint2*>(res + i * 1024 + m * 128 + ((((j >> 1) ^ m) & 7) << 4) + (j & 1) * 8) = codes;
+  res_sc[i * 256 + m * 16 + j] = static_cast<uint8_t>(sc);
+}
+
+// Block rb = (i, m, j) of the resident chunks (block j of 16 fastest, then
+// token m, then chunk i): its two 16-byte pieces of x.
+template <int M>
+NVFP4_DEVINL void qx_load_block(const TcArgs& a, int rb, int chunk0, uint4 (&raw)[2]) {
+  const int i = rb / (16 * M), m = (rb >> 4) % M, j = rb & 15;
+  int c = chunk0 + i;
+  if (c >= a.C) c -= a.C;
+  const uint4* p = reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + (size_t)c * kChunk + j * 16);
+  raw[0] = __ldcg(p);
+  raw[1] = __ldcg(p + 1);
+}
+
+template <int M>
+NVFP4_DEVINL float quantize_resident(const TcArgs& a, uint8_t* res, uint8_t* res_sc, uint32_t* s_wmax, int nres,
+                                     int chunk0) {
+  const int qt = (int)threadIdx.x - 64;      // 0 .. 255
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const int xbytes = M * K * 2;
+  // While the preceding kernel may still run: zero the atoms (rows >= M and
+  // the trailing atom stay zero) and the scale rows, and ask L2 for x.
+  for (int o = qt * 16; o < (nres + 1) * 1024; o += kQThreads * 16)
+    *reinterpret_cast<uint4*>(res + o) = make_uint4(0u, 0u, 0u, 0u);
+  for (int o = qt * 16; o < nres * 256; o += kQThreads * 16)
+    *reinterpret_cast<uint4*>(res_sc + o) = make_uint4(0u, 0u, 0u, 0u);
+  for (int o = qt * 128; o < xbytes; o += kQThreads * 128) prefetch_l2(reinterpret_cast<const uint8_t*>(a.x) + o);
+  griddep_wait();                            // x comes from the preceding kernel
+  const int nrb = nres * M * 16;
+  uint4 held[kQR][2];
+#pragma unroll
+  for (int u = 0; u < kQR; ++u) {
+    const int rb = qt + u * kQThreads;
+    if (rb < nrb) {
+      qx_load_block<M>(a, rb, chunk0, held[u]);
+    } else {
+      held[u][0] = held[u][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // max |x| over the tensor.  For BF16 magnitudes (sign cleared) the unsigned
+  // order of the bit patterns is the order of the values, so the maximum is
+  // taken on the bits, two halves at a time.
+  const uint4* x4 = reinterpret_cast<const uint4*>(a.x);
+  const int n4 = xbytes / 16;
+  uint32_t mx = 0u;
+  for (int b = qt; b < n4; b += kQThreads * 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = b + u * kQThreads;
+      v[u] = i < n4 ? __ldcg(x4 + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      mx = __vmaxu2(mx, v[u].x & 0x7FFF7FFFu);
+      mx = __vmaxu2(mx, v[u].y & 0x7FFF7FFFu);
+      mx = __vmaxu2(mx, v[u].z & 0x7FFF7FFFu);
+      mx = __vmaxu2(mx, v[u].w & 0x7FFF7FFFu);
+    }
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) s_wmax[qt >> 5] = mx;
+  qx_barrier();
+  uint32_t m8 = lane < kQThreads / 32 ? s_wmax[lane] : 0u;
+  m8 = __reduce_max_sync(0xffffffffu, m8);
+  const float g = __fdiv_rn(__uint_as_float(m8 << 16), 2688.0f);   // 448 * 6
+  if (blockIdx.x == 0 && qt == 0 && a.xg_out) *a.xg_out = g;
+#pragma unroll
+  for (int u = 0; u < kQR; ++u) {
+    const int rb = qt + u * kQThreads;
+    if (rb < nrb) qx_store_block<M>(res, res_sc, rb, held[u], g);
+  }
+  for (int rb = qt + kQR * kQThreads; rb < nrb; rb += kQThreads) {    // beyond what the registers hold
+    uint4 raw[2];
+    qx_load_block<M>(a, rb, chunk0, raw);
+    qx_store_block<M>(res, res_sc, rb, raw, g);
+  }
+  // The MMA reads the atoms through the async proxy.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  qx_barrier();
+  return g;
+}
+
+template <int M, int S, bool BF, bool QX = false>
 __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                               const __grid_constant__ CUtensorMap tm_scales,
                                                               const __grid_constant__ CUtensorMap tm_xcodes,
                                                               const __grid_constant__ CUtensorMap tm_xscales,
                                                               const TcArgs a) {
   static_assert(S >= 2 && kColSF + 32 * S <= kTmemCols, "scale columns must fit the TMEM allocation");
+  static_assert(!(QX && BF), "the in-kernel quantizer produces NVFP4 operands");
+  constexpr int kSl = QX ? kSlotQX : kSlot;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kSlot);
+  uint8_t* res = smem + S * kSl;                        // QX: resident activation atoms
+  uint8_t* res_sc = res + kResCodeBytes;                // QX: their token scale rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kSl + (QX ? kResCodeBytes + kResScaleBytes : 0));
   uint64_t* sf_ready = full + S;
   uint64_t* empty = sf_ready + S;
   uint64_t* acc_full = empty + S;           // [0], [1]: alternating tiles; [2]: the CTA's last tile
   uint64_t* acc_empty = acc_full + 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint32_t* s_wmax = tmem_slot + 4;                     // QX: the quantizing warps' maxima
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
   const long long u0 = unit_start(blockIdx.x, a.U, G);
   const long long u1 = unit_start(blockIdx.x + 1, a.U, G);
   const int nunits = (int)(u1 - u0);
+  const int nres = nunits < a.C ? nunits : a.C;         // QX: activation chunks this CTA uses (<= kMaxRes)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -273,16 +409,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   const int C = a.C;
   const int tile0 = (int)(u0 / C), chunk0 = (int)(u0 % C);
 
+  // QX: warps 2-9 quantize the activation chunks first; the scale writers'
+  // first arrival on sf_ready (which the MMA waits for) follows it.
+  float qg = 0.0f;
+  if (QX && warp >= 2 && nunits > 0) qg = quantize_resident<M>(a, res, res_sc, s_wmax, nres, chunk0);
+
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0 && nunits > 0) {
-      constexpr uint32_t tx = BF ? kStageTxBF16 : kStageTx;
+      constexpr uint32_t tx = QX ? (uint32_t)kPackedBlock : BF ? kStageTxBF16 : kStageTx;
       if (!a.wpacked) {
         prefetch_tmap(&tm_codes);
         if (!BF) prefetch_tmap(&tm_scales);
       }
-      prefetch_tmap(&tm_xcodes);
-      if (!BF) prefetch_tmap(&tm_xscales);
+      if (!QX) {
+        prefetch_tmap(&tm_xcodes);
+        if (!BF) prefetch_tmap(&tm_xscales);
+      }
       const int pre = nunits < S ? nunits : S;
       const uint8_t* wp = a.wpacked ? a.wpacked + (size_t)u0 * kPackedBlock : nullptr;
       // Weight tiles do not depend on the preceding kernel: issue the first
@@ -290,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       {
         int tile = tile0, c = chunk0;
         for (int k = 0; k < pre; ++k) {
-          uint8_t* slot = smem + k * kSlot;
+          uint8_t* slot = smem + k * kSl;
           mbar_arrive_expect_tx(&full[k], tx);
           if (wp) {
             bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[k]);
@@ -301,20 +444,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
           if (++c == C) { c = 0; ++tile; }
         }
       }
-      griddep_wait();          // the token codes and scales come from the preceding kernel
       int tile = tile0, c = chunk0;
-      for (int k = 0; k < pre; ++k) {
-        uint8_t* slot = smem + k * kSlot;
-        tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[k]);      // rows >= M arrive as zeros
-        if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
-        if (++c == C) { c = 0; ++tile; }
+      if (!QX) {               // (QX: the activation is quantized in this CTA; weights only here)
+        griddep_wait();        // the token codes and scales come from the preceding kernel
+        for (int k = 0; k < pre; ++k) {
+          uint8_t* slot = smem + k * kSlot;
+          tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[k]);      // rows >= M arrive as zeros
+          if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[k]);
+          if (++c == C) { c = 0; ++tile; }
+        }
+      } else {
+        for (int k = 0; k < pre; ++k)
+          if (++c == C) { c = 0; ++tile; }
       }
       int issued = pre;
       int s = pre % S;
       uint32_t phase = (pre / S) & 1;                    // phase of the slot's next fill
       for (int k = pre; k < nunits; ++k) {
         if (!mbar_wait(&empty[s], phase ^ 1u)) break;   // the slot's previous use has been consumed
-        uint8_t* slot = smem + s * kSlot;
+        uint8_t* slot = smem + s * kSl;
         mbar_arrive_expect_tx(&full[s], tx);
         if (wp) {
           bulk_g2s(slot, wp + (size_t)k * kPackedBlock, kPackedBlock, &full[s]);
@@ -322,8 +470,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
           tma_load_2d(slot, &tm_codes, c * 128, tile * kTR, &full[s]);
           if (!BF) tma_load_2d(slot + kOffSA, &tm_scales, c * 16, tile * kTR, &full[s]);
         }
-        tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[s]);
-        if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
+        if (!QX) {
+          tma_load_2d(slot + kOffB, &tm_xcodes, c * 128, 0, &full[s]);
+          if (!BF) tma_load_2d(slot + kOffSB, &tm_xscales, c * 16, 0, &full[s]);
+        }
         issued = k + 1;
         if (++c == C) { c = 0; ++tile; }
         if (++s == S) { s = 0; phase ^= 1u; }
@@ -338,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       // Descriptors of slot 0; the start-address field (bits 0-13, address / 16)
       // moves by (slot offset + 32 q) / 16 within the 14-bit field.
       const uint64_t da0 = smem_desc_sw128(smem_u32(smem));
-      const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB));
+      const uint64_t db0 = smem_desc_sw128(smem_u32(QX ? res : smem + kOffB));
       // The CTA's last tile accumulates in its own buffer (D_last), flushed by
       // the scale writers; the others alternate between D0 and D1.
       const int last_idx = (int)((u1 - 1) / C) - tile0;
@@ -347,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       int s = 0;
       uint32_t phase = 0;
       int issued = 0;
+      int ri = 0;                                        // QX: resident chunk of the unit
       uint32_t d_tmem = tmem;
       for (int k = 0; k < nunits; ++k) {
         const bool first_of_tile = (k == 0) || (c == 0);
@@ -364,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
         // BF16 has no scales: the MMA waits for the slot itself.
         if (!mbar_wait(BF ? &full[s] : &sf_ready[s], phase)) break;
         tc_fence_after();
-        const uint64_t doff = (uint64_t)((s * kSlot) >> 4);
+        const uint64_t doff = (uint64_t)((s * kSl) >> 4);
+        const uint64_t dboff = QX ? (uint64_t)(ri * (1024 >> 4)) : doff;
         const uint32_t sfa = tmem + kColSF + 32u * s;
         const uint32_t sfb = sfa + 16u;
 #pragma unroll
@@ -372,11 +524,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
           if (BF)
             mma_f16(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdescBF16, (first_of_tile && q == 0) ? 0u : 1u);
           else
-            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + doff + 2 * q, kIdesc, sfa + 4u * q, sfb + 4u * q,
+            mma_mxf4nvf4(d_tmem, da0 + doff + 2 * q, db0 + dboff + 2 * q, kIdesc, sfa + 4u * q, sfb + 4u * q,
                          (first_of_tile && q == 0) ? 0u : 1u);
         }
         mma_commit(&empty[s]);
         issued = k + 1;
+        if (QX && ++ri == C) ri = 0;
         if (++c == C) c = 0;
         if (k + 1 == nunits || c == 0)                                          // last unit of this tile
           mma_commit(&acc_full[tile_idx == last_idx ? 2 : (tile_idx & 1)]);
@@ -391,16 +544,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     // waiting on that kernel here costs nothing, and the output scale's load
     // overlaps the whole stream.
     griddep_wait();
-    const float yscale = output_scale<BF>(a);
+    const float yscale = QX ? __fmul_rn(qg, __ldcg(a.wg)) : output_scale<BF>(a);
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t ta0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + (uint32_t)quad;
     const uint32_t tb0 = tmem + ((uint32_t)(quad * 32) << 16) + kColSF + 16u;
     int s = 0;
     uint32_t phase = 0;
+    int ri = 0;                                        // QX: resident chunk of the unit
     for (int k = 0; k < (BF ? 0 : nunits); ++k) {     // BF16 has no scales to place
       if (!mbar_wait_warp(&full[s], phase)) break;
-      const uint8_t* slot = smem + s * kSlot;
+      const uint8_t* slot = smem + s * kSl;
       const uint4 sa = *reinterpret_cast<const uint4*>(slot + kOffSA + row * 16);
       const uint32_t ta = ta0 + 32u * s;
       tmem_st1(ta, sa.x);
@@ -410,7 +564,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
       // Token scales: the MMA reads token n's scales for accumulator rows of
       // quadrant p from lane 32p + n, so every quadrant holds a copy.
       uint4 sb = make_uint4(0u, 0u, 0u, 0u);
-      if (lane < kNT) sb = *reinterpret_cast<const uint4*>(slot + kOffSB + lane * 16);
+      if (lane < kNT) sb = *reinterpret_cast<const uint4*>(QX ? res_sc + ri * 256 + lane * 16 : slot + kOffSB + lane * 16);
+      if (QX && ++ri == C) ri = 0;
       const uint32_t tb = tb0 + 32u * s;
       tmem_st1(tb, sb.x);
       tmem_st1(tb + 4u, sb.y);
@@ -464,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     // ---------------- epilogue: rows 32*quad .. 32*quad + 31 ----------------
     const int quad = warp & 3;
     griddep_wait();            // y and the records belong to the preceding kernel's era
-    const float yscale = output_scale<BF>(a);
+    const float yscale = QX ? __fmul_rn(qg, __ldcg(a.wg)) : output_scale<BF>(a);
     // Every tile but the CTA's last (that one is flushed by the scale writers).
     const int tile_last = nunits > 0 ? (int)((u1 - 1) / C) : tile0 - 1;
     for (int tile = tile0, tile_idx = 0; tile < tile_last; ++tile, ++tile_idx) {
@@ -490,9 +645,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   }
 }
 
-template <int S>
+template <int S, bool QX = false>
 constexpr size_t tc_smem_bytes() {
-  return (size_t)S * kSlot + 1024 + (3 * S + 5) * sizeof(uint64_t) + 16;
+  return QX ? (size_t)S * kSlotQX + kResCodeBytes + kResScaleBytes + 1024 + (3 * S + 5) * sizeof(uint64_t) + 64
+            : (size_t)S * kSlot + 1024 + (3 * S + 5) * sizeof(uint64_t) + 16;
 }
 
 struct TcMaps {
@@ -518,12 +674,12 @@ int tc_stages() {
 // (plus the 1 KB the driver reserves per CTA), TMEM columns and registers
 // (allocated per warp in units of 256).  Sets the kernel's attributes on each
 // device the first time; 0 and *err on failure.
-template <int M, int S, bool BF>
+template <int M, int S, bool BF, bool QX = false>
 int tc_per_sm_fit(cudaError_t* err) {
   static PerDeviceInt fit;
   return fit.get([](int dev, cudaError_t* e_out) -> int {
-    constexpr size_t smem = tc_smem_bytes<S>();
-    auto kern = gemv_tc_kernel<M, S, BF>;
+    constexpr size_t smem = tc_smem_bytes<S, QX>();
+    auto kern = gemv_tc_kernel<M, S, BF, QX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) {
@@ -567,30 +723,41 @@ void nvfp4_internal_test_gemv_fault(unsigned int flag_spin_limit, int drop_recor
 uint32_t nvfp4_internal_test_flag_spins() { return g_test_flag_spins.load(std::memory_order_relaxed); }
 int nvfp4_internal_test_drop_records() { return g_test_drop_records.load(std::memory_order_relaxed); }
 
-template <int M, int S, bool BF = false>
-static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm) {
+// Launches the kernel; with QX, only when no CTA has more than kMaxRes
+// activation chunks to hold (*launched = false otherwise, nothing launched).
+template <int M, int S, bool BF = false, bool QX = false>
+static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm,
+                             bool* launched = nullptr, long long qx_max_blocks = 0) {
   cudaError_t e = cudaSuccess;
-  const int fit = tc_per_sm_fit<M, S, BF>(&e);
+  if (launched) *launched = false;
+  const int fit = tc_per_sm_fit<M, S, BF, QX>(&e);
   if (fit == 0) return e;
   const int per_sm = fit < max_ctas_per_sm ? fit : max_ctas_per_sm;
   long long G = (long long)per_sm * nvfp4_internal_device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
   if (G > tc_grid_max()) G = tc_grid_max();  // records exist for that many CTAs
+  if (QX) {
+    const long long most_units = (a.U + G - 1) / G;          // a CTA's units: floor or ceil of U / G
+    const long long most_res = most_units < a.C ? most_units : a.C;
+    if (most_res > kMaxRes || most_res * M * 16 > qx_max_blocks) return cudaSuccess;
+  }
   const uint32_t spins = g_test_flag_spins.load(std::memory_order_relaxed);
   a.flag_spins = spins ? spins : kFlagSpinLimit;
   a.drop_records = g_test_drop_records.load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = tc_smem_bytes<S>();
+  cfg.dynamicSmemBytes = tc_smem_bytes<S, QX>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<M, S, BF>, mp.w_codes, mp.w_scales, mp.x_codes, mp.x_scales, a);
+  e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel<M, S, BF, QX>, mp.w_codes, mp.w_scales, mp.x_codes, mp.x_scales, a);
+  if (launched) *launched = true;
+  return e;
 }
 
 template <int M>
@@ -641,6 +808,43 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
     case 6: return launch_tc_m<6>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     case 7: return launch_tc_m<7>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
     default: return launch_tc_m<8>(stages, mp, a, stream, grid_cap, max_ctas_per_sm);
+  }
+}
+
+// The activation quantizer and the GEMV in one launch (QX), packed weights,
+// the default ring depth.  *launched = false when a CTA would hold more than
+// kMaxRes activation chunks or quantize more than max_blocks blocks: the
+// caller then quantizes and multiplies in two launches.
+cudaError_t nvfp4_internal_quantize_gemv_tc(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg, int N,
+                                            int K, float* y, float* xg_out, unsigned int* records, int grid_cap,
+                                            int max_ctas_per_sm, long long max_blocks, cudaStream_t stream,
+                                            bool* launched) {
+  TcMaps mp;
+  memset(&mp, 0, sizeof(mp));   // no tensor maps: weights packed, activation quantized in the kernel
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.wpacked = wpacked;
+  a.xg = nullptr;
+  a.wg = wg;
+  a.y = y;
+  a.records = records;
+  a.x = x;
+  a.xg_out = xg_out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.C = K / kChunk;
+  a.RT = (N + kTR - 1) / kTR;
+  a.U = (long long)a.RT * a.C;
+  switch (M) {
+    case 1: return launch_tc<1, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 2: return launch_tc<2, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 3: return launch_tc<3, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 4: return launch_tc<4, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 5: return launch_tc<5, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 6: return launch_tc<6, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    case 7: return launch_tc<7, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
+    default: return launch_tc<8, 4, false, true>(mp, a, stream, grid_cap, max_ctas_per_sm, launched, max_blocks);
   }
 }
 

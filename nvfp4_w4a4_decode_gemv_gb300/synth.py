@@ -28,6 +28,13 @@ def gemv_bytes(M: int, N: int, K: int) -> int:
     return N * K // 2 + N * K // 16 + M * K // 2 + M * K // 16 + 8 + 4 * M * N
 
 
+def quantize_gemv_bytes(M: int, N: int, K: int) -> int:
+    """Algorithmic HBM bytes of one quantize-and-multiply call: weight codes +
+    scales, the BF16 activation, the weight's global scale and the FP32 output
+    (the quantized activation need not leave the chip)."""
+    return N * K // 2 + N * K // 16 + 2 * M * K + 4 + 4 * M * N
+
+
 def quantize_bytes(M: int, K: int) -> int:
     """Algorithmic bytes of one activation quantization: BF16 in, NVFP4 out."""
     return M * K * 2 + M * K // 2 + M * K // 16 + 4

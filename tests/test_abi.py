@@ -106,6 +106,22 @@ def test_packed_weight_argument_errors(lib):
     assert lib.nvfp4_gemv_smallm_packed(*args(1, 256, 256, w=FAKE + 8)) == 3
 
 
+def test_quantize_gemv_argument_errors(lib):
+    base = lib.nvfp4_gemv_workspace_bytes(8, 5120, 5120)
+    need = lib.nvfp4_quantize_gemv_workspace_bytes(8, 5120, 5120)
+    assert need >= base + 8 * 5120 // 2 + 8 * 5120 // 16 + 4          # room for the two-launch route
+    assert lib.nvfp4_quantize_gemv_workspace_bytes(9, 5120, 5120) == 0
+    assert lib.nvfp4_quantize_gemv_workspace_bytes(1, 5120, 5000) == 0
+    args = lambda M, N, K, x=FAKE, xg=None, wsb=1 << 30: (x, M, FAKE, FAKE, N, K, FAKE, xg, FAKE, wsb, None)
+    assert lib.nvfp4_quantize_gemv_packed(*args(0, 256, 256)) == 4
+    assert lib.nvfp4_quantize_gemv_packed(*args(9, 256, 256)) == 4
+    assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 300)) == 2
+    assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 256, x=None)) == 1
+    assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 256, x=FAKE + 8)) == 3
+    assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 256, xg=FAKE + 2)) == 3
+    assert lib.nvfp4_quantize_gemv_packed(*args(8, 5120, 5120, wsb=need - 1)) == 2
+
+
 def test_reset_argument_errors(lib):
     from nvfp4_w4a4_decode_gemv_gb300._lib import ResetParams
     p = ResetParams(0.6, 0.3, 1.0, 8)
