@@ -44,12 +44,13 @@ from nvfp4_w4a4_decode_gemv_gb300 import synth  # noqa: E402
 METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Qwen3 shapes"
 
 # DRAM traffic of the tensor-core GEMV from one ncu capture of this bench (the
-# launch list in profiles/launch_list_qwen3-32b_sweep_tc.md): mean read + write
-# bytes per GEMV launch over the Qwen3-32B sweep, valid only while the kernel
+# launch list in profiles/launch_list_qwen3-32b_sweep_tc.md): read + write
+# bytes per launch of the GEMV on quantized activations, averaged over the 32
+# (M, projection) calls of the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "c635ba148b62142a5e5ddecaeff6ea0e949bd58ac5f1280fa9eda49cf74b1662",
-                  "workload": "qwen3-32b", "bytes_per_launch": 68995654}
+                  "sha256": "5703895d4d1d958ec6d3c70b32c98928ed6a6466847c38532d94a248d026f3e3",
+                  "workload": "qwen3-32b", "bytes_per_launch": 69007170}
 
 
 def recorded_traffic(workload):
