@@ -243,21 +243,43 @@ NVFP4_DEVINL void read_acc(uint32_t tmem, int quad, int d, uint64_t* acc_empty_d
 
 NVFP4_DEVINL void qx_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kQThreads) : "memory"); }
 
-// The activation quantizer inside the GEMV (QX), run by warps 2-9 of every CTA.
-// Each CTA reads the whole BF16 activation for its maximum -- so no CTA waits
-// for another -- and quantizes the nres chunks it uses (chunk0, chunk0 + 1,
-// ... mod C) into the resident atoms and scale rows, with the same recipe and
-// roundings as the quantizer kernels (quant_block), so the codes are the ones
-// nvfp4_quantize_act writes.  The blocks a thread quantizes (the first kQR,
-// which is all of them for the shapes the host sends here) are loaded together
-// with the maximum's pass, so the activation crosses L2 once after the wait.
-// Returns the global scale amax / 2688.
-constexpr int kQR = 2;                       // blocks a quantizing thread holds in registers
+// The activation quantizer inside the GEMV (QX).
+// * qx_amax (warps 2-9): every CTA reads the whole BF16 activation for the
+//   tensor maximum -- so no CTA waits for another -- and forms the global
+//   scale amax / 2688 as nvfp4_quantize_act does.
+// * qx_quant_chunk (warps 6-9, the epilogue warps, idle until the first tile
+//   ends): the nres chunks the CTA uses (chunk0, chunk0 + 1, ... mod C), warp
+//   6 + q taking chunks q, q + 4, ..., each into its resident atom and scale
+//   row with the recipe's roundings (quant_block), so the codes are the ones
+//   nvfp4_quantize_act writes.  Chunk i's mbarrier completes when its codes
+//   are in place; the scale writers wait for it before the chunk's first
+//   unit, so only the first chunk sits on the path to the first MMA, and the
+//   others are quantized while the weights stream.  (Chunk 0 shared by all
+//   eight warps, one block a thread, measured slower: 0.538 against 0.529 ms
+//   for the sweep's step.)
+constexpr int kQF = 4;                       // blocks of one chunk a quantizing lane holds (M * 16 / 32)
 
+// Chunk i's blocks of x: lane l holds blocks l, l + 32, ... of the chunk's
+// M x 16 (block j of token m is number 16 m + j), two 16-byte pieces each.
 template <int M>
-NVFP4_DEVINL void qx_store_block(uint8_t* res, uint8_t* res_sc, int rb, const uint4 (&raw)[2], float g) {
-  const int i = rb / (16 * M), m = (rb >> 4) % M, j = rb & 15;
-  const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+NVFP4_DEVINL void qx_load_chunk(const TcArgs& a, int i, int chunk0, int lane, uint4 (&r)[kQF][2]) {
+  int c = chunk0 + i;
+  if (c >= a.C) c -= a.C;
+#pragma unroll
+  for (int u = 0; u < kQF; ++u) {
+    const int b = lane + 32 * u;
+    if (b < M * 16) {
+      const uint4* p = reinterpret_cast<const uint4*>(a.x + (size_t)(b >> 4) * a.K + (size_t)c * kChunk +
+                                                      (size_t)(b & 15) * 16);
+      r[u][0] = __ldcg(p);
+      r[u][1] = __ldcg(p + 1);
+    }
+  }
+}
+
+// Block j of token m of resident chunk i (16 BF16 values) into its atom and scale row.
+NVFP4_DEVINL void qx_quant_block(uint8_t* res, uint8_t* res_sc, int i, int m, int j, const uint4 (&r)[2], float g) {
+  const uint32_t w[8] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w};
   float v[16];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -272,25 +294,24 @@ NVFP4_DEVINL void qx_store_block(uint8_t* res, uint8_t* res_sc, int rb, const ui
   res_sc[i * 256 + m * 16 + j] = static_cast<uint8_t>(sc);
 }
 
-// Block rb = (i, m, j) of the resident chunks (block j of 16 fastest, then
-// token m, then chunk i): its two 16-byte pieces of x.
 template <int M>
-NVFP4_DEVINL void qx_load_block(const TcArgs& a, int rb, int chunk0, uint4 (&raw)[2]) {
-  const int i = rb / (16 * M), m = (rb >> 4) % M, j = rb & 15;
-  int c = chunk0 + i;
-  if (c >= a.C) c -= a.C;
-  const uint4* p = reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + (size_t)c * kChunk + j * 16);
-  raw[0] = __ldcg(p);
-  raw[1] = __ldcg(p + 1);
+NVFP4_DEVINL void qx_quant_chunk(uint8_t* res, uint8_t* res_sc, int i, int lane, const uint4 (&r)[kQF][2],
+                                 float g) {
+#pragma unroll
+  for (int u = 0; u < kQF; ++u) {
+    const int b = lane + 32 * u;
+    if (b < M * 16) qx_quant_block(res, res_sc, i, b >> 4, b & 15, r[u], g);
+  }
 }
 
+// Warps 2-9.  Warps 6-9 also load the first chunk they quantize (into
+// `first`) right after the dependency wait, with the maximum's loads.
 template <int M>
-NVFP4_DEVINL float quantize_resident(const TcArgs& a, uint8_t* res, uint8_t* res_sc, uint32_t* s_wmax, int nres,
-                                     int chunk0) {
+NVFP4_DEVINL float qx_amax(const TcArgs& a, uint8_t* res, uint8_t* res_sc, uint32_t* s_wmax, int nres, int chunk0,
+                           uint4 (&first)[kQF][2]) {
   const int qt = (int)threadIdx.x - 64;      // 0 .. 255
-  const int lane = threadIdx.x & 31;
-  const int K = a.K;
-  const int xbytes = M * K * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int xbytes = M * a.K * 2;
   // While the preceding kernel may still run: zero the atoms (rows >= M and
   // the trailing atom stay zero) and the scale rows, and ask L2 for x.
   for (int o = qt * 16; o < (nres + 1) * 1024; o += kQThreads * 16)
@@ -299,17 +320,7 @@ NVFP4_DEVINL float quantize_resident(const TcArgs& a, uint8_t* res, uint8_t* res
     *reinterpret_cast<uint4*>(res_sc + o) = make_uint4(0u, 0u, 0u, 0u);
   for (int o = qt * 128; o < xbytes; o += kQThreads * 128) prefetch_l2(reinterpret_cast<const uint8_t*>(a.x) + o);
   griddep_wait();                            // x comes from the preceding kernel
-  const int nrb = nres * M * 16;
-  uint4 held[kQR][2];
-#pragma unroll
-  for (int u = 0; u < kQR; ++u) {
-    const int rb = qt + u * kQThreads;
-    if (rb < nrb) {
-      qx_load_block<M>(a, rb, chunk0, held[u]);
-    } else {
-      held[u][0] = held[u][1] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
+  if (warp >= 6 && warp - 6 < nres) qx_load_chunk<M>(a, warp - 6, chunk0, lane, first);
   // max |x| over the tensor.  For BF16 magnitudes (sign cleared) the unsigned
   // order of the bit patterns is the order of the values, so the maximum is
   // taken on the bits, two halves at a time.
@@ -334,24 +345,11 @@ NVFP4_DEVINL float quantize_resident(const TcArgs& a, uint8_t* res, uint8_t* res
   mx = max(mx & 0xFFFFu, mx >> 16);
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) s_wmax[qt >> 5] = mx;
-  qx_barrier();
+  qx_barrier();                              // also orders the zeroing before every code store
   uint32_t m8 = lane < kQThreads / 32 ? s_wmax[lane] : 0u;
   m8 = __reduce_max_sync(0xffffffffu, m8);
   const float g = __fdiv_rn(__uint_as_float(m8 << 16), 2688.0f);   // 448 * 6
   if (blockIdx.x == 0 && qt == 0 && a.xg_out) *a.xg_out = g;
-#pragma unroll
-  for (int u = 0; u < kQR; ++u) {
-    const int rb = qt + u * kQThreads;
-    if (rb < nrb) qx_store_block<M>(res, res_sc, rb, held[u], g);
-  }
-  for (int rb = qt + kQR * kQThreads; rb < nrb; rb += kQThreads) {    // beyond what the registers hold
-    uint4 raw[2];
-    qx_load_block<M>(a, rb, chunk0, raw);
-    qx_store_block<M>(res, res_sc, rb, raw, g);
-  }
-  // The MMA reads the atoms through the async proxy.
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  qx_barrier();
   return g;
 }
 
@@ -373,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   uint64_t* empty = sf_ready + S;
   uint64_t* acc_full = empty + S;           // [0], [1]: alternating tiles; [2]: the CTA's last tile
   uint64_t* acc_empty = acc_full + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* chunk_ready = acc_empty + 2;                // QX: [kMaxRes] resident chunk i quantized
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(chunk_ready + (QX ? kMaxRes : 0));
   uint32_t* s_wmax = tmem_slot + 4;                     // QX: the quantizing warps' maxima
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     }
     for (int d = 0; d < 3; ++d) mbar_init(&acc_full[d], 1);
     for (int d = 0; d < 2; ++d) mbar_init(&acc_empty[d], 4);
+    if (QX)
+      for (int i = 0; i < kMaxRes; ++i) mbar_init(&chunk_ready[i], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -409,10 +410,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
   const int C = a.C;
   const int tile0 = (int)(u0 / C), chunk0 = (int)(u0 % C);
 
-  // QX: warps 2-9 quantize the activation chunks first; the scale writers'
-  // first arrival on sf_ready (which the MMA waits for) follows it.
+  // QX: warps 2-9 find the global scale; then warps 6-9 quantize the chunks,
+  // each signalling its chunk's mbarrier, and go on to the epilogue.  The
+  // scale writers wait for a chunk before its first unit, so their arrival on
+  // sf_ready (which the MMA waits for) follows the chunk's codes.
   float qg = 0.0f;
-  if (QX && warp >= 2 && nunits > 0) qg = quantize_resident<M>(a, res, res_sc, s_wmax, nres, chunk0);
+  if (QX && warp >= 2 && nunits > 0) {
+    uint4 first[kQF][2];
+    qg = qx_amax<M>(a, res, res_sc, s_wmax, nres, chunk0, first);
+    if (warp >= 6) {
+      for (int i = warp - 6; i < nres; i += 4) {
+        if (i != warp - 6) qx_load_chunk<M>(a, i, chunk0, lane, first);
+        qx_quant_chunk<M>(res, res_sc, i, lane, first, qg);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMA reads the atom via the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&chunk_ready[i]);
+      }
+    }
+  }
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -554,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
     int ri = 0;                                        // QX: resident chunk of the unit
     for (int k = 0; k < (BF ? 0 : nunits); ++k) {     // BF16 has no scales to place
       if (!mbar_wait_warp(&full[s], phase)) break;
+      if (QX && k < nres && !mbar_wait_warp(&chunk_ready[ri], 0)) break;   // the unit's chunk, on its first use
       const uint8_t* slot = smem + s * kSl;
       const uint4 sa = *reinterpret_cast<const uint4*>(slot + kOffSA + row * 16);
       const uint32_t ta = ta0 + 32u * s;
@@ -647,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tc_kernel(const __grid_const
 
 template <int S, bool QX = false>
 constexpr size_t tc_smem_bytes() {
-  return QX ? (size_t)S * kSlotQX + kResCodeBytes + kResScaleBytes + 1024 + (3 * S + 5) * sizeof(uint64_t) + 64
+  return QX ? (size_t)S * kSlotQX + kResCodeBytes + kResScaleBytes + 1024 + (3 * S + 5 + kMaxRes) * sizeof(uint64_t) + 64
             : (size_t)S * kSlot + 1024 + (3 * S + 5) * sizeof(uint64_t) + 16;
 }
 
