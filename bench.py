@@ -49,8 +49,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # (M, projection) calls of the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "5703895d4d1d958ec6d3c70b32c98928ed6a6466847c38532d94a248d026f3e3",
-                  "workload": "qwen3-32b", "bytes_per_launch": 69007170}
+                  "sha256": "be692e5da336bbb2530f0683c94a7cec108b79b87ce5c080c7948c43077b15f1",
+                  "workload": "qwen3-32b", "bytes_per_launch": 69002460}
 
 
 def recorded_traffic(workload):
