@@ -31,16 +31,19 @@ def _guarded_nvfp4(rows, K):
 
 
 # ---- 1. a bounded wait that runs out -------------------------------------------------------
-@pytest.mark.parametrize("packed", [False, True])
-def test_gemv_fixup_wait_runs_out_and_is_reported(packed):
+@pytest.mark.parametrize("path", ["rowmajor", "packed", "one-call"])
+def test_gemv_fixup_wait_runs_out_and_is_reported(path):
     M, N, K = 2, 1000, 768            # 24 units: one per CTA, every tile split three ways
     x, w = synth.activations(M, K, 31), synth.weights(N, K, 32)
     X, W = api.nvfp4_quantize_act(x.cuda()), api.nvfp4_quantize_act(w.cuda())
-    Wp = api.nvfp4_pack_weights(W) if packed else W
-    gemv = (lambda ws: api.nvfp4_gemv_smallm_packed(X, Wp, workspace=ws)) if packed else \
-        (lambda ws: api.nvfp4_gemv_smallm(X, Wp, workspace=ws))
+    Wp = api.nvfp4_pack_weights(W) if path != "rowmajor" else W
+    xd = x.cuda()
+    gemv = {"rowmajor": lambda ws: api.nvfp4_gemv_smallm(X, Wp, workspace=ws),
+            "packed": lambda ws: api.nvfp4_gemv_smallm_packed(X, Wp, workspace=ws),
+            # M = 2: the GEMV that quantizes its activation, one launch
+            "one-call": lambda ws: api.nvfp4_quantize_gemv_packed(xd, Wp, workspace=ws)}[path]
     wsp = api.GemvWorkspace()
-    ws = wsp.get(M, N, K)
+    ws = wsp.get_bytes(api.nvfp4_quantize_gemv_workspace_bytes(M, N, K))
     torch.cuda.synchronize()
     assert api.device_status() == 0
     L = lib()
@@ -134,6 +137,24 @@ def test_gemv_canaries(M, N, K, path):
     y.check("y")
     xq, xs, xg = Q.quantize_bf16(bits(x))
     wq, wsc, wg = Q.quantize_bf16(bits(w))
+    y_ref, bound = Q.gemv(xq, xs, xg, wq, wsc, wg)
+    assert_within(to_np(y.t), y_ref, bound)
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (3, 129, 256), (2, 129, 25856), (8, 1000, 768)])
+def test_quantize_gemv_canaries(M, N, K):
+    """nvfp4_quantize_gemv_packed into guarded y and global-scale buffers (one
+    launch for M <= 3 except where M * K is too large, two launches above)."""
+    x, w = synth.activations(M, K, seed=N + K + 2), synth.weights(N, K, seed=N + K + 3)
+    P = api.nvfp4_pack_weights(api.nvfp4_quantize_act(w.cuda()))
+    y, g = Guarded((M, N), torch.float32), Guarded((1,), torch.float32)
+    api.nvfp4_quantize_gemv_packed(x.cuda(), P, y=y.t, xg_out=g.t)
+    y.check("y")
+    g.check("global scale")
+    xq, xs, xg = Q.quantize_bf16(bits(x))
+    wq, wsc, wg = Q.quantize_bf16(bits(w))
+    assert to_np(g.t)[0] == xg
     y_ref, bound = Q.gemv(xq, xs, xg, wq, wsc, wg)
     assert_within(to_np(y.t), y_ref, bound)
     assert api.device_status() == 0
