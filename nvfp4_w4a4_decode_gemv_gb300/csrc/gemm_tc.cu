@@ -563,8 +563,8 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   //    number of CTAs (T x floor(SMs / T)), else Stream-K over all SMs; a split
   //    tile's finishing CTA then merges 64 KB of partial sums per contributor
   //    at M = 128, which measured as long as about 4.5 MMA steps per 16 tokens.
-  // (Qwen3-32B at M = 128: whole tiles for qkv, o and gate_up, split tiles for
-  // down, whose 40 tiles of 100 steps would leave 112 SMs idle.)
+  // (Qwen3-32B at M = 128: whole tiles for qkv and gate_up; clusters of two
+  // for o and of three for down, whose 40 tiles would leave 112 SMs idle.)
   const long long sms = nvfp4_internal_device_sms();
   const long long tiles = (N + kTR - 1) / kTR;
   a.tiles = (int)tiles;
@@ -578,11 +578,13 @@ cudaError_t nvfp4_internal_gemm_tc(const uint8_t* xq, const uint8_t* xs, const f
   // With fewer tiles than SMs, a tile can also go to a cluster of k <= 3 CTAs
   // (k <= units a tile) whose partial sums meet in shared memory: each other
   // rank stages 64 KB at M = 128, rank 0 reads it over distributed shared
-  // memory and adds it -- measured as long as about 2 MMA steps per 16 tokens
-  // per rank.  Ties go to the larger cluster.
+  // memory and adds it -- about 1.5 MMA steps per 16 tokens per rank, as
+  // fitted to whole calls at M = 128 (time = fixed + steps x 0.25 us: o on
+  // two ranks and down on three both gave 1.5-1.6).  Ties go to the larger
+  // cluster.
   long long best_k = 1, cost_cluster = -1;
   for (long long k = 2; k <= kMaxClusterK && tiles * k <= sms && k <= a.C; ++k) {
-    const long long c = (a.C + k - 1) / k + (k - 1) * 2 * ((M + 15) / 16);
+    const long long c = (a.C + k - 1) / k + (k - 1) * 3 * ((M + 15) / 16) / 2;
     if (cost_cluster < 0 || c <= cost_cluster) {
       cost_cluster = c;
       best_k = k;
