@@ -609,82 +609,138 @@ def cold_per_call(calls, weights, ws, R=200, trials=7):
 def run_e2e(args, calls, weights, ws):
     """The step end to end through the public API, with the step's activations
     arriving in one copy from pinned host memory and its outputs leaving in one
-    copy to pinned host memory, both inside the timed region.  `value`: the
-    step's API calls (one per projection on the one-call route, two on the
-    two-call route) captured once in a CUDA graph (as a decode loop runs
-    them) and replayed between the two copies; `eager`: the same calls issued
-    one by one from Python each step.  (One copy per M group on a second
-    stream, overlapped with the other groups' compute, measured slower: 1.21
-    against 0.74 ms per step.)"""
+    copy to pinned host memory, every step's copies inside the timed region.
+    The step's API calls (one per projection on the one-call route, two on the
+    two-call route) are captured once in a CUDA graph, as a decode loop runs
+    them.  `value`: two sets of device buffers and three streams, so that
+    step i's copies overlap steps i - 1 and i + 1's compute (copy in, compute
+    and copy out of one step stay ordered by events, and a set is reused only
+    after its previous step's copy out); `serial`: copy in, replay, copy out
+    on one stream; `eager`: the same calls issued one by one from Python each
+    step, serially.  (One copy per M group on a second stream, overlapped with
+    the other groups' compute, measured slower: 1.21 against 0.74 ms per step.)"""
     from nvfp4_w4a4_decode_gemv_gb300 import api
     dev = calls[0]["x"].device
-    # one arena per direction; every piece is a multiple of 512 bytes, so each
-    # view stays 16-byte aligned
+    # one arena per direction and buffer set; every piece is a multiple of 512
+    # bytes, so each view stays 16-byte aligned
     x_sizes = [c["x"].numel() for c in calls]
     y_sizes = [c["y"].numel() for c in calls]
     host_x = torch.cat([c["x"].reshape(-1).cpu() for c in calls]).pin_memory()
-    dev_xa = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
-    dev_ya = torch.empty(sum(y_sizes), dtype=torch.float32, device=dev)
-    host_y = torch.empty(sum(y_sizes), dtype=torch.float32).pin_memory()
-    dev_x = [v.view(c["x"].shape) for v, c in zip(torch.split(dev_xa, x_sizes), calls)]
-    dev_y = [v.view(c["y"].shape) for v, c in zip(torch.split(dev_ya, y_sizes), calls)]
+    sets = []
+    for _ in range(2):
+        xa = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
+        ya = torch.empty(sum(y_sizes), dtype=torch.float32, device=dev)
+        hy = torch.empty(sum(y_sizes), dtype=torch.float32).pin_memory()
+        xv = [v.view(c["x"].shape) for v, c in zip(torch.split(xa, x_sizes), calls)]
+        yv = [v.view(c["y"].shape) for v, c in zip(torch.split(ya, y_sizes), calls)]
+        sets.append((xa, ya, hy, xv, yv))
 
     route = args.route if args.weights == "packed" else "two-call"
 
-    def compute():
+    def compute(b):
+        _, _, _, xv, yv = sets[b]
         for j, c in enumerate(calls):
-            project(api, c, weights[c["name"]], ws, route, x=dev_x[j], y=dev_y[j])
+            project(api, c, weights[c["name"]], ws, route, x=xv[j], y=yv[j])
 
-    def check():
-        for j, c in enumerate(calls):        # the arena path computes what the per-call buffers hold
-            if not torch.equal(dev_y[j], c["y"]):
+    expected = torch.cat([c["y"].reshape(-1) for c in calls]).cpu()
+
+    def check(bufs):
+        for b in bufs:
+            _, ya, hy, _, _ = sets[b]
+            if not torch.equal(ya.cpu(), expected):
                 raise RuntimeError("end-to-end step disagrees with the device-resident step")
-        if not torch.equal(host_y, dev_ya.cpu()):
-            raise RuntimeError("end-to-end outputs did not all reach the host")
+            if not torch.equal(hy, expected):
+                raise RuntimeError("end-to-end outputs did not all reach the host")
 
-    stream = torch.cuda.Stream()
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     step_bytes = sum(c["qg_bytes"] if route == "one-call" else c["gemv_bytes"] + c["q_bytes"] for c in calls)
     out = {}
-    with torch.cuda.stream(stream):
-        dev_xa.copy_(host_x, non_blocking=True)
-        for _ in range(3):
-            compute()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            compute()
-        for mode in ("eager", "graph"):
-            def step():
-                dev_xa.copy_(host_x, non_blocking=True)
-                if mode == "graph":
-                    g.replay()
-                else:
-                    compute()
-                host_y.copy_(dev_ya, non_blocking=True)
-
-            for _ in range(max(3, args.warmup)):
-                step()
-            stream.synchronize()
-            check()
-            host_y.zero_()
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record()
-            for _ in range(args.steps):
-                step()
-            t1.record()
-            t1.synchronize()
-            check()
-            ms = t0.elapsed_time(t1)
-            out[mode] = {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                         "ms_per_step": round(ms / args.steps, 4)}
-    del g
+    graphs = []
+    with torch.cuda.stream(s_comp):
+        for b in range(2):
+            sets[b][0].copy_(host_x, non_blocking=True)
+            for _ in range(3):
+                compute(b)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s_comp):
+                compute(b)
+            graphs.append(g)
     torch.cuda.synchronize()
-    return {"value": out["graph"]["value"], "unit": "GB/s", "ms_per_step": out["graph"]["ms_per_step"],
+
+    def timed(run_steps, first, last):
+        for _ in range(max(3, args.warmup)):
+            run_steps(1)
+        torch.cuda.synchronize()
+        for b in range(2):
+            sets[b][2].zero_()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(first):
+            t0.record()
+        run_steps(args.steps)
+        with torch.cuda.stream(last):
+            t1.record()
+        t1.synchronize()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1)
+        return {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(ms / args.steps, 4)}
+
+    # serial: one stream, set 0 (eager: the calls from Python; graph: replay)
+    for mode in ("eager", "serial"):
+        def run_serial(n, mode=mode):
+            xa, ya, hy, _, _ = sets[0]
+            with torch.cuda.stream(s_comp):
+                for _ in range(n):
+                    xa.copy_(host_x, non_blocking=True)
+                    if mode == "serial":
+                        graphs[0].replay()
+                    else:
+                        compute(0)
+                    hy.copy_(ya, non_blocking=True)
+        out[mode] = timed(run_serial, s_comp, s_comp)
+        check([0])
+
+    # pipelined: step i on set i % 2; its copy in waits for the set's previous
+    # compute, its compute for its copy in and the set's previous copy out
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_comp = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+    for b in range(2):
+        for ev in (ev_comp[b], ev_out[b]):
+            with torch.cuda.stream(s_comp):
+                ev.record()
+    step_no = [0]
+
+    def run_pipelined(n):
+        for _ in range(n):
+            b = step_no[0] % 2
+            step_no[0] += 1
+            xa, ya, hy, _, _ = sets[b]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_comp[b])
+                xa.copy_(host_x, non_blocking=True)
+                ev_in[b].record()
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[b])
+                s_comp.wait_event(ev_out[b])
+                graphs[b].replay()
+                ev_comp[b].record()
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                hy.copy_(ya, non_blocking=True)
+                ev_out[b].record()
+    out["pipelined"] = timed(run_pipelined, s_in, s_out)
+    check([0, 1])
+    del graphs
+    torch.cuda.synchronize()
+    return {"value": out["pipelined"]["value"], "unit": "GB/s", "ms_per_step": out["pipelined"]["ms_per_step"],
             "h2d_bytes_per_step": int(host_x.numel() * host_x.element_size()),
-            "d2h_bytes_per_step": int(host_y.numel() * host_y.element_size()),
+            "d2h_bytes_per_step": int(sets[0][2].numel() * sets[0][2].element_size()),
             "method": f"per step: pinned host->device copy of the activations, the step's {len(calls)} projections "
                       f"({route} route; API calls captured once in a CUDA graph, replayed), device->host copy of "
-                      f"all outputs",
-            "eager": out["eager"]}
+                      f"all outputs; two buffer sets on three streams so one step's copies overlap its neighbours' "
+                      f"compute",
+            "serial": out["serial"], "eager": out["eager"]}
 
 
 def decode_stage_times(st, stream, reps=20):
