@@ -49,8 +49,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # (M, projection) calls of the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "be692e5da336bbb2530f0683c94a7cec108b79b87ce5c080c7948c43077b15f1",
-                  "workload": "qwen3-32b", "bytes_per_launch": 69002460}
+                  "sha256": "52e32bd04f2d78fa9dcf604ee9ca2ad67c30c36b6d9e5887dd8568d06c59f002",
+                  "workload": "qwen3-32b", "bytes_per_launch": 69015044}
 
 
 def recorded_traffic(workload):
@@ -225,14 +225,11 @@ def project(api, c, w, ws, route, x=None, y=None):
     return gemv_call(api, c, w, ws, y=y)
 
 
-def one_launch(M, N, K, sms=152):
-    """Whether nvfp4_quantize_gemv_packed runs as one launch for this shape, by
-    the library's default rule (M <= 3, M * K <= 65536, a CTA's chunks <= 24
-    and its blocks <= 1024); used only to count launches."""
-    C, U = K // 256, -(-N // 128) * (K // 256)
-    G = min(2 * sms, U)
-    res = min(-(-U // G), C)
-    return M <= 3 and M * K <= 65536 and res <= 24 and res * M * 16 <= 1024
+def one_launch(M, N, K):
+    """Whether nvfp4_quantize_gemv_packed runs this shape as one launch (the
+    library's answer); used to count launches."""
+    from nvfp4_w4a4_decode_gemv_gb300 import api
+    return api.nvfp4_quantize_gemv_launches(M, N, K) == 1
 
 def build_problem(shapes, Ms, rank, only=None, packed=True):
     from nvfp4_w4a4_decode_gemv_gb300 import api

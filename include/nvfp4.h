@@ -256,6 +256,13 @@ nvfp4_status nvfp4_gemv_smallm_packed(const uint8_t* xq, const uint8_t* xs, cons
  */
 size_t nvfp4_quantize_gemv_workspace_bytes(int M, int N, int K);
 
+/*
+ * How nvfp4_quantize_gemv_packed runs a shape on the current device: 1 (one
+ * launch), 2 (the quantizer, then the GEMV), 0 for a shape it rejects, -1
+ * when the device cannot be queried.  No launch, no synchronization.
+ */
+int nvfp4_quantize_gemv_launches(int M, int N, int K);
+
 nvfp4_status nvfp4_quantize_gemv_packed(const uint16_t* x_bf16, int M, const uint8_t* wpacked,
                                         const float* wg, int N, int K, float* y, float* xg_out,
                                         void* workspace, size_t workspace_bytes, cudaStream_t stream);

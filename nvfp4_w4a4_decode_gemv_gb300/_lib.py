@@ -53,6 +53,7 @@ SIGNATURES = {
     "nvfp4_pack_weights": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_sz, _c_p]),
     "nvfp4_gemv_smallm_packed": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_quantize_gemv_workspace_bytes": (_c_sz, [_c_i, _c_i, _c_i]),
+    "nvfp4_quantize_gemv_launches": (_c_i, [_c_i, _c_i, _c_i]),
     "nvfp4_quantize_gemv_packed": (_c_i, [_c_p, _c_i, _c_p, _c_p, _c_i, _c_i, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "nvfp4_bf16_gemv": (_c_i, [_c_p, _c_i, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "nvfp4_bf16_gemv_workspace_bytes": (ctypes.c_size_t, [_c_i, _c_i, _c_i]),

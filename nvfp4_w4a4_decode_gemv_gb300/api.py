@@ -14,7 +14,8 @@ __all__ = [
     "nvfp4_quantize_act", "nvfp4_quantize_f32", "nvfp4_silu_mul_quantize", "nvfp4_gemv_smallm",
     "nvfp4_gemv_smallm_cudacore", "DEVERR_FLAG_TIMEOUT", "nvfp4_gemm_packed", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemv_workspace_bytes", "nvfp4_packed_weight_bytes", "nvfp4_pack_weights", "nvfp4_gemv_smallm_packed",
-    "NVFP4PackedWeight", "nvfp4_quantize_gemv_packed", "nvfp4_quantize_gemv_workspace_bytes", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
+    "NVFP4PackedWeight", "nvfp4_quantize_gemv_packed", "nvfp4_quantize_gemv_workspace_bytes",
+    "nvfp4_quantize_gemv_launches", "nvfp4_bf16_gemv", "nvfp4_bf16_gemv_tc", "nvfp4_bf16_gemv_workspace_bytes",
     "nvfp4_rms_norm_bf16", "nvfp4_rms_norm_quantize", "nvfp4_f32_to_bf16",
     "reset_state_bytes",
     "reset_state_init", "reset_workspace_bytes", "reset_sample", "reset_sample_noalloc", "device_status", "GemvWorkspace",
@@ -198,6 +199,11 @@ def nvfp4_gemv_smallm_packed(x: NVFP4Tensor, w: NVFP4PackedWeight, y: torch.Tens
 
 def nvfp4_quantize_gemv_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(lib().nvfp4_quantize_gemv_workspace_bytes(M, N, K))
+
+
+def nvfp4_quantize_gemv_launches(M: int, N: int, K: int) -> int:
+    """1 or 2: how nvfp4_quantize_gemv_packed runs the shape; 0 invalid shape, -1 no device."""
+    return int(lib().nvfp4_quantize_gemv_launches(M, N, K))
 
 
 def nvfp4_quantize_gemv_packed(x_bf16: torch.Tensor, w: NVFP4PackedWeight, y: torch.Tensor | None = None,

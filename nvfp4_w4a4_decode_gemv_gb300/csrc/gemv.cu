@@ -511,6 +511,8 @@ cudaError_t nvfp4_internal_quantize_gemv_tc(const uint16_t* x, int M, const uint
                                             int K, float* y, float* xg_out, unsigned int* records, int grid_cap,
                                             int max_ctas_per_sm, long long max_blocks, cudaStream_t stream,
                                             bool* launched);
+cudaError_t nvfp4_internal_quantize_gemv_one_launch(int M, int N, int K, int grid_cap, int max_ctas_per_sm,
+                                                    long long max_blocks, bool* one);
 size_t nvfp4_internal_packed_bytes(int N, int K);
 cudaError_t nvfp4_internal_pack_weights(const uint8_t* wq, const uint8_t* ws, int N, int K, uint8_t* packed,
                                         cudaStream_t stream);
@@ -692,6 +694,17 @@ QgLayout qg_layout(int M, int N, int K) {
 extern "C" size_t nvfp4_quantize_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
   return qg_layout(M, N, K).total;
+}
+
+extern "C" int nvfp4_quantize_gemv_launches(int M, int N, int K) {
+  if (M < 1 || M > kMaxM || N < 1 || N > kMaxN || K < kChunk || (K % kChunk) != 0) return 0;
+  if (!(M <= qgemv_max_m() && (long long)M * K <= (long long)qgemv_max_mk())) return 2;
+  if (nvfp4_internal_check_device() != NVFP4_OK) return -1;
+  bool one = false;
+  if (nvfp4_internal_quantize_gemv_one_launch(M, N, K, gemv_grid_cap(), kMaxCtasPerSm, qgemv_max_blocks(), &one) !=
+      cudaSuccess)
+    return -1;
+  return one ? 1 : 2;
 }
 
 extern "C" nvfp4_status nvfp4_quantize_gemv_packed(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg,

@@ -739,25 +739,37 @@ void nvfp4_internal_test_gemv_fault(unsigned int flag_spin_limit, int drop_recor
 uint32_t nvfp4_internal_test_flag_spins() { return g_test_flag_spins.load(std::memory_order_relaxed); }
 int nvfp4_internal_test_drop_records() { return g_test_drop_records.load(std::memory_order_relaxed); }
 
-// Launches the kernel; with QX, only when no CTA has more than kMaxRes
-// activation chunks to hold (*launched = false otherwise, nothing launched).
-template <int M, int S, bool BF = false, bool QX = false>
-static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm,
-                             bool* launched = nullptr, long long qx_max_blocks = 0) {
-  cudaError_t e = cudaSuccess;
-  if (launched) *launched = false;
-  const int fit = tc_per_sm_fit<M, S, BF, QX>(&e);
-  if (fit == 0) return e;
+// The grid of an instance for a call (0 and *err on failure).
+template <int M, int S, bool BF, bool QX>
+static long long tc_grid(const TcArgs& a, int grid_cap, int max_ctas_per_sm, cudaError_t* err) {
+  const int fit = tc_per_sm_fit<M, S, BF, QX>(err);
+  if (fit == 0) return 0;
   const int per_sm = fit < max_ctas_per_sm ? fit : max_ctas_per_sm;
   long long G = (long long)per_sm * nvfp4_internal_device_sms();
   if (grid_cap > 0 && G > grid_cap) G = grid_cap;
   if (G > a.U) G = a.U;
   if (G > tc_grid_max()) G = tc_grid_max();  // records exist for that many CTAs
-  if (QX) {
-    const long long most_units = (a.U + G - 1) / G;          // a CTA's units: floor or ceil of U / G
-    const long long most_res = most_units < a.C ? most_units : a.C;
-    if (most_res > kMaxRes || most_res * M * 16 > qx_max_blocks) return cudaSuccess;
-  }
+  return G;
+}
+
+// With the activation quantized in the kernel: whether every CTA's chunks fit
+// its shared memory (kMaxRes) and its blocks stay within max_blocks.
+static bool qx_fits(const TcArgs& a, long long G, long long max_blocks) {
+  const long long most_units = (a.U + G - 1) / G;          // a CTA's units: floor or ceil of U / G
+  const long long most_res = most_units < a.C ? most_units : a.C;
+  return most_res <= kMaxRes && most_res * a.M * 16 <= max_blocks;
+}
+
+// Launches the kernel; with QX, only when qx_fits (*launched = false
+// otherwise, nothing launched).
+template <int M, int S, bool BF = false, bool QX = false>
+static cudaError_t launch_tc(const TcMaps& mp, TcArgs a, cudaStream_t stream, int grid_cap, int max_ctas_per_sm,
+                             bool* launched = nullptr, long long qx_max_blocks = 0) {
+  cudaError_t e = cudaSuccess;
+  if (launched) *launched = false;
+  const long long G = tc_grid<M, S, BF, QX>(a, grid_cap, max_ctas_per_sm, &e);
+  if (G == 0) return e;
+  if (QX && !qx_fits(a, G, qx_max_blocks)) return cudaSuccess;
   const uint32_t spins = g_test_flag_spins.load(std::memory_order_relaxed);
   a.flag_spins = spins ? spins : kFlagSpinLimit;
   a.drop_records = g_test_drop_records.load(std::memory_order_relaxed);
@@ -831,6 +843,41 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
 // the default ring depth.  *launched = false when a CTA would hold more than
 // kMaxRes activation chunks or quantize more than max_blocks blocks: the
 // caller then quantizes and multiplies in two launches.
+// Whether nvfp4_internal_quantize_gemv_tc would launch (the same grid and
+// limits), without launching.
+template <int M>
+static cudaError_t qx_would_launch(const TcArgs& a, int grid_cap, int max_ctas_per_sm, long long max_blocks,
+                                   bool* one) {
+  cudaError_t e = cudaSuccess;
+  const long long G = tc_grid<M, 4, false, true>(a, grid_cap, max_ctas_per_sm, &e);
+  if (G == 0) return e;
+  *one = qx_fits(a, G, max_blocks);
+  return cudaSuccess;
+}
+
+cudaError_t nvfp4_internal_quantize_gemv_one_launch(int M, int N, int K, int grid_cap, int max_ctas_per_sm,
+                                                    long long max_blocks, bool* one) {
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.C = K / kChunk;
+  a.RT = (N + kTR - 1) / kTR;
+  a.U = (long long)a.RT * a.C;
+  *one = false;
+  switch (M) {
+    case 1: return qx_would_launch<1>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 2: return qx_would_launch<2>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 3: return qx_would_launch<3>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 4: return qx_would_launch<4>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 5: return qx_would_launch<5>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 6: return qx_would_launch<6>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    case 7: return qx_would_launch<7>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+    default: return qx_would_launch<8>(a, grid_cap, max_ctas_per_sm, max_blocks, one);
+  }
+}
+
 cudaError_t nvfp4_internal_quantize_gemv_tc(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg, int N,
                                             int K, float* y, float* xg_out, unsigned int* records, int grid_cap,
                                             int max_ctas_per_sm, long long max_blocks, cudaStream_t stream,

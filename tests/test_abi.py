@@ -120,6 +120,9 @@ def test_quantize_gemv_argument_errors(lib):
     assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 256, x=FAKE + 8)) == 3
     assert lib.nvfp4_quantize_gemv_packed(*args(1, 256, 256, xg=FAKE + 2)) == 3
     assert lib.nvfp4_quantize_gemv_packed(*args(8, 5120, 5120, wsb=need - 1)) == 2
+    assert lib.nvfp4_quantize_gemv_launches(0, 256, 256) == 0
+    assert lib.nvfp4_quantize_gemv_launches(1, 256, 300) == 0
+    assert lib.nvfp4_quantize_gemv_launches(8, 5120, 5120) == 2          # M above the one-launch limit
 
 
 def test_reset_argument_errors(lib):

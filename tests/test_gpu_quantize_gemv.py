@@ -152,3 +152,14 @@ def test_one_launch_beyond_the_default_block_limit():
     env = dict(os.environ, NVFP4_QGEMV_MAX_BLOCKS="100000", NVFP4_QGEMV_MAX_M="8")
     r = subprocess.run([sys.executable, "-c", _CHILD], cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+def test_launch_query():
+    """nvfp4_quantize_gemv_launches: one launch for the Qwen3-32B shapes at M <= 3
+    (except down at M = 3, M * K above the limit), two above, 0 for bad shapes."""
+    for name, K, N in synth.QWEN3_32B:
+        for M in range(1, 9):
+            want = 1 if M <= 3 and M * K <= 65536 else 2
+            assert api.nvfp4_quantize_gemv_launches(M, N, K) == want, (name, M)
+    assert api.nvfp4_quantize_gemv_launches(1, 5120, 65536) == 2        # 34 chunks a CTA
+    assert api.nvfp4_quantize_gemv_launches(9, 5120, 5120) == 0
