@@ -49,8 +49,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # (M, projection) calls of the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "52e32bd04f2d78fa9dcf604ee9ca2ad67c30c36b6d9e5887dd8568d06c59f002",
-                  "workload": "qwen3-32b", "bytes_per_launch": 69015044}
+                  "sha256": "f28d743c8f6929e462a497112e62ccbfbd1d42892a34c49ea08e3fcd5b438c3b",
+                  "workload": "qwen3-32b", "bytes_per_launch": 69004188}
 
 
 def recorded_traffic(workload):

@@ -839,10 +839,6 @@ cudaError_t nvfp4_internal_gemv_tc(const uint8_t* xq, const uint8_t* xs, const f
   }
 }
 
-// The activation quantizer and the GEMV in one launch (QX), packed weights,
-// the default ring depth.  *launched = false when a CTA would hold more than
-// kMaxRes activation chunks or quantize more than max_blocks blocks: the
-// caller then quantizes and multiplies in two launches.
 // Whether nvfp4_internal_quantize_gemv_tc would launch (the same grid and
 // limits), without launching.
 template <int M>
@@ -878,6 +874,10 @@ cudaError_t nvfp4_internal_quantize_gemv_one_launch(int M, int N, int K, int gri
   }
 }
 
+// The activation quantizer and the GEMV in one launch (QX), packed weights,
+// the default ring depth.  *launched = false when a CTA would hold more than
+// kMaxRes activation chunks or quantize more than max_blocks blocks: the
+// caller then quantizes and multiplies in two launches.
 cudaError_t nvfp4_internal_quantize_gemv_tc(const uint16_t* x, int M, const uint8_t* wpacked, const float* wg, int N,
                                             int K, float* y, float* xg_out, unsigned int* records, int grid_cap,
                                             int max_ctas_per_sm, long long max_blocks, cudaStream_t stream,
