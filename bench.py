@@ -49,8 +49,8 @@ METRIC = "small-M NVFP4 GEMV µs/call and achieved HBM GB/s (% peak), M=1–8, Q
 # (M, projection) calls of the Qwen3-32B sweep, valid only while the kernel
 # source is the one that was measured.
 TRAFFIC_RECORD = {"source": "nvfp4_w4a4_decode_gemv_gb300/csrc/gemv_tc.cu",
-                  "sha256": "f28d743c8f6929e462a497112e62ccbfbd1d42892a34c49ea08e3fcd5b438c3b",
-                  "workload": "qwen3-32b", "bytes_per_launch": 69004188}
+                  "sha256": "16de29400665bd3139280542a6af34870d0d042fdd8ccaa7153464c7b9062020",
+                  "workload": "qwen3-32b", "bytes_per_launch": 69002212}
 
 
 def recorded_traffic(workload):

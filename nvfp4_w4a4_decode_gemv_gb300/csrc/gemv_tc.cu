@@ -42,6 +42,10 @@
 // lm_head (nvfp4_bf16_gemv_tc): `tcgen05.mma ... kind::f16` on BF16 operands,
 // units of [128 rows x 64 K] (the same 128 bytes per row as an E2M1 unit, so
 // the same swizzle, descriptor steps and ring), no scales and no output scale.
+// Instantiated with QX = true it takes the BF16 activation and quantizes it
+// itself (nvfp4_quantize_gemv_packed): the ring carries weights only, and the
+// CTA's activation chunks stay in shared memory (qx_amax and qx_quant_chunk
+// below).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
