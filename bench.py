@@ -603,7 +603,7 @@ def cold_per_call(calls, weights, ws, R=200, trials=7):
     return out
 
 
-def run_e2e(args, calls, weights, ws):
+def run_e2e(args, calls, weights, ws, world=1):
     """The step end to end through the public API, with the step's activations
     arriving in one copy from pinned host memory and its outputs leaving in one
     copy to pinned host memory, every step's copies inside the timed region.
@@ -668,6 +668,7 @@ def run_e2e(args, calls, weights, ws):
         for _ in range(max(3, args.warmup)):
             run_steps(1)
         torch.cuda.synchronize()
+        barrier(world)
         for b in range(2):
             sets[b][2].zero_()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -678,8 +679,9 @@ def run_e2e(args, calls, weights, ws):
             t1.record()
         t1.synchronize()
         torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1)
-        return {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        barrier(world)
+        ms = max_over_ranks(world, t0.elapsed_time(t1))      # the whole job: every rank's bytes, the slowest time
+        return {"value": round(aggregate_gbs(world, step_bytes, args.steps, ms), 1), "unit": "GB/s",
                 "ms_per_step": round(ms / args.steps, 4)}
 
     # serial: one stream, set 0 (eager: the calls from Python; graph: replay)
@@ -731,12 +733,12 @@ def run_e2e(args, calls, weights, ws):
     del graphs
     torch.cuda.synchronize()
     return {"value": out["pipelined"]["value"], "unit": "GB/s", "ms_per_step": out["pipelined"]["ms_per_step"],
-            "h2d_bytes_per_step": int(host_x.numel() * host_x.element_size()),
-            "d2h_bytes_per_step": int(sets[0][2].numel() * sets[0][2].element_size()),
+            "h2d_bytes_per_step": int(host_x.numel() * host_x.element_size()) * world,     # all ranks
+            "d2h_bytes_per_step": int(sets[0][2].numel() * sets[0][2].element_size()) * world,
             "method": f"per step: pinned host->device copy of the activations, the step's {len(calls)} projections "
                       f"({route} route; API calls captured once in a CUDA graph, replayed), device->host copy of "
                       f"all outputs; two buffer sets on three streams so one step's copies overlap its neighbours' "
-                      f"compute",
+                      f"compute; every rank's bytes over the slowest rank's time",
             "serial": out["serial"], "eager": out["eager"]}
 
 
@@ -1158,7 +1160,7 @@ def main():
         return
     result, calls, weights, ws = run_ours(args, world, rank)
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, calls, weights, ws)
+        result["e2e"] = run_e2e(args, calls, weights, ws, world)
     if not args.no_extras and args.workload == "qwen3-32b":
         del calls, weights, ws
         torch.cuda.synchronize()
